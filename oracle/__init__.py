@@ -1,0 +1,12 @@
+"""fp64 CPU oracle for the frame-wise Gated DeltaNet forward scan.
+
+TEST INFRASTRUCTURE ONLY.  Nothing in the product path imports this package:
+only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline /
+reference leg may import or run it.  It shares no code with the CUDA path.
+"""
+from .gdn_oracle import (  # noqa: F401
+    key_scale, out_scale, predict, residual, write, readout, frame_step,
+    scan_head, frame_fwd, transition, compose, apply_map, brute_force_states,
+    scan_hillis_steele, scan_blelloch_exclusive, fold_random_bracketing,
+    spectral_norm_sym, states_from_maps,
+)
