@@ -1,0 +1,430 @@
+"""Benchmark: frame-wise Gated DeltaNet forward tokens/s on the 961-frame,
+880-token, 20-head, d112 bf16 workload (one minute of 720p-shaped latents), with
+its fraction of the HBM roofline.
+
+One step = one gdn_frame_fwd_ex call over the whole workload (every stage of
+the path: key scale and beta, the per-frame transition terms, the D x D
+recurrence over all frames, the read-out).  Inputs are resident in HBM when
+the timed region starts and are larger than L2, so no flush is needed.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own full replica of the workload on
+its own GPU (weak scaling; the path needs no cross-GPU exchange), the ranks
+barrier around the timed region and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as dt
+import glob
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from linear_attention_video_gated_b300 import synth  # noqa: E402
+
+METRIC = "frame-GDN fwd tokens/s at 961f×880tok×20h×d112; % of roofline"
+UNIT = "tokens/s"
+
+
+# ----------------------------------------------------------------- algorithmic work
+
+def alg_bytes(wl) -> int:
+    """q, k, v read once, out written once, g and beta read once, state in and out."""
+    n = wl.B * wl.H * wl.T * wl.S * wl.D
+    return 4 * n * wl.elem_bytes + 4 * wl.B * wl.H * wl.T * (1 + wl.S) + 2 * 4 * wl.B * wl.H * wl.D * wl.D
+
+
+def alg_flops(wl) -> int:
+    """Three S x D x D contractions per frame-head (prediction, write, read-out)."""
+    return 6 * wl.B * wl.H * wl.T * wl.S * wl.D * wl.D
+
+
+def kernel_alg_bytes(name: str, wl) -> int | None:
+    """Algorithmic bytes each kernel is responsible for, per launch (one call).
+
+    gram-type kernels read k, v, beta (and g); read-out kernels read q and write
+    out; the fused kernel moves everything.  Scratch traffic is not algorithmic.
+    """
+    fh = wl.B * wl.H * wl.T
+    e = wl.elem_bytes
+    if name.endswith("_gram"):
+        return fh * (2 * wl.S * wl.D * e + 4 * wl.S + 4)
+    if name.endswith("_readout"):
+        return fh * 2 * wl.S * wl.D * e
+    if name.endswith("_fused"):
+        return alg_bytes(wl)
+    return None
+
+
+# ----------------------------------------------------------------- environment
+
+def peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+def csrc_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "linear_attention_video_gated_b300", "csrc", "*"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str, wl) -> float | None:
+    """DRAM bytes per launch from profiles/ncu_traffic.txt, if taken on the current sources.
+
+    Line format: <kernel> <dram bytes per launch> <csrc hash> <workload name>."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(p):
+        return None
+    cur = csrc_hash()
+    for line in open(p):
+        f = line.split()
+        if len(f) >= 4 and not line.startswith("#") and f[0] == kernel and f[2] == cur and f[3] == wl.name:
+            return float(f[1])
+    return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons in the background."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, bus_id: str | None):
+        self.rows = []
+        self.proc = None
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "50"]
+        if bus_id:
+            cmd += ["-i", bus_id]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                ts = dt.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f")
+            except ValueError:
+                continue
+            self.rows.append((ts, f))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: dt.datetime, t1: dt.datetime) -> dict | None:
+        rows = [f for ts, f in self.rows if t0 <= ts <= t1] or [f for _, f in self.rows[-5:]]
+        if not rows:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(f[2]) for f in rows if num(f[2]) is not None]
+        mx = [num(f[3]) for f in rows if num(f[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for f in rows for n, v in zip(names, f[6:10]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def bus_id(dev) -> str | None:
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample(wl, budget_s: float, max_heads: int | None = None, frames: int | None = None):
+    """Times the fp64 oracle on whole heads of the workload until `budget_s` of CPU
+    work.  Returns (equivalent tokens/s, cores, sample description, seconds)."""
+    from threadpoolctl import threadpool_limits
+
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    T = wl.T if frames is None else min(frames, wl.T)
+    max_heads = wl.B * wl.H if max_heads is None else max_heads
+    spent, n = 0.0, 0
+    with threadpool_limits(cores):
+        while n < max_heads and (n == 0 or spent < budget_s):
+            b, h = divmod(n, wl.H)
+            one = wl.with_(B=1, H=1)
+            hq = np.empty((1, 1, T, wl.S, wl.D), np.uint16 if wl.dtype == "bf16" else np.float32)
+            hk, hv = np.empty_like(hq), np.empty_like(hq)
+            hg = np.empty((1, 1, T), np.float32)
+            hb = np.empty((1, 1, T, wl.S), np.float32)
+            _fill_head(wl, b, h, hq, hk, hv, hg, hb)
+            cvt = (lambda a: synth.bf16_to_f32(a[0, 0])) if wl.dtype == "bf16" else (lambda a: a[0, 0])
+            q, k, v = cvt(hq), cvt(hk), cvt(hv)
+            t0 = time.perf_counter()
+            oracle.scan_head(q, k, v, hg[0, 0], hb[0, 0])
+            spent += time.perf_counter() - t0
+            n += 1
+            del one
+    tokens = n * T * wl.S / wl.H  # a token of the workload spans all H heads
+    desc = (f"{n} of {wl.B * wl.H} heads x {T} of {wl.T} frames x {wl.S} tokens (d{wl.D}) of the {wl.name} "
+            f"workload, numpy fp64; tokens counted as heads/{wl.H}")
+    return tokens / spent, cores, desc, spent
+
+
+def _fill_head(wl, b, h, hq, hk, hv, hg, hb):
+    from concurrent.futures import ThreadPoolExecutor
+    T = hq.shape[2]
+
+    def one(t):
+        for name, dst in (("q", hq), ("k", hk), ("v", hv)):
+            x = synth.frame_raw(wl, name, b, h, t)
+            dst[0, 0, t] = synth.bf16_bits(x) if wl.dtype == "bf16" else x
+        hg[0, 0, t] = synth.gate(wl, b, h, t)
+        hb[0, 0, t] = synth.beta(wl, b, h, t)
+
+    with ThreadPoolExecutor(len(os.sched_getaffinity(0))) as ex:
+        list(ex.map(one, range(T)))
+
+
+# ----------------------------------------------------------------- arms
+
+def config_of(wl, mode) -> dict:
+    return {"workload": f"{wl.name}: B={wl.B} H={wl.H} T={wl.T} S={wl.S} D={wl.D} {wl.dtype} I/O, fp32 state, "
+                        f"single call over all frames",
+            "B": wl.B, "H": wl.H, "T": wl.T, "S": wl.S, "D": wl.D,
+            "mode": {0: "sequential", 1: "prefix"}[mode],
+            "l2": f"no flush: inputs larger than L2 ({alg_bytes(wl) / 1e9:.1f} GB moved per step vs 126 MB L2)"}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    wl = synth.WORKLOADS[args.workload]
+    frames = min(wl.T, 240)
+    times = []
+    cores = len(os.sched_getaffinity(0))
+    for i in range(args.warmup + args.steps):
+        v, cores, desc, spent = oracle_sample(wl, 0.0, max_heads=1, frames=frames)
+        if i >= args.warmup:
+            times.append(spent)
+    ms = 1e3 * float(np.mean(times))
+    value = (frames * wl.S / wl.H) / (ms / 1e3)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, args.mode),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def ours_arm(args, rank, world, local_rank):
+    import torch
+
+    from linear_attention_video_gated_b300 import binding, build_lib
+    build_lib.ensure_built()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = synth.WORKLOADS[args.workload]
+    mode = args.mode
+    dtype = binding.GDN_BF16 if wl.dtype == "bf16" else binding.GDN_F32
+    tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+    hdt = torch.uint16 if wl.dtype == "bf16" else torch.float32
+
+    # inputs: generated into pinned host memory, copied once to the device
+    shape = (wl.B, wl.H, wl.T, wl.S, wl.D)
+    hq, hk, hv = (torch.empty(shape, dtype=hdt, pin_memory=True) for _ in range(3))
+    hg = torch.empty((wl.B, wl.H, wl.T), dtype=torch.float32, pin_memory=True)
+    hb = torch.empty((wl.B, wl.H, wl.T, wl.S), dtype=torch.float32, pin_memory=True)
+    synth.fill_io(wl, hq.numpy(), hk.numpy(), hv.numpy(), hg.numpy(), hb.numpy())
+    if wl.dtype == "bf16":
+        hq, hk, hv = (t.view(torch.bfloat16) for t in (hq, hk, hv))
+    q, k, v = (t.to(dev) for t in (hq, hk, hv))
+    g, beta = hg.to(dev), hb.to(dev)
+    out = torch.empty(shape, dtype=tdt, device=dev)
+    st_out = torch.empty((wl.B, wl.H, wl.D, wl.D), dtype=torch.float32, device=dev)
+    need = binding.gdn_workspace_bytes(wl.B, wl.H, wl.T, wl.S, wl.D, dtype, mode)
+    ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+
+    def step(qq=q, kk=k, vv=v, gg=g, bb=beta, oo=out, so=st_out):
+        rc = binding.gdn_frame_fwd_ex(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), gg.data_ptr(), bb.data_ptr(),
+                                      None, oo.data_ptr(), so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype,
+                                      mode, ws.data_ptr(), need, sp)
+        if rc != 0:
+            raise binding.GDNError(rc, "gdn_frame_fwd_ex")
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    rc = binding.gdn_last_error(sp)
+    if rc != 0:
+        raise binding.GDNError(rc, "warm-up")
+
+    clocks = ClockSampler(bus_id(dev))
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    binding.gdn_profile_begin()
+    w0 = dt.datetime.now()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    w1 = dt.datetime.now()
+    kstats = binding.gdn_profile_end()
+    barrier()
+    time.sleep(0.1)
+    clocks.stop()
+    clk = clocks.summary(w0, w1)
+    rc = binding.gdn_last_error(sp)
+    if rc != 0:
+        raise binding.GDNError(rc, "timed region")
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    value = wl.tokens * world / (ms / 1e3)
+    pk = peaks()
+
+    # roofline of the dominant kernel, from its own CUDA-event durations
+    dom = max(kstats.items(), key=lambda kv: kv[1][1]) if kstats else None
+    roof = None
+    if dom is not None:
+        name, (launches, tot) = dom
+        avg = tot / launches
+        ab = kernel_alg_bytes(name, wl)
+        if ab is not None:
+            ach = ab / (avg / 1e3) / 1e9
+            traffic = ncu_traffic(name, wl)
+            roof = {"bound": "hbm", "kernel": name, "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                    "frac": ach / pk["hbm_gbs"], "traffic": traffic, "alg_bytes_per_launch": ab,
+                    "avg_launch_ms": avg, "peak_source": f"{pk['source']} (MEASURED_PEAKS.json hbm_gbs)"
+                    if pk["source"] == "measured" else "fallback 6.4 TB/s"}
+    call_gbs = alg_bytes(wl) / (ms / 1e3) / 1e9
+
+    # end to end through the C ABI from pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        ho = torch.empty(shape, dtype=tdt, pin_memory=True)
+        hs = torch.empty((wl.B, wl.H, wl.D, wl.D), dtype=torch.float32, pin_memory=True)
+        n_e2e = max(2, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            for d_, h_ in ((q, hq), (k, hk), (v, hv), (g, hg), (beta, hb)):
+                d_.copy_(h_, non_blocking=True)
+            step()
+            ho.copy_(out, non_blocking=True)
+            hs.copy_(st_out, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = e0.elapsed_time(e1) / n_e2e
+        if world > 1:
+            t = torch.tensor([ems], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            ems = float(t.item())
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
+        d2h = ho.numel() * ho.element_size() + hs.numel() * hs.element_size()
+        e2e = {"value": wl.tokens * world / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": n_e2e}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v_, cores, desc, spent = oracle_sample(wl, args.cpu_seconds)
+        cpu = {"value": v_, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "seconds": spent}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+                "config": config_of(wl, mode),
+                "roofline_pct": 100.0 * call_gbs / pk["hbm_gbs"],
+                "call_achieved_gbs": call_gbs,
+                "tflops": alg_flops(wl) / (ms / 1e3) / 1e12,
+                "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
+                "gpu_launches": int(sum(n for n, _ in kstats.values())),
+                "kernels": {k_: {"launches": n, "avg_ms": t / n} for k_, (n, t) in kstats.items()}}
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="minute", choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--mode", type=int, default=0, choices=[0, 1])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        ours_arm(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+/*
+ * gdn.h -- C ABI of libgdn: the frame-wise Gated DeltaNet (GDN) forward scan on
+ * NVIDIA B300 (sm_103a).
+ *
+ * The operation (SANA-WM's frame-wise GDN sequence mixer).  Per head (b, h),
+ * for frames t = 0 .. T-1, with S tokens per frame and head dim D:
+ *
+ *     K~_t = K_t / sqrt(D*S)                                   (key scaling)
+ *     S_t  = g_t S_{t-1} + K~_t^T diag(beta_t) (V_t - g_t K~_t S_{t-1})
+ *     O_t  = Q_t S_t / sqrt(D)
+ *
+ * Sources, by page and section:
+ *   - frame-wise recurrence, one step per latent frame: bilibili SANA-WM
+ *     article, fourth key point (frame-wise Gated DeltaNet replacing most
+ *     attention blocks; decay g in the update rule);
+ *   - decay gate multiplies the previous state by a scalar; beta delta rule
+ *     writes only the residual between target and prediction; constant D x D
+ *     state; keys scaled by 1/sqrt(D*S): zhichai.net SANA-WM summary, section
+ *     "四大工程设计" item 1 (Hybrid Linear Attention -- Gated DeltaNet + Softmax);
+ *   - state carried across chunk-causal autoregressive calls: bilibili article,
+ *     second key point (chunk-causal autoregressive generator), and zhichai.net
+ *     summary, training pipeline Stage 4;
+ *   - composition of the per-frame transition maps by prefix sums, exact:
+ *     zhichai.net summary, training pipeline Stage 3 (context parallel).
+ * The pages print no equation; the 1/sqrt(D) read-out scale is not on them.
+ *
+ * Conventions for every entry point below:
+ *   - Tensors are dense, row-major, contiguous:
+ *       q, k, v, out : [B, H, T, S, D]  elements of `dtype` (GDN_F32 or GDN_BF16)
+ *       g            : [B, H, T]        float32, the per-frame decay, in [0, 1]
+ *       beta         : [B, H, T, S]     float32, the per-token delta-rule weight
+ *       state_in/out : [B, H, D, D]     float32, S[i][j]: i = key dim, j = value dim
+ *   - Every pointer is a DEVICE pointer on the current CUDA device, owned by the
+ *     caller.  The library allocates no persistent memory and keeps no state
+ *     beyond cached function attributes and one device-side status word.
+ *   - q, k, v, out, state_in, state_out and workspace must be 16-byte aligned
+ *     (TMA requirement); g and beta 4-byte aligned.  Otherwise GDN_ERR_MISALIGNED.
+ *   - Supported shapes: B >= 1, H >= 1, T >= 0, S >= 1, D in {16, 32, ..., 128}.
+ *     Other D -> GDN_ERR_UNSUPPORTED.  T = 0 copies state_in to state_out (zeros
+ *     if state_in is NULL) and touches nothing else.
+ *   - state_in == NULL means a zero initial state; state_out == NULL means the
+ *     final state is not written; state_in == state_out is allowed (the kernel
+ *     reads a head's state before it writes it).  No other overlap is allowed.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls are
+ *     asynchronous: the return code covers argument validation and launch
+ *     errors only.  Faults detected on the device (a bounded wait that timed
+ *     out) are reported by gdn_last_error().
+ *   - Returns 0 (GDN_OK) or a gdn_status_t code; gdn_status_string() names it.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  GDN_F32 = 0,  /* q, k, v, out are float32 */
+  GDN_BF16 = 1  /* q, k, v, out are bfloat16 (the state stays float32) */
+} gdn_dtype_t;
+
+typedef enum {
+  GDN_OK = 0,
+  GDN_ERR_INVALID_ARG = 1, /* NULL pointer, bad count, bad dtype/mode     */
+  GDN_ERR_UNSUPPORTED = 2, /* D not a multiple of 16 in [16, 128]         */
+  GDN_ERR_MISALIGNED = 3,  /* a pointer misses its alignment              */
+  GDN_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
+  GDN_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up          */
+  GDN_ERR_WORKSPACE = 6    /* workspace NULL or smaller than required     */
+} gdn_status_t;
+
+typedef enum {
+  /* One pass over the frames per head: per-frame transition terms are formed in
+   * parallel, the D x D recurrence runs frame by frame, outputs in parallel. */
+  GDN_MODE_SEQUENTIAL = 0,
+  /* Chunked prefix composition of the affine maps (A_t, b_t) across frames:
+   * per-chunk composed maps in parallel, a short scan over chunk boundaries,
+   * then every chunk replayed from its true initial state (zhichai.net summary,
+   * training pipeline Stage 3).  Same result up to rounding. */
+  GDN_MODE_PREFIX = 1
+} gdn_mode_t;
+
+/*
+ * gdn_frame_fwd -- the forward scan over T frames of every (b, h) head.
+ *   q, k, v   : inputs, see conventions.  K is scaled by 1/sqrt(D*S) inside.
+ *   g, beta   : decay per frame, delta-rule weight per token.
+ *   state_in  : initial state or NULL (zeros).
+ *   out       : output O_t for every frame, same dtype as q.
+ *   state_out : final state S_{T-1} or NULL.
+ *   dtype     : gdn_dtype_t.
+ * Uses GDN_MODE_SEQUENTIAL.  Its scratch memory (gdn_workspace_bytes()) is
+ * taken with cudaMallocAsync on `stream` and released with cudaFreeAsync on
+ * the same stream, so nothing persists past the call.
+ */
+int gdn_frame_fwd(const void* q, const void* k, const void* v,
+                  const float* g, const float* beta, const float* state_in,
+                  void* out, float* state_out,
+                  int B, int H, int T, int S, int D, int dtype, void* stream);
+
+/*
+ * gdn_workspace_bytes -- scratch bytes gdn_frame_fwd_ex needs for this shape,
+ * dtype and mode (0 for T = 0).  Returns 0 for arguments gdn_frame_fwd_ex would
+ * reject.  The result is a pure function of the arguments.
+ */
+size_t gdn_workspace_bytes(int B, int H, int T, int S, int D, int dtype, int mode);
+
+/*
+ * gdn_frame_fwd_ex -- gdn_frame_fwd with an explicit algorithm form and a
+ * caller-owned device workspace of at least gdn_workspace_bytes() bytes,
+ * 256-byte aligned.  The workspace is not read before it is written; its
+ * contents after the call are unspecified.  Two calls in flight at the same time
+ * must not share a workspace.
+ *   mode : gdn_mode_t.
+ */
+int gdn_frame_fwd_ex(const void* q, const void* k, const void* v,
+                     const float* g, const float* beta, const float* state_in,
+                     void* out, float* state_out,
+                     int B, int H, int T, int S, int D, int dtype, int mode,
+                     void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gdn_last_error -- synchronises `stream`, then returns and clears the
+ * device-side status word: GDN_OK, GDN_ERR_TIMEOUT (a kernel's bounded wait on
+ * an mbarrier or a flag gave up; its results are invalid), or GDN_ERR_CUDA
+ * (the stream reported an error).
+ */
+int gdn_last_error(void* stream);
+
+/* gdn_status_string -- a static, human-readable name for a status code. */
+const char* gdn_status_string(int status);
+
+/* gdn_version -- library version as major * 10000 + minor * 100 + patch. */
+int gdn_version(void);
+
+/*
+ * Per-kernel timing (a tracing aid; no counterpart on the pages).
+ * Between gdn_profile_begin() and gdn_profile_end(), every kernel launch the
+ * library makes in this process is bracketed by two CUDA events recorded on
+ * the launch stream.  gdn_profile_end() waits for those events, aggregates the
+ * device time per kernel name into `stats` (at most `max_stats` entries, the
+ * count in *n_stats) and stops recording.  Host-side cost: two event records
+ * per launch.  Returns GDN_OK, GDN_ERR_INVALID_ARG (NULL n_stats or stats with
+ * max_stats > 0) or GDN_ERR_CUDA.
+ */
+typedef struct {
+  char name[32];   /* kernel name, NUL-terminated */
+  int launches;    /* launches recorded */
+  double total_ms; /* summed device time between each launch's two events */
+} gdn_kernel_stat_t;
+
+int gdn_profile_begin(void);
+int gdn_profile_end(gdn_kernel_stat_t* stats, int max_stats, int* n_stats);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,161 @@
+"""Thin Python binding of libgdn's C ABI (include/gdn.h).
+
+Argument marshalling only: every step of the forward scan runs in the library's
+CUDA kernels.  The raw functions take integer device addresses; ``frame_fwd``
+additionally accepts torch tensors (torch is used for device memory and
+streams only).  There is no fallback: if ``libgdn.so`` is missing or fails to
+load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libgdn.so")
+
+GDN_F32, GDN_BF16 = 0, 1
+GDN_MODE_SEQUENTIAL, GDN_MODE_PREFIX = 0, 1
+STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_MISALIGNED",
+          4: "GDN_ERR_CUDA", 5: "GDN_ERR_TIMEOUT", 6: "GDN_ERR_WORKSPACE"}
+
+_lib = None
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_SIGS = {
+    "gdn_frame_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "gdn_frame_fwd_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
+                              ctypes.c_size_t, _P]),
+    "gdn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
+    "gdn_last_error": (_I, [_P]),
+    "gdn_status_string": (ctypes.c_char_p, [_I]),
+    "gdn_version": (_I, []),
+    "gdn_profile_begin": (_I, []),
+    "gdn_profile_end": (_I, [_P, _I, ctypes.POINTER(_I)]),
+}
+
+
+class KernelStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 32), ("launches", ctypes.c_int), ("total_ms", ctypes.c_double)]
+
+
+class GDNError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libgdn.so (once).  Raises if it is not built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+# ---- raw C-ABI calls (integer device addresses) ------------------------------------
+
+def gdn_frame_fwd(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, stream) -> int:
+    return lib().gdn_frame_fwd(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, stream)
+
+
+def gdn_frame_fwd_ex(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode,
+                     workspace, workspace_bytes, stream) -> int:
+    return lib().gdn_frame_fwd_ex(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode,
+                                  workspace, workspace_bytes, stream)
+
+
+def gdn_workspace_bytes(B, H, T, S, D, dtype, mode) -> int:
+    return lib().gdn_workspace_bytes(B, H, T, S, D, dtype, mode)
+
+
+def gdn_last_error(stream) -> int:
+    return lib().gdn_last_error(stream)
+
+
+def gdn_status_string(status: int) -> str:
+    return lib().gdn_status_string(status).decode()
+
+
+def gdn_version() -> int:
+    return lib().gdn_version()
+
+
+def gdn_profile_begin() -> int:
+    return lib().gdn_profile_begin()
+
+
+def gdn_profile_end(max_stats: int = 64) -> dict:
+    """Stops per-kernel timing; returns {kernel name: (launches, total_ms)}."""
+    arr = (KernelStat * max_stats)()
+    n = ctypes.c_int(0)
+    rc = lib().gdn_profile_end(ctypes.cast(arr, ctypes.c_void_p), max_stats, ctypes.byref(n))
+    if rc != 0:
+        raise GDNError(rc, "gdn_profile_end")
+    return {arr[i].name.decode(): (arr[i].launches, arr[i].total_ms) for i in range(min(n.value, max_stats))}
+
+
+# ---- torch marshalling -------------------------------------------------------------
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def frame_fwd(q, k, v, g, beta, state_in=None, out=None, state_out=None, mode=None,
+              workspace=None, stream=None, want_state=True):
+    """Runs the forward scan on torch CUDA tensors through the C ABI.
+
+    q, k, v: [B,H,T,S,D] float32 or bfloat16, contiguous; g: [B,H,T] float32;
+    beta: [B,H,T,S] float32; state_in: [B,H,D,D] float32 or None.  ``out`` and
+    ``state_out`` are allocated if not given (state_out only if want_state).
+    mode=None calls gdn_frame_fwd (library-managed scratch); mode=0/1 calls
+    gdn_frame_fwd_ex with ``workspace`` (a uint8 CUDA tensor, allocated if None).
+    Returns (out, state_out).  Raises GDNError on a non-zero status.
+    """
+    import torch
+
+    B, H, T, S, D = q.shape
+    dtype = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}[q.dtype]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name}: expected a contiguous CUDA tensor like q")
+    if g.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise ValueError("g and beta must be float32")
+    if tuple(g.shape) != (B, H, T) or tuple(beta.shape) != (B, H, T, S):
+        raise ValueError("g must be [B,H,T] and beta [B,H,T,S]")
+    if not g.is_contiguous() or not beta.is_contiguous():
+        raise ValueError("g and beta must be contiguous")
+    if state_in is not None and (tuple(state_in.shape) != (B, H, D, D) or state_in.dtype != torch.float32
+                                 or not state_in.is_contiguous()):
+        raise ValueError("state_in must be a contiguous float32 [B,H,D,D] tensor")
+    if out is None:
+        out = torch.empty_like(q)
+    if state_out is None and want_state:
+        state_out = torch.empty((B, H, D, D), dtype=torch.float32, device=q.device)
+    cur = torch.cuda.current_stream(q.device)
+    strm = stream if stream is not None else cur
+    st = strm.cuda_stream
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(out), _ptr(state_out),
+            B, H, T, S, D, dtype)
+    if mode is None:
+        rc = gdn_frame_fwd(*args, st)
+    else:
+        need = gdn_workspace_bytes(B, H, T, S, D, dtype, mode)
+        if workspace is None and need > 0:
+            # allocated on the current stream; keep it alive for `strm` too
+            workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+            if strm != cur:
+                workspace.record_stream(strm)
+        wbytes = 0 if workspace is None else workspace.numel()
+        rc = gdn_frame_fwd_ex(*args, mode, _ptr(workspace), wbytes, st)
+    if rc != 0:
+        raise GDNError(rc, "gdn_frame_fwd")
+    return out, state_out

@@ -1,0 +1,244 @@
+// C ABI of libgdn (declared in include/gdn.h): argument validation, workspace
+// management and dispatch to the float32 SIMT path or the bf16 tensor-core path.
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "../../include/gdn.h"
+#include "gdn_internal.h"
+
+namespace gdn {
+
+__device__ unsigned int g_device_status = 0;
+
+namespace {
+
+// Device address of the status word on the current device (cached per device).
+unsigned int* status_word() {
+  static unsigned int* cache[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (!cache[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<unsigned int*>(ptr);
+  }
+  return cache[dev];
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+// Validates everything that can be checked on the host.  Fills `p`.
+int validate(const void* q, const void* k, const void* v, const float* g, const float* beta,
+             const float* state_in, void* out, float* state_out, int B, int H, int T, int S, int D, int dtype,
+             int mode, Problem* p) {
+  if (B < 1 || H < 1 || T < 0 || S < 1 || D < 1) return kInvalidArg;
+  if (dtype != GDN_F32 && dtype != GDN_BF16) return kInvalidArg;
+  if (mode != GDN_MODE_SEQUENTIAL && mode != GDN_MODE_PREFIX) return kInvalidArg;
+  if (D % 16 != 0 || D > 128) return kUnsupported;
+  // Counts must stay inside what the kernels index with 64-bit offsets and
+  // 32-bit grid dimensions / tensor-map extents.
+  const long long bht = (long long)B * H * T;
+  if ((long long)B * H > (1LL << 31) - 1 || bht > (1LL << 31) - 1) return kInvalidArg;
+  if ((long long)S * D > (1LL << 31) - 1) return kInvalidArg;
+  if (T > 0) {
+    if (!q || !k || !v || !g || !beta || !out) return kInvalidArg;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return kMisaligned;
+    if (!aligned(g, 4) || !aligned(beta, 4)) return kMisaligned;
+  }
+  if (state_in && !aligned(state_in, 16)) return kMisaligned;
+  if (state_out && !aligned(state_out, 16)) return kMisaligned;
+  p->q = q;
+  p->k = k;
+  p->v = v;
+  p->g = g;
+  p->beta = beta;
+  p->state_in = state_in;
+  p->out = out;
+  p->state_out = state_out;
+  p->B = B;
+  p->H = H;
+  p->T = T;
+  p->S = S;
+  p->D = D;
+  p->dtype = dtype;
+  p->mode = mode;
+  p->key_scale = (float)(1.0 / std::sqrt((double)D * (double)S));
+  p->out_scale = (float)(1.0 / std::sqrt((double)D));
+  return kOk;
+}
+
+size_t workspace_for(const Problem& p) {
+  if (p.T == 0) return 0;
+  return p.dtype == GDN_F32 ? simt_workspace_bytes(p, p.mode) : tc_workspace_bytes(p, p.mode);
+}
+
+// T = 0: the final state is the initial state.
+int copy_state(const Problem& p, cudaStream_t st) {
+  if (!p.state_out) return kOk;
+  const size_t bytes = (size_t)p.BH() * p.D * p.D * sizeof(float);
+  cudaError_t e;
+  if (!p.state_in)
+    e = cudaMemsetAsync(p.state_out, 0, bytes, st);
+  else if (p.state_in != p.state_out)
+    e = cudaMemcpyAsync(p.state_out, p.state_in, bytes, cudaMemcpyDeviceToDevice, st);
+  else
+    e = cudaSuccess;
+  return e == cudaSuccess ? kOk : kCuda;
+}
+
+int forward(Problem p, void* ws, cudaStream_t st) {
+  if (p.T == 0) return copy_state(p, st);
+  p.status = status_word();
+  if (!p.status) return kCuda;
+  return p.dtype == GDN_F32 ? simt_forward(p, ws, st) : tc_forward(p, ws, st);
+}
+
+// ---- per-kernel event profiler --------------------------------------------------
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof_on = false;
+std::vector<ProfRec> g_prof_recs;
+std::vector<cudaEvent_t> g_prof_pool;
+
+cudaEvent_t prof_event() {
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+}  // namespace
+
+ProfScope::ProfScope(cudaStream_t st, const char* name) : st_(st), idx_(-1) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (!g_prof_on) return;
+  ProfRec r{name, prof_event(), prof_event()};
+  if (!r.a || !r.b) return;
+  if (cudaEventRecord(r.a, st) != cudaSuccess) return;
+  g_prof_recs.push_back(r);
+  idx_ = (int)g_prof_recs.size() - 1;
+}
+
+ProfScope::~ProfScope() {
+  if (idx_ < 0) return;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  if (idx_ < (int)g_prof_recs.size()) cudaEventRecord(g_prof_recs[idx_].b, st_);
+}
+
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" {
+
+int gdn_frame_fwd_ex(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                     const float* state_in, void* out, float* state_out, int B, int H, int T, int S, int D,
+                     int dtype, int mode, void* workspace, size_t workspace_bytes, void* stream) {
+  Problem p{};
+  int rc = validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode, &p);
+  if (rc != kOk) return rc;
+  const size_t need = workspace_for(p);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return kWorkspace;
+    if (!aligned(workspace, 256)) return kMisaligned;
+  }
+  return forward(p, workspace, static_cast<cudaStream_t>(stream));
+}
+
+int gdn_frame_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                  const float* state_in, void* out, float* state_out, int B, int H, int T, int S, int D, int dtype,
+                  void* stream) {
+  Problem p{};
+  int rc = validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, GDN_MODE_SEQUENTIAL, &p);
+  if (rc != kOk) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const size_t need = workspace_for(p);
+  void* ws = nullptr;
+  if (need > 0 && cudaMallocAsync(&ws, need, st) != cudaSuccess) return kCuda;
+  rc = forward(p, ws, st);
+  if (ws && cudaFreeAsync(ws, st) != cudaSuccess && rc == kOk) rc = kCuda;
+  return rc;
+}
+
+size_t gdn_workspace_bytes(int B, int H, int T, int S, int D, int dtype, int mode) {
+  Problem p{};
+  // Pointers are irrelevant here: validate as if T = 0 for the pointer checks.
+  static const char dummy[16] __attribute__((aligned(16))) = {0};
+  const void* d = dummy;
+  if (validate(d, d, d, (const float*)d, (const float*)d, nullptr, (void*)d, nullptr, B, H, T, S, D, dtype, mode,
+               &p) != kOk)
+    return 0;
+  return workspace_for(p);
+}
+
+int gdn_last_error(void* stream) {
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return kCuda;
+  unsigned int status = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&status, g_device_status, sizeof(status)) != cudaSuccess) return kCuda;
+  if (status != 0 && cudaMemcpyToSymbol(g_device_status, &zero, sizeof(zero)) != cudaSuccess) return kCuda;
+  return (int)status;
+}
+
+const char* gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "GDN_OK";
+    case GDN_ERR_INVALID_ARG: return "GDN_ERR_INVALID_ARG";
+    case GDN_ERR_UNSUPPORTED: return "GDN_ERR_UNSUPPORTED";
+    case GDN_ERR_MISALIGNED: return "GDN_ERR_MISALIGNED";
+    case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
+    case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    default: return "GDN_ERR_UNKNOWN";
+  }
+}
+
+int gdn_version(void) { return 100; }
+
+int gdn_profile_begin(void) {
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_on = true;
+  return GDN_OK;
+}
+
+int gdn_profile_end(gdn_kernel_stat_t* stats, int max_stats, int* n_stats) {
+  if (!n_stats || (max_stats > 0 && !stats)) return GDN_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_prof_mu);
+  g_prof_on = false;
+  int rc = GDN_OK;
+  std::vector<gdn_kernel_stat_t> agg;
+  for (const ProfRec& r : g_prof_recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) {
+      rc = GDN_ERR_CUDA;
+      ms = 0.f;
+    }
+    size_t i = 0;
+    while (i < agg.size() && std::strncmp(agg[i].name, r.name, sizeof(agg[i].name)) != 0) ++i;
+    if (i == agg.size()) {
+      gdn_kernel_stat_t z{};
+      std::strncpy(z.name, r.name, sizeof(z.name) - 1);
+      agg.push_back(z);
+    }
+    agg[i].launches += 1;
+    agg[i].total_ms += ms;
+    g_prof_pool.push_back(r.a);
+    g_prof_pool.push_back(r.b);
+  }
+  g_prof_recs.clear();
+  *n_stats = (int)agg.size();
+  for (int i = 0; i < (int)agg.size() && i < max_stats; ++i) stats[i] = agg[i];
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// Internal declarations shared by the libgdn translation units.
+//
+// Every path computes the scan in its affine ("transition") form, which is the
+// residual-form update multiplied out:
+//
+//   S_t = g_t S_{t-1} + K~^T diag(beta) (V - g_t K~ S_{t-1})
+//       = g_t (S_{t-1} - M_t S_{t-1}) + b_t,
+//   M_t = K~^T diag(beta) K~   (D x D, symmetric PSD),   b_t = K~^T diag(beta) V_t.
+//
+// M_t and b_t depend only on frame t's inputs, so they are formed for every
+// frame in parallel ("gram" stage); only the D x D x D recurrence is serial
+// ("scan" stage); the read-out O_t = Q_t S_t / sqrt(D) is parallel again
+// ("readout" stage).  The same maps (A_t = g_t (I - M_t), b_t) are what the
+// prefix mode composes (zhichai.net SANA-WM summary, training Stage 3).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace gdn {
+
+struct Problem {
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  const float* state_in;
+  void* out;
+  float* state_out;
+  int B, H, T, S, D;
+  int dtype;  // gdn_dtype_t
+  int mode;   // gdn_mode_t
+  float key_scale;  // 1/sqrt(D*S)
+  float out_scale;  // 1/sqrt(D)
+  unsigned int* status;  // device-side status word (first error wins)
+  long long BH() const { return (long long)B * H; }
+  long long BHT() const { return (long long)B * H * T; }
+};
+
+// Status codes (mirror gdn_status_t).
+enum Status {
+  kOk = 0, kInvalidArg = 1, kUnsupported = 2, kMisaligned = 3, kCuda = 4, kTimeout = 5, kWorkspace = 6
+};
+
+// Records a device-side error in the status word; the first error wins.
+__device__ __forceinline__ void report_device_error(unsigned int* status, unsigned int code) {
+  atomicCAS(status, 0u, code);
+}
+
+// ---- SIMT path (float32 arithmetic; used for float32 I/O) --------------------
+size_t simt_workspace_bytes(const Problem& p, int mode);
+int simt_forward(const Problem& p, void* ws, cudaStream_t st);
+
+// ---- tensor-core path (bf16 I/O) ------------------------------------------------
+size_t tc_workspace_bytes(const Problem& p, int mode);
+int tc_forward(const Problem& p, void* ws, cudaStream_t st);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Brackets one kernel launch with CUDA events while gdn_profile_begin() is in
+// effect (no-op otherwise).  Construct immediately before the launch.
+class ProfScope {
+ public:
+  ProfScope(cudaStream_t st, const char* name);
+  ~ProfScope();
+ private:
+  cudaStream_t st_;
+  int idx_;
+};
+
+}  // namespace gdn

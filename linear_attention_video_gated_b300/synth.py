@@ -176,27 +176,30 @@ def _threads() -> int:
 
 
 def fill_io(wl: Workload, q: np.ndarray, k: np.ndarray, v: np.ndarray,
-            g: np.ndarray, bt: np.ndarray, t0: int = 0, threads: int | None = None) -> None:
-    """Fill caller-owned host arrays with frames [t0, t0 + q.shape[2]) of every head.
+            g: np.ndarray, bt: np.ndarray, t0: int = 0, b0: int = 0, threads: int | None = None) -> None:
+    """Fill caller-owned host arrays with frames [t0, t0 + q.shape[2]) of batch
+    indices [b0, b0 + q.shape[0]), every head.
 
-    q, k, v: [B, H, T', S, D] uint16 (bf16 bits) for bf16 workloads or float32 for f32;
-    g: [B, H, T'] float32; bt: [B, H, T', S] float32.  The arrays may be numpy views of
-    pinned torch tensors.  Generation runs on a thread pool (numpy releases the GIL).
+    q, k, v: [B', H, T', S, D] uint16 (bf16 bits) for bf16 workloads or float32 for
+    f32; g: [B', H, T'] float32; bt: [B', H, T', S] float32.  The arrays may be numpy
+    views of pinned torch tensors.  Generation runs on a thread pool (numpy
+    releases the GIL while drawing).
     """
-    Tn = q.shape[2]
-    jobs = [(b, h, t) for b in range(wl.B) for h in range(wl.H) for t in range(Tn)]
+    Bn, Hn, Tn = q.shape[0], q.shape[1], q.shape[2]
+    jobs = [(bb, h, tt) for bb in range(Bn) for h in range(Hn) for tt in range(Tn)]
+    nthreads = threads or _threads()
 
     def one(job):
-        b, h, tt = job
-        t = t0 + tt
+        bb, h, tt = job
+        b, t = b0 + bb, t0 + tt
         for name, dst in (("q", q), ("k", k), ("v", v)):
             x = frame_raw(wl, name, b, h, t)
-            dst[b, h, tt] = bf16_bits(x) if wl.dtype == "bf16" else x
-        g[b, h, tt] = gate(wl, b, h, t)
-        bt[b, h, tt] = beta(wl, b, h, t)
+            dst[bb, h, tt] = bf16_bits(x) if wl.dtype == "bf16" else x
+        g[bb, h, tt] = gate(wl, b, h, t)
+        bt[bb, h, tt] = beta(wl, b, h, t)
 
-    with ThreadPoolExecutor(threads or _threads()) as ex:
-        for _ in ex.map(one, jobs, chunksize=max(1, len(jobs) // (64 * (threads or _threads())))):
+    with ThreadPoolExecutor(nthreads) as ex:
+        for _ in ex.map(one, jobs, chunksize=max(1, len(jobs) // (16 * nthreads))):
             pass
 
 

@@ -1,0 +1,98 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+function include/gdn.h declares, and rejects bad arguments on the host before
+any CUDA call is made."""
+import os
+import re
+import subprocess
+
+import pytest
+
+from linear_attention_video_gated_b300 import binding, build_lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADERS = [os.path.join(ROOT, "include", f) for f in sorted(os.listdir(os.path.join(ROOT, "include")))
+           if f.endswith(".h")]
+
+# Fake, never-dereferenced device addresses: every call below fails validation
+# before the library touches CUDA.
+A16 = 0x10000
+MIS = 0x10002
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return binding.lib()
+
+
+def declared_functions():
+    names = []
+    for h in HEADERS:
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"^[A-Za-z_][\w \*]*?\b(gdn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("gdn_frame_fwd", "gdn_frame_fwd_ex", "gdn_workspace_bytes", "gdn_last_error",
+                     "gdn_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
+    exported = set(re.findall(r"\bT (gdn_\w+)$", out, flags=re.M))
+    for name in declared_functions():
+        assert name in exported, name
+        assert hasattr(lib, name)
+
+
+def test_status_strings(lib):
+    for code, name in binding.STATUS.items():
+        assert binding.gdn_status_string(code) == name
+    assert binding.gdn_status_string(99) == "GDN_ERR_UNKNOWN"
+    assert binding.gdn_version() >= 100
+
+
+def _call(B=1, H=2, T=3, S=17, D=32, dtype=1, ptr=A16, g=A16, beta=A16, out=A16, state_in=None, state_out=None,
+          mode=0, ws=A16, wsb=1 << 40):
+    return binding.gdn_frame_fwd_ex(ptr, ptr, ptr, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode,
+                                    ws, wsb, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), 1), (dict(H=0), 1), (dict(T=-1), 1), (dict(S=0), 1), (dict(D=0), 1),
+    (dict(dtype=2), 1), (dict(mode=2), 1),
+    (dict(D=24), 2), (dict(D=144), 2), (dict(D=8), 2),
+    (dict(ptr=None), 1), (dict(g=None), 1), (dict(beta=None), 1), (dict(out=None), 1),
+    (dict(ptr=MIS), 3), (dict(out=MIS), 3), (dict(g=A16 + 2), 3), (dict(state_in=MIS), 3),
+    (dict(state_out=MIS), 3),
+    (dict(ws=None), 6), (dict(wsb=16), 6), (dict(ws=A16 + 16), 3),
+])
+def test_validation_rejects(lib, kw, code):
+    assert _call(**kw) == code
+
+
+def test_validation_rejects_plain_entry(lib):
+    assert binding.gdn_frame_fwd(A16, A16, A16, A16, A16, None, A16, None, 1, 1, 1, 1, 24, 1, None) == 2
+    assert binding.gdn_frame_fwd(None, A16, A16, A16, A16, None, A16, None, 1, 1, 1, 1, 32, 1, None) == 1
+
+
+def test_workspace_bytes_is_pure_and_scales(lib):
+    a = binding.gdn_workspace_bytes(1, 20, 961, 880, 112, 1, 0)
+    assert a > 0 and a == binding.gdn_workspace_bytes(1, 20, 961, 880, 112, 1, 0)
+    assert binding.gdn_workspace_bytes(1, 20, 0, 880, 112, 1, 0) == 0
+    assert binding.gdn_workspace_bytes(1, 20, 961, 880, 24, 1, 0) == 0
+    assert binding.gdn_workspace_bytes(1, 20, 961, 880, 112, 1, 1) >= a
+    assert binding.gdn_workspace_bytes(2, 20, 961, 880, 112, 1, 0) >= a
+    assert binding.gdn_workspace_bytes(1, 2, 8, 16, 16, 0, 0) > 0
+
+
+def test_no_gpu_call_fails_loudly_not_silently(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    # with no device, a valid-looking call must report a CUDA error, never succeed
+    assert binding.gdn_last_error(None) == 4

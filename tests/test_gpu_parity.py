@@ -1,0 +1,208 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, on the
+same seeded inputs.  Tolerances are in tests/parity.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from linear_attention_video_gated_b300 import binding, build_lib, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    build_lib.ensure_built()
+    binding.lib()
+
+
+def run(q, k, v, g, beta, state_in=None, mode=None, **kw):
+    out, st = binding.frame_fwd(q, k, v, g, beta, state_in=state_in, mode=mode, **kw)
+    torch.cuda.synchronize()
+    parity.check_status()
+    return out, st
+
+
+def np_(t):
+    return t.float().cpu().numpy()
+
+
+@pytest.mark.parametrize("mode", [None, 0, 1])
+def test_tiny_f32(mode):
+    wl = synth.WORKLOADS["tiny"]
+    x = synth.full(wl)
+    out, st = run(*parity.upload(wl, x), mode=mode)
+    ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"])
+    parity.assert_parity("f32", np_(out), ro, np_(st), rs, f"tiny mode={mode}")
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_short_bf16(mode):
+    wl = synth.WORKLOADS["short"]
+    x = synth.full(wl)
+    out, st = run(*parity.upload(wl, x), mode=mode)
+    ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"])
+    eo, es = parity.assert_parity("bf16", np_(out), ro, np_(st), rs, f"short mode={mode}")
+    print(f"short mode={mode}: out {eo} state {es}")
+
+
+# (dtype, B, H, T, S, D, nonzero initial state)
+EDGE = [
+    ("bf16", 1, 1, 1, 1, 16, False),
+    ("bf16", 1, 2, 5, 17, 32, True),
+    ("bf16", 2, 1, 4, 129, 48, False),
+    ("bf16", 1, 1, 3, 300, 64, True),
+    ("bf16", 1, 2, 2, 257, 80, False),
+    ("bf16", 1, 1, 17, 200, 96, True),
+    ("bf16", 1, 1, 33, 64, 128, False),
+    ("bf16", 1, 3, 6, 880, 112, True),
+    ("f32", 1, 1, 1, 1, 16, False),
+    ("f32", 2, 2, 5, 33, 128, True),
+    ("f32", 1, 1, 3, 100, 112, True),
+    ("f32", 1, 1, 20, 7, 64, False),
+]
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("case", EDGE, ids=lambda c: "-".join(map(str, c)))
+def test_edge_shapes(case, mode):
+    dt, B, H, T, S, D, nz = case
+    base = synth.WORKLOADS["short" if dt == "bf16" else "tiny"]
+    wl = base.with_(B=B, H=H, T=T, S=S, D=D, seed=base.seed + 17 * S + D)
+    x = synth.full(wl)
+    S0 = np.stack([np.stack([synth.state(wl, b, h, 0.3) for h in range(H)]) for b in range(B)]) if nz else None
+    si = None if S0 is None else torch.from_numpy(S0).cuda()
+    out, st = run(*parity.upload(wl, x), state_in=si, mode=mode)
+    ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0)
+    parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"edge {case} mode={mode}")
+
+
+def _small_bf16(T=21, H=3, S=300, D=112):
+    wl = synth.WORKLOADS["short"].with_(H=H, T=T, S=S, D=D)
+    return wl, synth.full(wl)
+
+
+def test_state_aliasing_is_bitwise_identical():
+    wl, x = _small_bf16()
+    ins = parity.upload(wl, x)
+    S0 = torch.from_numpy(np.stack([np.stack([synth.state(wl, 0, h) for h in range(wl.H)])])).cuda()
+    out_a, st_a = run(*ins, state_in=S0.clone(), mode=0)
+    buf = S0.clone()
+    out_b, st_b = run(*ins, state_in=buf, state_out=buf, mode=0)
+    assert torch.equal(out_a, out_b) and torch.equal(st_a, buf)
+
+
+def test_zero_frames_copies_state():
+    wl, x = _small_bf16(T=1)
+    q, k, v, g, beta = parity.upload(wl, x)
+    e = lambda t: t[:, :, :0].contiguous()  # noqa: E731
+    S0 = torch.randn(1, wl.H, wl.D, wl.D, device="cuda")
+    _, st = run(e(q), e(k), e(v), e(g), e(beta), state_in=S0, mode=0)
+    assert torch.equal(st, S0)
+    st2 = torch.full_like(S0, 7.0)
+    run(e(q), e(k), e(v), e(g), e(beta), state_out=st2, mode=0)
+    assert torch.count_nonzero(st2) == 0
+
+
+@pytest.mark.parametrize("mode", [0, 1])
+def test_chunked_calls_equal_single_call(mode):
+    """Chunk-causal rollout: consecutive calls passing state_out -> state_in give the
+    single call's outputs.  In sequential mode the per-frame arithmetic does not
+    depend on where the calls split, so the results are bitwise equal."""
+    wl, x = _small_bf16(T=21)
+    q, k, v, g, beta = parity.upload(wl, x)
+    out1, st1 = run(q, k, v, g, beta, mode=mode)
+    outs, st = [], None
+    for a, b in ((0, 10), (10, 20), (20, 21)):
+        sl = lambda t: t[:, :, a:b].contiguous()  # noqa: E731
+        o, st = run(sl(q), sl(k), sl(v), sl(g), sl(beta), state_in=st, mode=mode)
+        outs.append(o)
+    out2 = torch.cat(outs, dim=2)
+    if mode == 0:
+        assert torch.equal(out1, out2) and torch.equal(st1, st)
+    else:
+        ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"])
+        parity.assert_parity("bf16", np_(out2), ro, np_(st), rs, "chunked prefix")
+
+
+def test_repeat_calls_are_deterministic():
+    wl, x = _small_bf16(T=9)
+    ins = parity.upload(wl, x)
+    a = run(*ins, mode=0)
+    b = run(*ins, mode=0)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_plain_entry_matches_explicit_workspace():
+    wl, x = _small_bf16(T=5)
+    ins = parity.upload(wl, x)
+    a = run(*ins, mode=None)
+    b = run(*ins, mode=0)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+# ------------------------------------------------------------------ full sizes
+
+@pytest.fixture(scope="module")
+def minute_inputs():
+    wl = synth.WORKLOADS["minute"]
+    return wl, parity.device_inputs(wl)
+
+
+@pytest.fixture(scope="module")
+def minute_oracle():
+    wl = synth.WORKLOADS["minute"]
+    return {bh: parity.oracle_head(wl, *bh) for bh in synth.head_sample(wl, 2)}
+
+
+def _check_heads(wl, out, st, ref, what):
+    for (b, h), (ro, rs) in ref.items():
+        eo, es = parity.assert_parity(wl.dtype, np_(out[b, h]), ro, np_(st[b, h]), rs, f"{what} head {(b, h)}")
+        print(f"{what} head {(b, h)}: out {eo} state {es}")
+
+
+def test_minute_single_call(minute_inputs, minute_oracle):
+    """961 frames x 880 tokens x 20 heads x d112, one call, in the bench's launch
+    configuration; sampled heads checked over every frame against the oracle."""
+    wl, ins = minute_inputs
+    out, st = run(*ins, mode=0)
+    _check_heads(wl, out, st, minute_oracle, "minute")
+
+
+def test_minute_chunked_rollout(minute_inputs, minute_oracle):
+    """The same tensors as 97 calls of <= 10 frames carrying the state."""
+    wl, (q, k, v, g, beta) = minute_inputs
+    cw = synth.WORKLOADS["chunked"]
+    outs, st, t0 = [], None, 0
+    for n in cw.chunks:
+        sl = lambda t: t[:, :, t0:t0 + n].contiguous()  # noqa: E731
+        o, st = run(sl(q), sl(k), sl(v), sl(g), sl(beta), state_in=st, mode=0)
+        outs.append(o)
+        t0 += n
+    assert t0 == wl.T
+    out = torch.cat(outs, dim=2)
+    _check_heads(wl, out, st, minute_oracle, "chunked")
+
+
+def test_large_sequential_and_prefix_agree():
+    """4 x 16 heads, 241 frames of 3600 tokens, d128: the sequential scan and the
+    chunked prefix composition agree everywhere, and sampled heads match the oracle."""
+    wl = synth.WORKLOADS["large"]
+    ins = parity.device_inputs(wl)
+    out0, st0 = run(*ins, mode=0)
+    out1, st1 = run(*ins, mode=1)
+    del ins
+    rms_o = torch.sqrt(torch.mean(out0.float() ** 2)).item()
+    rms_s = torch.sqrt(torch.mean(st0 ** 2)).item()
+    d_o = 0.0
+    for b in range(wl.B):
+        d_o = max(d_o, (out0[b].float() - out1[b].float()).abs().max().item())
+    d_s = (st0 - st1).abs().max().item()
+    print(f"large: seq vs prefix out max-abs/rms {d_o / rms_o:.3e}, state {d_s / rms_s:.3e}")
+    assert d_o / rms_o <= parity.BF16_MAX_ABS_OVER_RMS and d_s / rms_s <= parity.BF16_MAX_ABS_OVER_RMS
+    ref = {bh: parity.oracle_head(wl, *bh) for bh in synth.head_sample(wl, 2)}
+    _check_heads(wl, out0, st0, ref, "large seq")
+    _check_heads(wl, out1, st1, ref, "large prefix")
