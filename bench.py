@@ -172,9 +172,13 @@ def bus_id(dev) -> str | None:
 def oracle_sample(wl, budget_s: float, max_heads: int | None = None, frames: int | None = None):
     """Times the fp64 oracle on whole heads of the workload until `budget_s` of CPU
     work.  Returns (equivalent tokens/s, cores, sample description, seconds)."""
-    from threadpoolctl import threadpool_limits
+    import contextlib
 
     import oracle
+    try:
+        from threadpoolctl import threadpool_limits
+    except ImportError:  # BLAS then runs on its default thread count: every core
+        threadpool_limits = lambda n: contextlib.nullcontext()  # noqa: E731
     cores = len(os.sched_getaffinity(0))
     T = wl.T if frames is None else min(frames, wl.T)
     max_heads = wl.B * wl.H if max_heads is None else max_heads

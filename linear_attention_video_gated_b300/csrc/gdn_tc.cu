@@ -1,8 +1,849 @@
-// bf16 tensor-core path (placeholder: routes to the SIMT kernels until the
-// tcgen05 kernels are in place).
+// bf16 tensor-core path of the frame-wise GDN forward scan (sm_103a: tcgen05
+// MMAs with TMEM accumulators, operands staged by TMA / bulk copies).
+//
+// The scan runs in its transition form (gdn_internal.h):
+//   gram    : [M_t | b_t] = (diag(beta) K)^T [K | V], every frame-head in
+//             parallel.  diag(beta)K is split into bf16 hi + lo parts (the lo
+//             part only feeds b_t, whose precision sets the state's);
+//             M_t -> bf16 image (the scan's B operand), b_t -> fp32.
+//   scan    : per head, frame by frame: P^T = S^T M_t on the tensor core with S
+//             split into bf16 hi + lo (A operand), then S <- g (S - P) + b_t in
+//             fp32 registers.  Writes S_t as a bf16 hi/lo image for the read-out.
+//   readout : O_t^T = S_t^T Q_t^T (A = S image, B = Q tile, N = 128 tokens),
+//             epilogue x 1/sqrt(D) -> bf16 -> TMA store.
+//
+// Shared-memory tiles use 128-byte rows with the 128-byte swizzle.  A 16-bit
+// matrix with more than 64 columns is kept as "atoms" of 64 columns each, one
+// region per atom.  Descriptor conventions (canonical tcgen05 layouts):
+//   K-major operand (K contiguous): SBO = 1024 (8 rows x 128 B); one MMA K-step of
+//     16 elements advances the start address 32 bytes inside an atom.
+//   MN-major operand (M/N contiguous): LBO = byte stride between 64-wide MN atoms,
+//     SBO = 1024 (8 K-rows x 128 B); one K-step of 16 rows advances 2048 bytes.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "gdn_internal.h"
+#include "ptx.cuh"
 
 namespace gdn {
-size_t tc_workspace_bytes(const Problem& p, int mode) { return simt_workspace_bytes(p, mode); }
-int tc_forward(const Problem& p, void* ws, cudaStream_t st) { return simt_forward(p, ws, st); }
+namespace {
+
+using namespace ptx;
+
+constexpr int kGramTok = 64;                   // tokens per gram stage
+constexpr int kGramStages = 3;
+constexpr int kGramRegion = kGramTok * 128;    // one 64-column atom of a stage
+constexpr int kGramThreads = 320;              // 4 epilogue, 4 convert, 1 TMA, 1 MMA warps
+constexpr int kScanStages = 2;
+constexpr int kScanThreads = 320;              // 8 epilogue, 1 copy, 1 MMA warps
+constexpr int kImgRegion = 128 * 128;          // one atom of a 128-row operand image
+constexpr int kOutTok = 128;                   // tokens per read-out tile (MMA N)
+constexpr int kOutQStages = 2;
+constexpr int kOutAcc = 4;                     // TMEM accumulators in flight
+constexpr int kOutThreads = 192;               // 4 epilogue, 1 TMA, 1 MMA warps
+
+__host__ __device__ inline int num_atoms(int D) { return (D + 63) / 64; }
+
+// ---------------------------------------------------------------- workspace layout
+struct TcLayout {
+  size_t m_off, b_off, s_off, total;
+  size_t m_bytes, b_bytes, s_bytes;  // per frame-head
+};
+
+TcLayout tc_layout(const Problem& p) {
+  TcLayout L{};
+  const int NA = num_atoms(p.D);
+  L.m_bytes = (size_t)NA * p.D * 128;      // M_t image: NA regions of D rows x 128 B
+  L.b_bytes = (size_t)p.D * p.D * 4;       // b_t: fp32 [i][j]
+  L.s_bytes = (size_t)2 * NA * p.D * 128;  // S_t image: hi/lo x NA regions of D rows
+  const size_t F = (size_t)p.BHT();
+  L.m_off = 0;
+  L.b_off = align_up(L.m_off + F * L.m_bytes, 1024);
+  L.s_off = align_up(L.b_off + F * L.b_bytes, 1024);
+  L.total = align_up(L.s_off + F * L.s_bytes, 1024);
+  return L;
+}
+
+// ---------------------------------------------------------------- tensor maps
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 3D view [frames][S][D] of a bf16 [B,H,T,S,D] tensor; box = 64 columns x rows x 1 frame.
+bool make_map(CUtensorMap* m, const void* base, int D, int S, long long F, int rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)F};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Bounded wait that also gives up when another role has aborted; a timeout is
+// recorded in the status word and raises the CTA's abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                              unsigned int* status) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*abort_flag) return false;
+      if (globaltimer() - t0 > kWaitTimeoutNs) {
+        report_device_error(status, kTimeout);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+}
+
+// A bounded wait used only while tearing down after an abort.
+__device__ __forceinline__ void wait_bounded(uint32_t bar, uint32_t parity, uint64_t ns) {
+  const uint64_t t0 = globaltimer();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer() - t0 > ns) return;
+}
+
+// Pipeline ring position plus, per slot, the parity of the last fill issued into
+// it, so that an aborting producer can wait for its own copies still in flight.
+template <int N>
+struct Ring {
+  int stage = 0;
+  uint32_t phase = 0;
+  uint32_t issued_mask = 0;
+  uint32_t last_phase_mask = 0;
+  __device__ void mark_issued() {
+    issued_mask |= 1u << stage;
+    last_phase_mask = (last_phase_mask & ~(1u << stage)) | (phase << stage);
+  }
+  __device__ void advance() {
+    if (++stage == N) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+  // Waits (bounded) for the last fill of every slot to land on its `full` barrier.
+  __device__ void drain(const uint64_t* full) const {
+    for (int s = 0; s < N; ++s)
+      if (issued_mask & (1u << s)) wait_bounded(smem_u32(&full[s]), (last_phase_mask >> s) & 1u, 500000000ull);
+  }
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Splits x into bf16 hi + lo with hi = rne(x), lo = rne(x - hi).
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+// =============================================================================
+// gram: [M | b] = (diag(beta) K)^T [K | V] per frame-head.
+// =============================================================================
+struct GramArgs {
+  const float* beta;
+  uint8_t* m_img;   // F x m_bytes
+  float* b_mat;     // F x D x D
+  long long nitems;
+  int S, D, NA;
+  float m_scale, b_scale;
+  unsigned int* status;
+};
+
+__global__ void __launch_bounds__(kGramThreads, 1)
+    tc_gram_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV, GramArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int NA = a.NA, D = a.D, S = a.S;
+  // stage layout: K atoms [NA], V atoms [NA], AH atoms [2], AL atoms [2]
+  const int stage_bytes = (2 * NA + 4) * kGramRegion;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kGramStages * stage_bytes);
+  uint64_t* full = bars;
+  uint64_t* scaled = bars + kGramStages;
+  uint64_t* empty = bars + 2 * kGramStages;
+  uint64_t* accfull = bars + 3 * kGramStages;
+  uint64_t* accempty = accfull + 2;
+  uint64_t* mma_done = accempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(mma_done), 1);
+    for (int s = 0; s < kGramStages; ++s) {
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&scaled[s]), 4);
+      mbar_init(smem_u32(&empty[s]), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&accfull[b]), 1);
+      mbar_init(smem_u32(&accempty[b]), 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (NA == 1) {  // A operands span 128 rows of M: zero the unused upper atom once
+    for (int s = 0; s < kGramStages; ++s) {
+      uint4* ah1 = reinterpret_cast<uint4*>(smem + s * stage_bytes + (2 * NA + 1) * kGramRegion);
+      uint4* al1 = reinterpret_cast<uint4*>(smem + s * stage_bytes + (2 * NA + 3) * kGramRegion);
+      for (int i = threadIdx.x; i < kGramRegion / 16; i += blockDim.x) {
+        ah1[i] = make_uint4(0, 0, 0, 0);
+        al1[i] = make_uint4(0, 0, 0, 0);
+      }
+    }
+    fence_proxy_async_smem();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nchunks = (S + kGramTok - 1) / kGramTok;
+
+  if (warp == 8) {
+    // ---------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&mapK);
+      prefetch_tmap(&mapV);
+      Ring<kGramStages> r;
+      bool ok = true;
+      for (long long f = blockIdx.x; ok && f < a.nitems; f += gridDim.x) {
+        for (int c = 0; c < nchunks; ++c) {
+          if (!wait_or_abort(smem_u32(&empty[r.stage]), r.phase ^ 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          uint8_t* st = smem + r.stage * stage_bytes;
+          const uint32_t fb = smem_u32(&full[r.stage]);
+          mbar_arrive_expect_tx(fb, 2 * NA * kGramRegion);
+          for (int at = 0; at < NA; ++at) {
+            tma_load_3d(smem_u32(st + at * kGramRegion), &mapK, fb, 64 * at, c * kGramTok, (int)f);
+            tma_load_3d(smem_u32(st + (NA + at) * kGramRegion), &mapV, fb, 64 * at, c * kGramTok, (int)f);
+          }
+          r.mark_issued();
+          r.advance();
+        }
+      }
+      r.drain(full);  // every issued load has landed before the CTA may exit
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA issuer
+    if (lane == 0) {
+      const uint32_t id1 = idesc_bf16(128, NA * 64 + D, 1, 1);
+      const uint32_t id2 = idesc_bf16(128, D, 1, 1);
+      int stage = 0;
+      uint32_t phase = 0;
+      int ab = 0;
+      uint32_t aphase = 0;
+      for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+        if (!wait_or_abort(smem_u32(&accempty[ab]), aphase ^ 1, abort_flag, a.status)) goto done;
+        tc_fence_after();
+        const uint32_t acc = tmem + ab * 256;
+        for (int c = 0; c < nchunks; ++c) {
+          if (!wait_or_abort(smem_u32(&scaled[stage]), phase, abort_flag, a.status)) goto done;
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + stage * stage_bytes);
+          const uint32_t k0 = st, v0 = st + NA * kGramRegion;
+          const uint32_t ah0 = st + 2 * NA * kGramRegion, al0 = ah0 + 2 * kGramRegion;
+#pragma unroll
+          for (int kk = 0; kk < kGramTok / 16; ++kk) {
+            const uint32_t off = kk * 2048;
+            mma_bf16(acc, smem_desc(ah0 + off, kGramRegion, 1024), smem_desc(k0 + off, kGramRegion, 1024), id1,
+                     (c > 0 || kk > 0) ? 1u : 0u);
+            mma_bf16(acc + NA * 64, smem_desc(al0 + off, kGramRegion, 1024), smem_desc(v0 + off, kGramRegion, 1024),
+                     id2, 1u);
+          }
+          mma_commit(smem_u32(&empty[stage]));
+          if (++stage == kGramStages) { stage = 0; phase ^= 1; }
+        }
+        mma_commit(smem_u32(&accfull[ab]));
+        if (++ab == 2) { ab = 0; aphase ^= 1; }
+      }
+    }
+  } else if (warp >= 4) {
+    // ---------------- beta scaling: A = diag(beta) K, split into bf16 hi + lo
+    const int ct = threadIdx.x - 128;
+    int stage = 0;
+    uint32_t phase = 0;
+    const int chunks_per_atom = kGramTok * 8;
+    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+      const float* bf = a.beta + f * S;
+      for (int c = 0; c < nchunks; ++c) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status))) goto done;
+        uint8_t* st = smem + stage * stage_bytes;
+        for (int ch = ct; ch < NA * chunks_per_atom; ch += 128) {
+          const int at = ch / chunks_per_atom;
+          const int off = (ch % chunks_per_atom) * 16;
+          const int s = c * kGramTok + off / 128;
+          const float bs = s < S ? __ldg(bf + s) : 0.f;
+          const uint4 kv = *reinterpret_cast<const uint4*>(st + at * kGramRegion + off);
+          const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            split2(bs * x.x, bs * x.y, hi[e], lo[e]);
+          }
+          *reinterpret_cast<uint4*>(st + (2 * NA + at) * kGramRegion + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(st + (2 * NA + 2 + at) * kGramRegion + off) =
+              make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&scaled[stage]));
+        if (++stage == kGramStages) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else {
+    // ---------------- epilogue: TMEM -> M image (bf16) and b (fp32)
+    const int i = warp * 32 + lane;  // accumulator row = key index
+    int ab = 0;
+    uint32_t aphase = 0;
+    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+      if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[ab]), aphase, abort_flag, a.status))) goto done;
+      tc_fence_after();
+      const uint32_t acc = tmem + ((uint32_t)(warp * 32) << 16) + ab * 256;
+      uint8_t* mimg = a.m_img + (size_t)f * NA * D * 128;
+      float* brow = a.b_mat + (size_t)f * D * D + (size_t)i * D;
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+        tmem_ld16(acc + c0, v);
+        tmem_ld_wait();
+        if (i < D) {
+          uint8_t* reg = mimg + (size_t)(c0 / 64) * D * 128;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int col = (c0 % 64) + 8 * h;
+            uint4 o;
+            o.x = pack_bf16(v[8 * h + 0] * a.m_scale, v[8 * h + 1] * a.m_scale);
+            o.y = pack_bf16(v[8 * h + 2] * a.m_scale, v[8 * h + 3] * a.m_scale);
+            o.z = pack_bf16(v[8 * h + 4] * a.m_scale, v[8 * h + 5] * a.m_scale);
+            o.w = pack_bf16(v[8 * h + 6] * a.m_scale, v[8 * h + 7] * a.m_scale);
+            *reinterpret_cast<uint4*>(reg + sw128_off(i, col)) = o;
+          }
+        }
+      }
+      for (int c0 = 0; c0 < D; c0 += 16) {
+        float v[16];
+        tmem_ld16(acc + NA * 64 + c0, v);
+        tmem_ld_wait();
+        if (i < D) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(brow + c0 + 4 * q) =
+                make_float4(v[4 * q] * a.b_scale, v[4 * q + 1] * a.b_scale, v[4 * q + 2] * a.b_scale,
+                            v[4 * q + 3] * a.b_scale);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
+      if (++ab == 2) { ab = 0; aphase ^= 1; }
+    }
+  }
+done:
+  if (warp == 9 && lane == 0) {  // every MMA this CTA issued has completed
+    mma_commit(smem_u32(mma_done));
+    wait_bounded(smem_u32(mma_done), 0, 500000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// =============================================================================
+// scan: S_t = g_t (S_{t-1} - M_t S_{t-1}) + b_t per head, frame by frame.
+// =============================================================================
+struct ScanArgs {
+  const uint8_t* m_img;
+  const float* b_mat;
+  const float* g;
+  const float* state_in;
+  uint8_t* s_img;
+  float* state_out;
+  int T, D, NA;
+  unsigned int* status;
+};
+
+__global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int NA = a.NA, D = a.D, T = a.T;
+  // A image (S^T hi/lo): [hl][atom] regions of 128 rows; M stages: [stage][atom] of D rows
+  uint8_t* img = smem;
+  uint8_t* mst = smem + 2 * NA * kImgRegion;
+  const int m_stage_bytes = NA * D * 128;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(mst + kScanStages * m_stage_bytes);
+  uint64_t* mfull = bars;
+  uint64_t* mempty = bars + kScanStages;
+  uint64_t* accfull = bars + 2 * kScanStages;
+  uint64_t* sready = accfull + 1;
+  uint64_t* mma_done = sready + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const long long bh = blockIdx.x;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kScanStages; ++s) {
+      mbar_init(smem_u32(&mfull[s]), 1);
+      mbar_init(smem_u32(&mempty[s]), 1);
+    }
+    mbar_init(smem_u32(accfull), 1);
+    mbar_init(smem_u32(sready), 1);
+    mbar_init(smem_u32(mma_done), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(tmem_slot), 128);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 8) {
+    // ---------------- copy M_t images in
+    if (lane == 0) {
+      Ring<kScanStages> r;
+      for (int t = 0; t < T; ++t) {
+        if (!wait_or_abort(smem_u32(&mempty[r.stage]), r.phase ^ 1, abort_flag, a.status)) break;
+        const uint32_t fb = smem_u32(&mfull[r.stage]);
+        mbar_arrive_expect_tx(fb, m_stage_bytes);
+        const uint8_t* src = a.m_img + (size_t)(bh * T + t) * m_stage_bytes;
+        for (int at = 0; at < NA; ++at)
+          bulk_g2s(smem_u32(mst + r.stage * m_stage_bytes + at * D * 128), src + at * D * 128, D * 128, fb);
+        r.mark_issued();
+        r.advance();
+      }
+      r.drain(mfull);
+    }
+  } else if (warp == 9) {
+    // ---------------- MMA: P^T = S^T M_t
+    if (lane == 0) {
+      const uint32_t id = idesc_bf16(128, D, 0, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = 0; t < T; ++t) {
+        if (!wait_or_abort(smem_u32(sready), t & 1, abort_flag, a.status)) goto done;
+        if (!wait_or_abort(smem_u32(&mfull[stage]), phase, abort_flag, a.status)) goto done;
+        tc_fence_after();
+        const uint32_t ms = smem_u32(mst + stage * m_stage_bytes);
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const int at = kk / 4;
+          const uint32_t ko = (kk % 4) * 32;
+          const uint64_t bdesc = smem_desc(ms + at * D * 128 + ko, 16, 1024);
+          mma_bf16(tmem, smem_desc(smem_u32(img + at * kImgRegion) + ko, 16, 1024), bdesc, id, kk > 0 ? 1u : 0u);
+          mma_bf16(tmem, smem_desc(smem_u32(img + (NA + at) * kImgRegion) + ko, 16, 1024), bdesc, id, 1u);
+        }
+        mma_commit(smem_u32(&mempty[stage]));
+        mma_commit(smem_u32(accfull));
+        if (++stage == kScanStages) { stage = 0; phase ^= 1; }
+      }
+    }
+  } else {
+    // ---------------- epilogue (8 warps): thread owns column j of S, half of its rows
+    const int q = warp & 3, half = warp >> 2;
+    const int j = q * 32 + lane;
+    const int Dh = D / 2;
+    const int i0 = half * Dh;
+    const bool active = j < D;
+    float s[64], bn[64];
+#pragma unroll
+    for (int ii = 0; ii < 64; ++ii) {
+      s[ii] = 0.f;
+      bn[ii] = 0.f;
+    }
+    if (active && a.state_in) {
+      const float* si = a.state_in + (size_t)bh * D * D;
+#pragma unroll
+      for (int ii = 0; ii < 64; ++ii)
+        if (ii < Dh) s[ii] = si[(size_t)(i0 + ii) * D + j];
+    }
+    auto load_b = [&](int t) {
+      const float* bp = a.b_mat + (size_t)(bh * T + t) * D * D;
+#pragma unroll
+      for (int ii = 0; ii < 64; ++ii)
+        if (ii < Dh && active) bn[ii] = __ldg(bp + (size_t)(i0 + ii) * D + j);
+    };
+    // S^T image row j, columns [i0, i0 + Dh): hi and lo parts
+    auto write_img = [&]() {
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        if (c * 8 < Dh) {
+          const int col = i0 + c * 8;
+          const int at = col / 64;
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split2(s[c * 8 + 2 * e], s[c * 8 + 2 * e + 1], hi[e], lo[e]);
+          const uint32_t off = sw128_off(j, col % 64);
+          *reinterpret_cast<uint4*>(img + at * kImgRegion + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(img + (NA + at) * kImgRegion + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
+        }
+      }
+    };
+    write_img();  // S_0 (zeros for rows j >= D)
+    fence_proxy_async_smem();
+    named_barrier(1, 256);
+    if (threadIdx.x == 0) mbar_arrive(smem_u32(sready));
+    if (T > 0) load_b(0);
+    for (int t = 0; t < T; ++t) {
+      const long long f = bh * T + t;
+      const float gt = __ldg(a.g + f);
+      const bool ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(accfull), t & 1, abort_flag, a.status));
+      if (ok) {
+        tc_fence_after();
+        const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + i0;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 16) {
+          if (c0 < Dh) {
+            float p[16];
+            tmem_ld16(acc + c0, p);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; ++u)
+              if (c0 + u < Dh) s[c0 + u] = fmaf(gt, s[c0 + u] - p[u], bn[c0 + u]);
+          }
+        }
+        if (t + 1 < T) load_b(t + 1);
+      }
+      tc_fence_before();
+      if (threadIdx.x == 0) bulk_wait_read0();  // the previous S image copy has read smem
+      if (barrier_any(1, 256, !ok || *abort_flag)) goto done;
+      write_img();
+      fence_proxy_async_smem();
+      named_barrier(1, 256);
+      if (threadIdx.x == 0) {
+        uint8_t* dst = a.s_img + (size_t)f * 2 * NA * D * 128;
+        for (int r = 0; r < 2 * NA; ++r) bulk_s2g(dst + (size_t)r * D * 128, smem_u32(img + r * kImgRegion), D * 128);
+        bulk_commit();
+        mbar_arrive(smem_u32(sready));
+      }
+    }
+    if (active && a.state_out) {
+      float* so = a.state_out + (size_t)bh * D * D;
+#pragma unroll
+      for (int ii = 0; ii < 64; ++ii)
+        if (ii < Dh) so[(size_t)(i0 + ii) * D + j] = s[ii];
+    }
+  }
+done:
+  if (threadIdx.x == 0) bulk_wait0();  // S image copies complete
+  if (warp == 9 && lane == 0) {
+    mma_commit(smem_u32(mma_done));
+    wait_bounded(smem_u32(mma_done), 0, 500000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 9) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 128);
+  }
+}
+
+// =============================================================================
+// readout: O_t^T = S_t^T Q_t^T per frame-head and 128-token tile.
+// =============================================================================
+struct OutArgs {
+  const uint8_t* s_img;
+  long long nitems;
+  int S, D, NA, n_abuf;
+  float scale;
+  unsigned int* status;
+};
+
+__global__ void __launch_bounds__(kOutThreads, 1)
+    tc_readout_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapO, OutArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int NA = a.NA, D = a.D, S = a.S, NB = a.n_abuf;
+  const int img_bytes = 2 * NA * kImgRegion;           // one S^T image (hi, lo)
+  const int q_bytes = NA * kOutTok * 128;              // one Q tile
+  uint8_t* imgs = smem;
+  uint8_t* qst = imgs + NB * img_bytes;
+  uint8_t* stg = qst + kOutQStages * q_bytes;          // output staging: NA atoms of 128 rows
+  uint64_t* bars = reinterpret_cast<uint64_t*>(stg + NA * kOutTok * 128);
+  uint64_t* afull = bars;
+  uint64_t* aempty = bars + 2;
+  uint64_t* qfull = bars + 4;
+  uint64_t* qempty = qfull + kOutQStages;
+  uint64_t* accfull = qempty + kOutQStages;
+  uint64_t* accempty = accfull + kOutAcc;
+  uint64_t* mma_done = accempty + kOutAcc;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&afull[b]), 1);
+      mbar_init(smem_u32(&aempty[b]), 1);
+    }
+    for (int s = 0; s < kOutQStages; ++s) {
+      mbar_init(smem_u32(&qfull[s]), 1);
+      mbar_init(smem_u32(&qempty[s]), 1);
+    }
+    for (int b = 0; b < kOutAcc; ++b) {
+      mbar_init(smem_u32(&accfull[b]), 1);
+      mbar_init(smem_u32(&accempty[b]), 4);
+    }
+    mbar_init(smem_u32(mma_done), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // S images hold D rows; rows D..127 of every region are zero (they only feed
+  // accumulator rows that are never stored).
+  for (int idx = threadIdx.x; idx < NB * img_bytes / 16; idx += blockDim.x)
+    reinterpret_cast<uint4*>(imgs)[idx] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ntiles = (S + kOutTok - 1) / kOutTok;
+
+  if (warp == 4) {
+    // ---------------- producer: S image per item, Q tiles per tile
+    if (lane == 0) {
+      prefetch_tmap(&mapQ);
+      Ring<2> ra;  // S images (NB <= 2 slots in use)
+      Ring<kOutQStages> rq;
+      bool ok = true;
+      for (long long f = blockIdx.x; ok && f < a.nitems; f += gridDim.x) {
+        if (!wait_or_abort(smem_u32(&aempty[ra.stage]), ra.phase ^ 1, abort_flag, a.status)) break;
+        const uint32_t afb = smem_u32(&afull[ra.stage]);
+        mbar_arrive_expect_tx(afb, 2 * NA * D * 128);
+        const uint8_t* src = a.s_img + (size_t)f * 2 * NA * D * 128;
+        for (int r = 0; r < 2 * NA; ++r)
+          bulk_g2s(smem_u32(imgs + ra.stage * img_bytes + r * kImgRegion), src + (size_t)r * D * 128, D * 128, afb);
+        ra.mark_issued();
+        if (++ra.stage == NB) { ra.stage = 0; ra.phase ^= 1; }
+        for (int tile = 0; tile < ntiles; ++tile) {
+          if (!wait_or_abort(smem_u32(&qempty[rq.stage]), rq.phase ^ 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t qfb = smem_u32(&qfull[rq.stage]);
+          mbar_arrive_expect_tx(qfb, q_bytes);
+          for (int at = 0; at < NA; ++at)
+            tma_load_3d(smem_u32(qst + rq.stage * q_bytes + at * kOutTok * 128), &mapQ, qfb, 64 * at,
+                        tile * kOutTok, (int)f);
+          rq.mark_issued();
+          rq.advance();
+        }
+      }
+      ra.drain(afull);
+      rq.drain(qfull);
+    }
+  } else if (warp == 5) {
+    // ---------------- MMA
+    if (lane == 0) {
+      const uint32_t id = idesc_bf16(128, kOutTok, 0, 0);
+      int ab = 0;
+      uint32_t aphase = 0;
+      int qs = 0;
+      uint32_t qphase = 0;
+      int cb = 0;
+      uint32_t cphase = 0;
+      for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+        if (!wait_or_abort(smem_u32(&afull[ab]), aphase, abort_flag, a.status)) goto done;
+        const uint32_t im = smem_u32(imgs + ab * img_bytes);
+        for (int tile = 0; tile < ntiles; ++tile) {
+          if (!wait_or_abort(smem_u32(&accempty[cb]), cphase ^ 1, abort_flag, a.status)) goto done;
+          if (!wait_or_abort(smem_u32(&qfull[qs]), qphase, abort_flag, a.status)) goto done;
+          tc_fence_after();
+          const uint32_t qb = smem_u32(qst + qs * q_bytes);
+          const uint32_t acc = tmem + cb * kOutTok;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const int at = kk / 4;
+            const uint32_t ko = (kk % 4) * 32;
+            const uint64_t bdesc = smem_desc(qb + at * kOutTok * 128 + ko, 16, 1024);
+            mma_bf16(acc, smem_desc(im + at * kImgRegion + ko, 16, 1024), bdesc, id, kk > 0 ? 1u : 0u);
+            mma_bf16(acc, smem_desc(im + (NA + at) * kImgRegion + ko, 16, 1024), bdesc, id, 1u);
+          }
+          mma_commit(smem_u32(&qempty[qs]));
+          mma_commit(smem_u32(&accfull[cb]));
+          if (++qs == kOutQStages) { qs = 0; qphase ^= 1; }
+          if (++cb == kOutAcc) { cb = 0; cphase ^= 1; }
+        }
+        mma_commit(smem_u32(&aempty[ab]));
+        if (++ab == NB) { ab = 0; aphase ^= 1; }
+      }
+    }
+  } else {
+    // ---------------- epilogue: thread = output column j, 128 tokens per tile
+    const int j = warp * 32 + lane;
+    int cb = 0;
+    uint32_t cphase = 0;
+    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+      for (int tile = 0; tile < ntiles; ++tile) {
+        if (threadIdx.x == 0) bulk_wait_read0();  // staging buffer free again
+        if (barrier_any(1, 128, *abort_flag)) goto done;
+        const bool ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[cb]), cphase, abort_flag, a.status));
+        if (ok) {
+          tc_fence_after();
+          const uint32_t acc = tmem + ((uint32_t)(warp * 32) << 16) + cb * kOutTok;
+          uint8_t* sreg = stg + (j / 64) * kOutTok * 128;
+          for (int c0 = 0; c0 < kOutTok; c0 += 16) {
+            float v[16];
+            tmem_ld16(acc + c0, v);
+            tmem_ld_wait();
+            if (j < D) {
+#pragma unroll
+              for (int u = 0; u < 16; ++u)
+                *reinterpret_cast<__nv_bfloat16*>(sreg + sw128_off(c0 + u, j % 64)) =
+                    __float2bfloat16_rn(v[u] * a.scale);
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&accempty[cb]));
+        }
+        if (++cb == kOutAcc) { cb = 0; cphase ^= 1; }
+        fence_proxy_async_smem();
+        if (barrier_any(1, 128, !ok || *abort_flag)) goto done;
+        if (threadIdx.x == 0) {
+          for (int at = 0; at < NA; ++at)
+            tma_store_3d(&mapO, smem_u32(stg + at * kOutTok * 128), 64 * at, tile * kOutTok, (int)f);
+          bulk_commit();
+        }
+      }
+    }
+  }
+done:
+  if (threadIdx.x == 0) bulk_wait0();  // output stores complete
+  if (warp == 5 && lane == 0) {
+    mma_commit(smem_u32(mma_done));
+    wait_bounded(smem_u32(mma_done), 0, 500000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (!cache[dev]) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+constexpr int kBarBytes = 256;
+
+// Kernels that allocate all 512 TMEM columns ask for more than half of the SM's
+// shared memory so that two of them never share an SM.
+constexpr int kOneCtaPerSm = 116 * 1024;
+int at_least_half(int b) { return b > kOneCtaPerSm ? b : kOneCtaPerSm; }
+int gram_smem(int NA) { return at_least_half(kGramStages * (2 * NA + 4) * kGramRegion + kBarBytes + 1024); }
+int scan_smem(int NA, int D) { return 2 * NA * kImgRegion + kScanStages * NA * D * 128 + kBarBytes + 1024; }
+int out_smem(int NA, int nb) {
+  return at_least_half(nb * 2 * NA * kImgRegion + kOutQStages * NA * kOutTok * 128 + NA * kOutTok * 128 + kBarBytes +
+                       1024);
+}
+constexpr int kMaxSmem = 227 * 1024;
+
+}  // namespace
+
+size_t tc_workspace_bytes(const Problem& p, int mode) {
+  if (mode != 0) return simt_workspace_bytes(p, mode);
+  return tc_layout(p).total;
+}
+
+int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
+  if (p.mode != 0) return simt_forward(p, ws, st);  // prefix form: SIMT kernels for now
+  const TcLayout L = tc_layout(p);
+  const int NA = num_atoms(p.D);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint8_t* m_img = w + L.m_off;
+  float* b_mat = reinterpret_cast<float*>(w + L.b_off);
+  uint8_t* s_img = w + L.s_off;
+  const long long F = p.BHT();
+  const int nsm = num_sms();
+
+  CUtensorMap mapK, mapV, mapQ, mapO;
+  if (!make_map(&mapK, p.k, p.D, p.S, F, kGramTok) || !make_map(&mapV, p.v, p.D, p.S, F, kGramTok) ||
+      !make_map(&mapQ, p.q, p.D, p.S, F, kOutTok) || !make_map(&mapO, p.out, p.D, p.S, F, kOutTok))
+    return kCuda;
+
+  {
+    const int smem = gram_smem(NA);
+    if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return kCuda;
+    GramArgs ga{p.beta, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale, p.key_scale, p.status};
+    const unsigned grid = (unsigned)(F < nsm ? F : nsm);
+    ProfScope ps(st, "tc_gram");
+    tc_gram_kernel<<<grid, kGramThreads, smem, st>>>(mapK, mapV, ga);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  {
+    const int smem = scan_smem(NA, p.D);
+    if (cudaFuncSetAttribute(tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return kCuda;
+    ScanArgs sa{m_img, b_mat, p.g, p.state_in, s_img, p.state_out, p.T, p.D, NA, p.status};
+    ProfScope ps(st, "tc_scan");
+    tc_scan_kernel<<<(unsigned)p.BH(), kScanThreads, smem, st>>>(sa);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  {
+    const int nb = out_smem(NA, 2) <= kMaxSmem ? 2 : 1;
+    const int smem = out_smem(NA, nb);
+    if (cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return kCuda;
+    OutArgs oa{s_img, F, p.S, p.D, NA, nb, p.out_scale, p.status};
+    const unsigned grid = (unsigned)(F < nsm ? F : nsm);
+    ProfScope ps(st, "tc_readout");
+    tc_readout_kernel<<<grid, kOutThreads, smem, st>>>(mapQ, mapO, oa);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  return kOk;
+}
+
 }  // namespace gdn

@@ -3,11 +3,20 @@ tolerance checks.
 
 Tolerances (written here, used by every parity test):
   * float32 I/O: max |gpu - oracle| <= 1e-4, for out and for the final state.
-  * bf16 I/O: max |gpu - oracle| / rms(oracle) <= 2e-2, per tensor (out and the
-    final state separately).  rms(gpu - oracle) / rms(oracle) is reported too.
-    Rounding the outputs to bf16 alone costs up to 2^-8 relative at the largest
-    elements (about 0.016 of the RMS on the 720p-shaped workloads), so the
-    kernels' own error has to stay well below the remaining margin.
+  * bf16 I/O, strict (the five named workloads): max |gpu - oracle| / rms(oracle)
+    <= 2e-2, per tensor (out and the final state separately).
+  * bf16 I/O, edge shapes (arbitrary initial states and shapes): an element of a
+    bf16 output can never be closer to the exact value than half a bf16 ulp, and
+    when the output's distribution is heavy-tailed (e.g. a large initial state
+    dominating the first frames) that representation error alone exceeds
+    2e-2 x rms at the largest elements.  There the bound is
+    |gpu - oracle| <= 0.5 ulp_bf16(oracle) + 2e-2 x rms(oracle) per element.
+  * bf16 I/O, always: rms(gpu - oracle) / rms(oracle) <= 5e-3.  Derivation: RNE
+    rounding of the outputs gives ~1.6e-3 (uniform error of up to 2^-9 relative,
+    averaged over the significand range); the kernels' bf16 hi+lo operand splits
+    add < 1e-4; single-bf16 operands where a split is needed would add ~1e-3 on
+    top and still pass, a wrong or dropped term would not.
+The final state is float32 and always held to the strict bound.
 """
 from __future__ import annotations
 
@@ -19,6 +28,7 @@ from linear_attention_video_gated_b300 import binding, synth
 
 F32_MAX_ABS = 1e-4
 BF16_MAX_ABS_OVER_RMS = 2e-2
+BF16_RMS_ERR_OVER_RMS = 5e-3
 
 
 def torch_dtype(wl):
@@ -69,33 +79,46 @@ def oracle_head(wl, b, h, S0=None):
     return oracle.scan_head(x["q"], x["k"], x["v"], x["g"], x["beta"], S0)
 
 
+def half_ulp_bf16(x):
+    """Half the bf16 spacing at |x| (bf16 has 8 significand bits)."""
+    ax = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.where(ax > 0, ax, 1.0)))
+    return np.where(ax > 0, 2.0 ** (e - 8), 0.0)
+
+
 def errors(gpu, ref):
     gpu = np.asarray(gpu, np.float64)
     ref = np.asarray(ref, np.float64)
     d = np.abs(gpu - ref)
     rms = float(np.sqrt(np.mean(ref ** 2))) if ref.size else 0.0
+    excess = np.maximum(d - half_ulp_bf16(ref), 0.0)
     return {"max_abs": float(d.max()) if d.size else 0.0, "rms_ref": rms,
             "max_abs_over_rms": float(d.max()) / rms if rms > 0 else 0.0,
+            "max_beyond_half_ulp_over_rms": float(excess.max()) / rms if rms > 0 and d.size else 0.0,
             "rms_err_over_rms": float(np.sqrt(np.mean(d ** 2))) / rms if rms > 0 else 0.0,
             "finite": bool(np.all(np.isfinite(gpu)))}
 
 
-def assert_parity(wl_dtype, out_gpu, out_ref, st_gpu, st_ref, what=""):
+def assert_parity(wl_dtype, out_gpu, out_ref, st_gpu, st_ref, what="", strict=True):
+    """strict=True: the named workloads' bound; strict=False: edge shapes, with the
+    half-ulp representation allowance on bf16 outputs (see the module docstring)."""
     eo = errors(out_gpu, out_ref)
     es = errors(st_gpu, st_ref)
     assert eo["finite"] and es["finite"], f"{what}: non-finite values"
     if wl_dtype == "f32":
         assert eo["max_abs"] <= F32_MAX_ABS, f"{what}: out {eo}"
         assert es["max_abs"] <= F32_MAX_ABS, f"{what}: state {es}"
+        return eo, es
+    if eo["rms_ref"] > 0:
+        key = "max_abs_over_rms" if strict else "max_beyond_half_ulp_over_rms"
+        assert eo[key] <= BF16_MAX_ABS_OVER_RMS, f"{what}: out {eo}"
+        assert eo["rms_err_over_rms"] <= BF16_RMS_ERR_OVER_RMS, f"{what}: out {eo}"
     else:
-        if eo["rms_ref"] > 0:
-            assert eo["max_abs_over_rms"] <= BF16_MAX_ABS_OVER_RMS, f"{what}: out {eo}"
-        else:
-            assert eo["max_abs"] == 0.0, f"{what}: out {eo}"
-        if es["rms_ref"] > 0:
-            assert es["max_abs_over_rms"] <= BF16_MAX_ABS_OVER_RMS, f"{what}: state {es}"
-        else:
-            assert es["max_abs"] == 0.0, f"{what}: state {es}"
+        assert eo["max_abs"] == 0.0, f"{what}: out {eo}"
+    if es["rms_ref"] > 0:
+        assert es["max_abs_over_rms"] <= BF16_MAX_ABS_OVER_RMS, f"{what}: state {es}"
+    else:
+        assert es["max_abs"] == 0.0, f"{what}: state {es}"
     return eo, es
 
 
