@@ -188,21 +188,37 @@ def test_minute_chunked_rollout(minute_inputs, minute_oracle):
 
 
 def test_large_sequential_and_prefix_agree():
-    """4 x 16 heads, 241 frames of 3600 tokens, d128: the sequential scan and the
-    chunked prefix composition agree everywhere, and sampled heads match the oracle."""
+    """4 x 16 heads, 241 frames of 3600 tokens, d128: sampled heads of both the
+    sequential scan and the chunked prefix composition match the oracle, and the
+    two forms agree everywhere.
+
+    Agreement of two bf16 outputs: each form rounds its own fp32 value, so the two
+    may land on adjacent bf16 values even when both are within the bound of the
+    exact result; one bf16 ulp of |out| is the smallest difference the output type
+    can show.  The element-wise bound is therefore |a - b| <= ulp_bf16 + 2e-2 rms;
+    the fp32 final states are held to the plain 2e-2 rms bound."""
     wl = synth.WORKLOADS["large"]
     ins = parity.device_inputs(wl)
     out0, st0 = run(*ins, mode=0)
     out1, st1 = run(*ins, mode=1)
     del ins
-    rms_o = torch.sqrt(torch.mean(out0.float() ** 2)).item()
-    rms_s = torch.sqrt(torch.mean(st0 ** 2)).item()
-    d_o = 0.0
-    for b in range(wl.B):
-        d_o = max(d_o, (out0[b].float() - out1[b].float()).abs().max().item())
-    d_s = (st0 - st1).abs().max().item()
-    print(f"large: seq vs prefix out max-abs/rms {d_o / rms_o:.3e}, state {d_s / rms_s:.3e}")
-    assert d_o / rms_o <= parity.BF16_MAX_ABS_OVER_RMS and d_s / rms_s <= parity.BF16_MAX_ABS_OVER_RMS
     ref = {bh: parity.oracle_head(wl, *bh) for bh in synth.head_sample(wl, 2)}
     _check_heads(wl, out0, st0, ref, "large seq")
     _check_heads(wl, out1, st1, ref, "large prefix")
+    rms_o = torch.sqrt(torch.mean(out0.float() ** 2)).item()
+    rms_s = torch.sqrt(torch.mean(st0 ** 2)).item()
+    beyond, sq = 0.0, 0.0
+    for b in range(wl.B):
+        a, c = out0[b].float(), out1[b].float()
+        m = torch.maximum(a.abs(), c.abs())
+        ulp = torch.where(m > 0, torch.exp2(torch.floor(torch.log2(torch.where(m > 0, m, 1.0))) - 7), 0.0)
+        d = (a - c).abs()
+        beyond = max(beyond, (d - ulp).clamp_min(0.0).max().item())
+        sq += (d.double() ** 2).sum().item()
+    rms_d = (sq / out0.numel()) ** 0.5
+    d_s = (st0 - st1).abs().max().item()
+    print(f"large: seq vs prefix out beyond-1-ulp/rms {beyond / rms_o:.3e}, rms diff/rms {rms_d / rms_o:.3e}, "
+          f"state max/rms {d_s / rms_s:.3e}")
+    assert beyond / rms_o <= parity.BF16_MAX_ABS_OVER_RMS
+    assert rms_d / rms_o <= parity.BF16_RMS_ERR_OVER_RMS
+    assert d_s / rms_s <= parity.BF16_MAX_ABS_OVER_RMS
