@@ -135,6 +135,41 @@ const char* gdn_status_string(int status);
 int gdn_version(void);
 
 /*
+ * gdn_frame_fwd_noalloc -- gdn_frame_fwd for callers that cannot allocate
+ * device memory.  (No counterpart on the pages: this is a property of the
+ * library, not of the method.)
+ *
+ * Some callers cannot call cudaMalloc: code plugged into another runtime whose
+ * caching allocator already owns the GPU's memory (a raw cudaMalloc would fail
+ * or fragment that pool), and latency-critical loops in which an allocation or
+ * a free that synchronises the device would stall other streams.  This entry
+ * point takes the same arguments as gdn_frame_fwd and runs the same kernels
+ * (GDN_MODE_SEQUENTIAL), but it calls no cudaMalloc, cudaFree or other
+ * allocating routine: its scratch is one fixed array of
+ * gdn_noalloc_scratch_bytes() bytes (64 MiB) in the library's own device
+ * memory, which every GPU that loads the library holds until the process exits.
+ *   - Shapes whose scratch (gdn_workspace_bytes(..., GDN_MODE_SEQUENTIAL)) is
+ *     larger than that are rejected with GDN_ERR_WORKSPACE before any CUDA call.
+ *     At D = 112 that is about 490 frame-heads per call, e.g. 20 heads
+ *     x 24 frames: chunk-causal rollouts of a few frames per call fit.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - Every call, on every stream, shares the one array, and it keeps the last
+ *     call's contents (each call writes its scratch before reading it, so nothing
+ *     needs clearing).  Calls that overlap on the GPU race on it: serialise them
+ *     (one stream, or events between streams).
+ * Returns as gdn_frame_fwd.
+ */
+int gdn_frame_fwd_noalloc(const void* q, const void* k, const void* v,
+                          const float* g, const float* beta, const float* state_in,
+                          void* out, float* state_out,
+                          int B, int H, int T, int S, int D, int dtype, void* stream);
+
+/* gdn_noalloc_scratch_bytes -- size of gdn_frame_fwd_noalloc's fixed scratch. */
+size_t gdn_noalloc_scratch_bytes(void);
+
+/*
  * Per-kernel timing (a tracing aid; no counterpart on the pages).
  * Between gdn_profile_begin() and gdn_profile_end(), every kernel launch the
  * library makes in this process is bracketed by two CUDA events recorded on

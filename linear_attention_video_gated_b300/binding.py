@@ -28,6 +28,8 @@ _SIGS = {
     "gdn_frame_fwd_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                               ctypes.c_size_t, _P]),
     "gdn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
+    "gdn_frame_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    "gdn_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "gdn_last_error": (_I, [_P]),
     "gdn_status_string": (ctypes.c_char_p, [_I]),
     "gdn_version": (_I, []),
@@ -71,6 +73,14 @@ def gdn_frame_fwd_ex(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, 
                      workspace, workspace_bytes, stream) -> int:
     return lib().gdn_frame_fwd_ex(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode,
                                   workspace, workspace_bytes, stream)
+
+
+def gdn_frame_fwd_noalloc(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, stream) -> int:
+    return lib().gdn_frame_fwd_noalloc(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, stream)
+
+
+def gdn_noalloc_scratch_bytes() -> int:
+    return lib().gdn_noalloc_scratch_bytes()
 
 
 def gdn_workspace_bytes(B, H, T, S, D, dtype, mode) -> int:
