@@ -62,7 +62,7 @@ def kernel_alg_bytes(name: str, wl) -> int | None:
         return fh * (2 * wl.S * wl.D * e + 4 * wl.S + 4)
     if name.endswith("_readout"):
         return fh * 2 * wl.S * wl.D * e
-    if name.endswith("_fused"):
+    if "_fused" in name:
         return alg_bytes(wl)
     return None
 
@@ -226,7 +226,7 @@ def config_of(wl, mode) -> dict:
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} T={wl.T} S={wl.S} D={wl.D} {wl.dtype} I/O, fp32 state, "
                         f"single call over all frames",
             "B": wl.B, "H": wl.H, "T": wl.T, "S": wl.S, "D": wl.D,
-            "mode": {0: "sequential", 1: "prefix"}[mode],
+            "mode": {0: "sequential", 1: "prefix", 2: "split", 3: "cluster"}[mode],
             "l2": f"no flush: inputs larger than L2 ({alg_bytes(wl) / 1e9:.1f} GB moved per step vs 126 MB L2)"}
 
 
@@ -404,7 +404,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="minute", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--mode", type=int, default=0, choices=[0, 1])
+    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -72,14 +72,25 @@ typedef enum {
 } gdn_status_t;
 
 typedef enum {
-  /* One pass over the frames per head: per-frame transition terms are formed in
-   * parallel, the D x D recurrence runs frame by frame, outputs in parallel. */
+  /* One pass over the frames per head: the library's fastest form for the
+   * shape and dtype (currently the split form below). */
   GDN_MODE_SEQUENTIAL = 0,
   /* Chunked prefix composition of the affine maps (A_t, b_t) across frames:
    * per-chunk composed maps in parallel, a short scan over chunk boundaries,
    * then every chunk replayed from its true initial state (zhichai.net summary,
    * training pipeline Stage 3).  Same result up to rounding. */
-  GDN_MODE_PREFIX = 1
+  GDN_MODE_PREFIX = 1,
+  /* Three kernels through a workspace: the per-frame transition terms
+   * (M_t = K~^T diag(beta) K~, b_t = K~^T diag(beta) V_t) for all frames in
+   * parallel, the serial D x D recurrence, then the read-out for all frames in
+   * parallel. */
+  GDN_MODE_SPLIT = 2,
+  /* bf16 I/O only: one fused kernel, one thread-block cluster per head split
+   * over its value columns (columns of the state evolve independently), K and
+   * Q tiles multicast to the cluster, every stage of a frame on chip; no
+   * workspace.  Slower than the split form on B300 (its tile rings are shared
+   * by the whole cluster, so too few bytes are in flight per head). */
+  GDN_MODE_CLUSTER = 3
 } gdn_mode_t;
 
 /*
@@ -91,8 +102,9 @@ typedef enum {
  *   state_out : final state S_{T-1} or NULL.
  *   dtype     : gdn_dtype_t.
  * Uses GDN_MODE_SEQUENTIAL.  Its scratch memory (gdn_workspace_bytes()) is
- * taken with cudaMallocAsync on `stream` and released with cudaFreeAsync on
- * the same stream, so nothing persists past the call.
+ * taken with cudaMallocAsync on
+ * `stream` and released with cudaFreeAsync on the same stream, so nothing
+ * persists past the call.
  */
 int gdn_frame_fwd(const void* q, const void* k, const void* v,
                   const float* g, const float* beta, const float* state_in,
@@ -143,12 +155,13 @@ int gdn_version(void);
  * caching allocator already owns the GPU's memory (a raw cudaMalloc would fail
  * or fragment that pool), and latency-critical loops in which an allocation or
  * a free that synchronises the device would stall other streams.  This entry
- * point takes the same arguments as gdn_frame_fwd and runs the same kernels
- * (GDN_MODE_SEQUENTIAL), but it calls no cudaMalloc, cudaFree or other
- * allocating routine: its scratch is one fixed array of
+ * point takes the same arguments as gdn_frame_fwd and runs the split form
+ * (GDN_MODE_SPLIT, the form whose kernels use scratch memory), but it calls no
+ * cudaMalloc, cudaFree or other allocating routine: its scratch is one fixed
+ * array of
  * gdn_noalloc_scratch_bytes() bytes (64 MiB) in the library's own device
  * memory, which every GPU that loads the library holds until the process exits.
- *   - Shapes whose scratch (gdn_workspace_bytes(..., GDN_MODE_SEQUENTIAL)) is
+ *   - Shapes whose scratch (gdn_workspace_bytes(..., GDN_MODE_SPLIT)) is
  *     larger than that are rejected with GDN_ERR_WORKSPACE before any CUDA call.
  *     At D = 112 that is about 490 frame-heads per call, e.g. 20 heads
  *     x 24 frames: chunk-causal rollouts of a few frames per call fit.

@@ -36,7 +36,8 @@ int validate(const void* q, const void* k, const void* v, const float* g, const 
              int mode, Problem* p) {
   if (B < 1 || H < 1 || T < 0 || S < 1 || D < 1) return kInvalidArg;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return kInvalidArg;
-  if (mode != GDN_MODE_SEQUENTIAL && mode != GDN_MODE_PREFIX) return kInvalidArg;
+  if (mode < GDN_MODE_SEQUENTIAL || mode > GDN_MODE_CLUSTER) return kInvalidArg;
+  if (mode == GDN_MODE_CLUSTER && dtype != GDN_BF16) return kUnsupported;
   if (D % 16 != 0 || D > 128) return kUnsupported;
   // Counts must stay inside what the kernels index with 64-bit offsets and
   // 32-bit grid dimensions / tensor-map extents.
@@ -245,9 +246,9 @@ int gdn_profile_end(gdn_kernel_stat_t* stats, int max_stats, int* n_stats) {
 
 // ---- entry point that allocates nothing ------------------------------------------
 //
-// gdn_frame_fwd_noalloc runs the same kernels as gdn_frame_fwd, but its scratch
-// is a fixed array in the library's own device memory instead of memory taken
-// from an allocator.  It exists for callers that cannot call cudaMalloc: code
+// gdn_frame_fwd_noalloc runs the split form (the kernels that use scratch), but
+// its scratch is a fixed array in the library's own device memory instead of
+// memory taken from an allocator.  It exists for callers that cannot call cudaMalloc: code
 // plugged into another runtime that owns the device memory (its caching
 // allocator has reserved the HBM, so a raw cudaMalloc fails or fragments the
 // pool), and latency-critical loops in which an allocation or free that
@@ -283,7 +284,7 @@ extern "C" int gdn_frame_fwd_noalloc(const void* q, const void* k, const void* v
                                      const float* beta, const float* state_in, void* out, float* state_out, int B,
                                      int H, int T, int S, int D, int dtype, void* stream) {
   gdn::Problem p{};
-  int rc = gdn::validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, GDN_MODE_SEQUENTIAL, &p);
+  int rc = gdn::validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, GDN_MODE_SPLIT, &p);
   if (rc != gdn::kOk) return rc;
   // Every stage writes its scratch before reading it, so the previous call's
   // contents never need clearing.

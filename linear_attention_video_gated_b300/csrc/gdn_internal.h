@@ -57,6 +57,10 @@ int simt_forward(const Problem& p, void* ws, cudaStream_t st);
 size_t tc_workspace_bytes(const Problem& p, int mode);
 int tc_forward(const Problem& p, void* ws, cudaStream_t st);
 
+// ---- fused tensor-core path (bf16 I/O, one cluster per head, no scratch) ---------
+bool fused_supported(const Problem& p);
+int fused_forward(const Problem& p, cudaStream_t st);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Brackets one kernel launch with CUDA events while gdn_profile_begin() is in

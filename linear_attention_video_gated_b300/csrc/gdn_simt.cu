@@ -362,7 +362,7 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
 
-  if (p.mode == 0) {
+  if (p.mode != 1) {  // sequential and split forms are the same three stages here
     const size_t smem = 2 * mat;
     if (cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return kCuda;

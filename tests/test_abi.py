@@ -64,12 +64,13 @@ def _call(B=1, H=2, T=3, S=17, D=32, dtype=1, ptr=A16, g=A16, beta=A16, out=A16,
 
 @pytest.mark.parametrize("kw,code", [
     (dict(B=0), 1), (dict(H=0), 1), (dict(T=-1), 1), (dict(S=0), 1), (dict(D=0), 1),
-    (dict(dtype=2), 1), (dict(mode=2), 1),
+    (dict(dtype=2), 1), (dict(mode=4), 1), (dict(mode=-1), 1), (dict(mode=3, dtype=0), 2),
     (dict(D=24), 2), (dict(D=144), 2), (dict(D=8), 2),
     (dict(ptr=None), 1), (dict(g=None), 1), (dict(beta=None), 1), (dict(out=None), 1),
     (dict(ptr=MIS), 3), (dict(out=MIS), 3), (dict(g=A16 + 2), 3), (dict(state_in=MIS), 3),
     (dict(state_out=MIS), 3),
-    (dict(ws=None), 6), (dict(wsb=16), 6), (dict(ws=A16 + 16), 3),
+    (dict(ws=None, mode=2), 6), (dict(wsb=16, mode=2), 6), (dict(ws=A16 + 16, mode=2), 3),
+    (dict(ws=None, mode=1), 6), (dict(ws=None, dtype=0), 6),
 ])
 def test_validation_rejects(lib, kw, code):
     assert _call(**kw) == code
@@ -81,13 +82,20 @@ def test_validation_rejects_plain_entry(lib):
 
 
 def test_workspace_bytes_is_pure_and_scales(lib):
-    a = binding.gdn_workspace_bytes(1, 20, 961, 880, 112, 1, 0)
-    assert a > 0 and a == binding.gdn_workspace_bytes(1, 20, 961, 880, 112, 1, 0)
-    assert binding.gdn_workspace_bytes(1, 20, 0, 880, 112, 1, 0) == 0
-    assert binding.gdn_workspace_bytes(1, 20, 961, 880, 24, 1, 0) == 0
+    a = binding.gdn_workspace_bytes(1, 20, 961, 880, 112, 1, 2)
+    assert a > 0 and a == binding.gdn_workspace_bytes(1, 20, 961, 880, 112, 1, 2)
+    assert binding.gdn_workspace_bytes(1, 20, 0, 880, 112, 1, 2) == 0
+    assert binding.gdn_workspace_bytes(1, 20, 961, 880, 24, 1, 2) == 0
     assert binding.gdn_workspace_bytes(1, 20, 961, 880, 112, 1, 1) >= a
-    assert binding.gdn_workspace_bytes(2, 20, 961, 880, 112, 1, 0) >= a
+    assert binding.gdn_workspace_bytes(2, 20, 961, 880, 112, 1, 2) >= a
     assert binding.gdn_workspace_bytes(1, 2, 8, 16, 16, 0, 0) > 0
+
+
+@pytest.mark.parametrize("D", [16, 32, 48, 64, 80, 96, 112, 128])
+def test_cluster_form_needs_no_workspace(lib, D):
+    """The cluster form keeps every stage of a frame on chip: no scratch."""
+    assert binding.gdn_workspace_bytes(4, 16, 241, 3600, D, 1, 3) == 0
+    assert binding.gdn_workspace_bytes(4, 16, 241, 3600, D, 1, 2) > 0
 
 
 def test_no_gpu_call_fails_loudly_not_silently(lib):

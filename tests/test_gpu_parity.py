@@ -30,7 +30,7 @@ def np_(t):
     return t.float().cpu().numpy()
 
 
-@pytest.mark.parametrize("mode", [None, 0, 1])
+@pytest.mark.parametrize("mode", [None, 0, 1, 2])
 def test_tiny_f32(mode):
     wl = synth.WORKLOADS["tiny"]
     x = synth.full(wl)
@@ -39,7 +39,7 @@ def test_tiny_f32(mode):
     parity.assert_parity("f32", np_(out), ro, np_(st), rs, f"tiny mode={mode}")
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_short_bf16(mode):
     wl = synth.WORKLOADS["short"]
     x = synth.full(wl)
@@ -66,10 +66,12 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 @pytest.mark.parametrize("case", EDGE, ids=lambda c: "-".join(map(str, c)))
 def test_edge_shapes(case, mode):
     dt, B, H, T, S, D, nz = case
+    if mode == 3 and dt != "bf16":
+        pytest.skip("the cluster form is bf16 only")
     base = synth.WORKLOADS["short" if dt == "bf16" else "tiny"]
     wl = base.with_(B=B, H=H, T=T, S=S, D=D, seed=base.seed + 17 * S + D)
     x = synth.full(wl)
@@ -85,13 +87,14 @@ def _small_bf16(T=21, H=3, S=300, D=112):
     return wl, synth.full(wl)
 
 
-def test_state_aliasing_is_bitwise_identical():
+@pytest.mark.parametrize("mode", [0, 2, 3])
+def test_state_aliasing_is_bitwise_identical(mode):
     wl, x = _small_bf16()
     ins = parity.upload(wl, x)
     S0 = torch.from_numpy(np.stack([np.stack([synth.state(wl, 0, h) for h in range(wl.H)])])).cuda()
-    out_a, st_a = run(*ins, state_in=S0.clone(), mode=0)
+    out_a, st_a = run(*ins, state_in=S0.clone(), mode=mode)
     buf = S0.clone()
-    out_b, st_b = run(*ins, state_in=buf, state_out=buf, mode=0)
+    out_b, st_b = run(*ins, state_in=buf, state_out=buf, mode=mode)
     assert torch.equal(out_a, out_b) and torch.equal(st_a, buf)
 
 
@@ -107,11 +110,12 @@ def test_zero_frames_copies_state():
     assert torch.count_nonzero(st2) == 0
 
 
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
 def test_chunked_calls_equal_single_call(mode):
     """Chunk-causal rollout: consecutive calls passing state_out -> state_in give the
-    single call's outputs.  In sequential mode the per-frame arithmetic does not
-    depend on where the calls split, so the results are bitwise equal."""
+    single call's outputs.  In the sequential and split forms the per-frame
+    arithmetic does not depend on where the calls split, so the results are
+    bitwise equal."""
     wl, x = _small_bf16(T=21)
     q, k, v, g, beta = parity.upload(wl, x)
     out1, st1 = run(q, k, v, g, beta, mode=mode)
@@ -121,18 +125,19 @@ def test_chunked_calls_equal_single_call(mode):
         o, st = run(sl(q), sl(k), sl(v), sl(g), sl(beta), state_in=st, mode=mode)
         outs.append(o)
     out2 = torch.cat(outs, dim=2)
-    if mode == 0:
+    if mode in (0, 2, 3):
         assert torch.equal(out1, out2) and torch.equal(st1, st)
     else:
         ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"])
         parity.assert_parity("bf16", np_(out2), ro, np_(st), rs, "chunked prefix", strict=False)
 
 
-def test_repeat_calls_are_deterministic():
+@pytest.mark.parametrize("mode", [0, 2, 3])
+def test_repeat_calls_are_deterministic(mode):
     wl, x = _small_bf16(T=9)
     ins = parity.upload(wl, x)
-    a = run(*ins, mode=0)
-    b = run(*ins, mode=0)
+    a = run(*ins, mode=mode)
+    b = run(*ins, mode=mode)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
@@ -164,12 +169,13 @@ def _check_heads(wl, out, st, ref, what):
         print(f"{what} head {(b, h)}: out {eo} state {es}")
 
 
-def test_minute_single_call(minute_inputs, minute_oracle):
-    """961 frames x 880 tokens x 20 heads x d112, one call, in the bench's launch
-    configuration; sampled heads checked over every frame against the oracle."""
+@pytest.mark.parametrize("mode", [0, 3])
+def test_minute_single_call(minute_inputs, minute_oracle, mode):
+    """961 frames x 880 tokens x 20 heads x d112, one call (mode 0 is the bench's
+    launch configuration); sampled heads checked over every frame against the oracle."""
     wl, ins = minute_inputs
-    out, st = run(*ins, mode=0)
-    _check_heads(wl, out, st, minute_oracle, "minute")
+    out, st = run(*ins, mode=mode)
+    _check_heads(wl, out, st, minute_oracle, f"minute mode={mode}")
 
 
 def test_minute_chunked_rollout(minute_inputs, minute_oracle):

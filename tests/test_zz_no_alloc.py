@@ -1,9 +1,10 @@
 """gdn_frame_fwd_noalloc: the entry point for callers that cannot allocate device
 memory (for example code running inside another runtime whose allocator owns the
-GPU's memory).  It runs the same kernels as the allocating entry points with its
+GPU's memory).  It runs the split form (the kernels that use scratch) with its
 scratch in one fixed array inside the library, so these tests check that
 
-  * on the GPU, its results match gdn_frame_fwd_ex (caller-owned workspace) within
+  * on the GPU, its results match gdn_frame_fwd_ex (caller-owned workspace, same
+    form) within
     the parity tolerances of tests/parity.py, on two calls in a row with different
     shapes and data (the second call reuses the array the first one left behind);
   * on the host, a shape whose scratch does not fit in the array is rejected with
@@ -22,7 +23,7 @@ def test_oversized_shape_is_rejected_on_the_host():
     cap = binding.gdn_noalloc_scratch_bytes()
     assert cap == 64 << 20
     # 20 heads x 961 frames x 880 tokens x d112 needs ~2.6 GB of scratch.
-    need = binding.gdn_workspace_bytes(1, 20, 961, 880, 112, binding.GDN_BF16, binding.GDN_MODE_SEQUENTIAL)
+    need = binding.gdn_workspace_bytes(1, 20, 961, 880, 112, binding.GDN_BF16, binding.GDN_MODE_SPLIT)
     assert need > cap
     fake = 0x10000  # never dereferenced: the call fails before touching CUDA
     rc = binding.gdn_frame_fwd_noalloc(fake, fake, fake, fake, fake, None, fake, None,
@@ -49,7 +50,7 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
     ]
     for wl, nonzero in cases:
         dtype = binding.GDN_BF16 if wl.dtype == "bf16" else binding.GDN_F32
-        need = binding.gdn_workspace_bytes(wl.B, wl.H, wl.T, wl.S, wl.D, dtype, binding.GDN_MODE_SEQUENTIAL)
+        need = binding.gdn_workspace_bytes(wl.B, wl.H, wl.T, wl.S, wl.D, dtype, binding.GDN_MODE_SPLIT)
         assert 0 < need <= binding.gdn_noalloc_scratch_bytes()
         x = synth.full(wl)
         q, k, v, g, beta = parity.upload(wl, x)
@@ -66,7 +67,7 @@ def test_noalloc_matches_workspace_entry_on_two_calls_in_a_row():
         out_ref = torch.empty_like(q)
         st_ref = torch.empty((wl.B, wl.H, wl.D, wl.D), dtype=torch.float32, device="cuda")
         ws = torch.empty(need, dtype=torch.uint8, device="cuda")
-        rc = binding.gdn_frame_fwd_ex(*ptrs(out_ref, st_ref), *shape_args, binding.GDN_MODE_SEQUENTIAL,
+        rc = binding.gdn_frame_fwd_ex(*ptrs(out_ref, st_ref), *shape_args, binding.GDN_MODE_SPLIT,
                                       ws.data_ptr(), need, stream)
         assert rc == 0
         out = torch.full_like(q, float("nan"))
