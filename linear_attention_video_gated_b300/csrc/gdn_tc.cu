@@ -34,11 +34,8 @@ namespace {
 using namespace ptx;
 
 constexpr int kGramTok = 64;                   // tokens per gram stage
-constexpr int kGramStages = 3;
 constexpr int kGramRegion = kGramTok * 128;    // one 64-column atom of a stage
-constexpr int kGramThreads = 320;              // 4 epilogue, 4 convert, 1 TMA, 1 MMA warps
-constexpr int kScanStages = 2;
-constexpr int kScanThreads = 320;              // 8 epilogue, 1 copy, 1 MMA warps
+constexpr int kGramThreads = 448;              // 4 epilogue, 8 convert, 1 TMA, 1 MMA warps
 constexpr int kImgRegion = 128 * 128;          // one atom of a 128-row operand image
 constexpr int kOutTok = 128;                   // tokens per read-out tile (MMA N)
 constexpr int kOutQStages = 2;
@@ -57,7 +54,7 @@ TcLayout tc_layout(const Problem& p) {
   TcLayout L{};
   const int NA = num_atoms(p.D);
   L.m_bytes = (size_t)NA * p.D * 128;      // M_t image: NA regions of D rows x 128 B
-  L.b_bytes = (size_t)p.D * p.D * 4;       // b_t: fp32 [i][j]
+  L.b_bytes = (size_t)p.D * p.D * 4;       // b_t: fp32 column blocks [D/16][i][16]
   L.s_bytes = (size_t)2 * NA * p.D * 128;  // S_t image: hi/lo x NA regions of D rows
   const size_t F = (size_t)p.BHT();
   L.m_off = 0;
@@ -166,12 +163,26 @@ __device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_
 }
 
 // =============================================================================
-// gram: [M | b] = (diag(beta) K)^T [K | V] per frame-head.
+// gram: [M_t | b_t] = (diag(beta) K)^T [K | V] per frame-head.
+//
+// Persistent CTAs stream K and V tiles of 64 tokens through a 4-deep ring (TMA);
+// eight warps scale each tile by beta and split it into bf16 hi + lo parts in a
+// 2-deep ring of their own; one thread issues the MMAs; four warps drain the
+// fp32 accumulators (double-buffered in TMEM) into
+//   the M_t image: bf16, the scan's A operand (K-major, 128-byte swizzle, NA
+//     atoms of D rows x 128 B), staged in shared memory and bulk-stored;
+//   b_t: fp32 in column blocks of 16 ([D/16][D rows][16]), so each block the
+//     scan's column-split CTAs read is contiguous.
 // =============================================================================
+constexpr int kGramRaw = 4;
+constexpr int kGramConv = 2;
+constexpr int kRawStage = 4 * kGramRegion;   // K atoms (NA) then V atoms (NA): 32 KB
+constexpr int kConvStage = 4 * kGramRegion;  // AH atoms (2) then AL atoms (2): 32 KB
+
 struct GramArgs {
   const float* beta;
-  uint8_t* m_img;   // F x m_bytes
-  float* b_mat;     // F x D x D
+  uint8_t* m_img;  // F x NA x D rows x 128 B
+  float* b_blk;    // F x (D/16) x D x 16
   long long nitems;
   int S, D, NA;
   float m_scale, b_scale;
@@ -183,13 +194,15 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int NA = a.NA, D = a.D, S = a.S;
-  // stage layout: K atoms [NA], V atoms [NA], AH atoms [2], AL atoms [2]
-  const int stage_bytes = (2 * NA + 4) * kGramRegion;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kGramStages * stage_bytes);
-  uint64_t* full = bars;
-  uint64_t* scaled = bars + kGramStages;
-  uint64_t* empty = bars + 2 * kGramStages;
-  uint64_t* accfull = bars + 3 * kGramStages;
+  uint8_t* raw = smem;
+  uint8_t* conv = raw + kGramRaw * kRawStage;
+  uint8_t* mstage = conv + kGramConv * kConvStage;  // NA x D rows x 128 B
+  uint64_t* bars = reinterpret_cast<uint64_t*>(mstage + NA * D * 128);
+  uint64_t* raw_full = bars;
+  uint64_t* raw_empty = raw_full + kGramRaw;
+  uint64_t* conv_full = raw_empty + kGramRaw;
+  uint64_t* conv_empty = conv_full + kGramConv;
+  uint64_t* accfull = conv_empty + kGramConv;
   uint64_t* accempty = accfull + 2;
   uint64_t* mma_done = accempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
@@ -197,31 +210,30 @@ __global__ void __launch_bounds__(kGramThreads, 1)
 
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
-    mbar_init(smem_u32(mma_done), 1);
-    for (int s = 0; s < kGramStages; ++s) {
-      mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&scaled[s]), 4);
-      mbar_init(smem_u32(&empty[s]), 1);
+    for (int s = 0; s < kGramRaw; ++s) {
+      mbar_init(smem_u32(&raw_full[s]), 1);
+      mbar_init(smem_u32(&raw_empty[s]), 1);
+    }
+    for (int s = 0; s < kGramConv; ++s) {
+      mbar_init(smem_u32(&conv_full[s]), 8);
+      mbar_init(smem_u32(&conv_empty[s]), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&accfull[b]), 1);
       mbar_init(smem_u32(&accempty[b]), 4);
     }
+    mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (NA == 1) {  // A operands span 128 rows of M: zero the unused upper atom once
-    for (int s = 0; s < kGramStages; ++s) {
-      uint4* ah1 = reinterpret_cast<uint4*>(smem + s * stage_bytes + (2 * NA + 1) * kGramRegion);
-      uint4* al1 = reinterpret_cast<uint4*>(smem + s * stage_bytes + (2 * NA + 3) * kGramRegion);
-      for (int i = threadIdx.x; i < kGramRegion / 16; i += blockDim.x) {
-        ah1[i] = make_uint4(0, 0, 0, 0);
-        al1[i] = make_uint4(0, 0, 0, 0);
+  if (NA == 1)  // the A operands span 128 rows of M: key dims 64..127 are zero
+    for (int s = 0; s < kGramConv; ++s)
+      for (int idx = threadIdx.x; idx < kGramRegion / 16; idx += blockDim.x) {
+        reinterpret_cast<uint4*>(conv + s * kConvStage + kGramRegion)[idx] = make_uint4(0, 0, 0, 0);
+        reinterpret_cast<uint4*>(conv + s * kConvStage + 3 * kGramRegion)[idx] = make_uint4(0, 0, 0, 0);
       }
-    }
-    fence_proxy_async_smem();
-  }
-  if (warp == 9) {
+  fence_proxy_async_smem();
+  if (warp == 13) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -231,21 +243,21 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int nchunks = (S + kGramTok - 1) / kGramTok;
 
-  if (warp == 8) {
+  if (warp == 12) {
     // ---------------- TMA producer
     if (lane == 0) {
       prefetch_tmap(&mapK);
       prefetch_tmap(&mapV);
-      Ring<kGramStages> r;
+      Ring<kGramRaw> r;
       bool ok = true;
       for (long long f = blockIdx.x; ok && f < a.nitems; f += gridDim.x) {
         for (int c = 0; c < nchunks; ++c) {
-          if (!wait_or_abort(smem_u32(&empty[r.stage]), r.phase ^ 1, abort_flag, a.status)) {
+          if (!wait_or_abort(smem_u32(&raw_empty[r.stage]), r.phase ^ 1, abort_flag, a.status)) {
             ok = false;
             break;
           }
-          uint8_t* st = smem + r.stage * stage_bytes;
-          const uint32_t fb = smem_u32(&full[r.stage]);
+          uint8_t* st = raw + r.stage * kRawStage;
+          const uint32_t fb = smem_u32(&raw_full[r.stage]);
           mbar_arrive_expect_tx(fb, 2 * NA * kGramRegion);
           for (int at = 0; at < NA; ++at) {
             tma_load_3d(smem_u32(st + at * kGramRegion), &mapK, fb, 64 * at, c * kGramTok, (int)f);
@@ -255,59 +267,62 @@ __global__ void __launch_bounds__(kGramThreads, 1)
           r.advance();
         }
       }
-      r.drain(full);  // every issued load has landed before the CTA may exit
+      r.drain(raw_full);  // every issued load has landed before the CTA may exit
     }
-  } else if (warp == 9) {
+  } else if (warp == 13) {
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t id1 = idesc_bf16(128, NA * 64 + D, 1, 1);
       const uint32_t id2 = idesc_bf16(128, D, 1, 1);
-      int stage = 0;
-      uint32_t phase = 0;
-      int ab = 0;
-      uint32_t aphase = 0;
+      int rs = 0, cs = 0, ab = 0;
+      uint32_t rph = 0, cph = 0, aph = 0;
       for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
-        if (!wait_or_abort(smem_u32(&accempty[ab]), aphase ^ 1, abort_flag, a.status)) goto done;
+        if (!wait_or_abort(smem_u32(&accempty[ab]), aph ^ 1, abort_flag, a.status)) goto done;
         tc_fence_after();
         const uint32_t acc = tmem + ab * 256;
         for (int c = 0; c < nchunks; ++c) {
-          if (!wait_or_abort(smem_u32(&scaled[stage]), phase, abort_flag, a.status)) goto done;
+          if (!wait_or_abort(smem_u32(&conv_full[cs]), cph, abort_flag, a.status)) goto done;
           tc_fence_after();
-          const uint32_t st = smem_u32(smem + stage * stage_bytes);
-          const uint32_t k0 = st, v0 = st + NA * kGramRegion;
-          const uint32_t ah0 = st + 2 * NA * kGramRegion, al0 = ah0 + 2 * kGramRegion;
+          const uint32_t rb = smem_u32(raw + rs * kRawStage);
+          const uint32_t ah = smem_u32(conv + cs * kConvStage), al = ah + 2 * kGramRegion;
 #pragma unroll
           for (int kk = 0; kk < kGramTok / 16; ++kk) {
             const uint32_t off = kk * 2048;
-            mma_bf16(acc, smem_desc(ah0 + off, kGramRegion, 1024), smem_desc(k0 + off, kGramRegion, 1024), id1,
+            mma_bf16(acc, smem_desc(ah + off, kGramRegion, 1024), smem_desc(rb + off, kGramRegion, 1024), id1,
                      (c > 0 || kk > 0) ? 1u : 0u);
-            mma_bf16(acc + NA * 64, smem_desc(al0 + off, kGramRegion, 1024), smem_desc(v0 + off, kGramRegion, 1024),
-                     id2, 1u);
+            mma_bf16(acc + NA * 64, smem_desc(al + off, kGramRegion, 1024),
+                     smem_desc(rb + NA * kGramRegion + off, kGramRegion, 1024), id2, 1u);
           }
-          mma_commit(smem_u32(&empty[stage]));
-          if (++stage == kGramStages) { stage = 0; phase ^= 1; }
+          mma_commit(smem_u32(&raw_empty[rs]));
+          mma_commit(smem_u32(&conv_empty[cs]));
+          if (++rs == kGramRaw) { rs = 0; rph ^= 1; }
+          if (++cs == kGramConv) { cs = 0; cph ^= 1; }
         }
         mma_commit(smem_u32(&accfull[ab]));
-        if (++ab == 2) { ab = 0; aphase ^= 1; }
+        if (++ab == 2) { ab = 0; aph ^= 1; }
       }
     }
   } else if (warp >= 4) {
-    // ---------------- beta scaling: A = diag(beta) K, split into bf16 hi + lo
+    // ---------------- beta scaling: A = diag(beta) K, split into bf16 hi + lo.
+    // Elementwise, so each 16-byte chunk is transformed where it lies in the
+    // swizzled tile (the hi / lo tiles share the K tile's layout).
     const int ct = threadIdx.x - 128;
-    int stage = 0;
-    uint32_t phase = 0;
-    const int chunks_per_atom = kGramTok * 8;
+    int rs = 0, cs = 0;
+    uint32_t rph = 0, cph = 0;
+    const int units = NA * kGramTok * 8;  // 16-byte chunks of K per tile
     for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
       const float* bf = a.beta + f * S;
       for (int c = 0; c < nchunks; ++c) {
-        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status))) goto done;
-        uint8_t* st = smem + stage * stage_bytes;
-        for (int ch = ct; ch < NA * chunks_per_atom; ch += 128) {
-          const int at = ch / chunks_per_atom;
-          const int off = (ch % chunks_per_atom) * 16;
-          const int s = c * kGramTok + off / 128;
+        const bool ok = wait_or_abort(smem_u32(&raw_full[rs]), rph, abort_flag, a.status) &&
+                        wait_or_abort(smem_u32(&conv_empty[cs]), cph ^ 1, abort_flag, a.status);
+        if (!__all_sync(0xffffffffu, ok)) goto done;
+        const uint8_t* kt = raw + rs * kRawStage;
+        uint8_t* ah = conv + cs * kConvStage;
+        for (int u = ct; u < units; u += 256) {
+          const int row = (u >> 3) & (kGramTok - 1);
+          const int s = c * kGramTok + row;
           const float bs = s < S ? __ldg(bf + s) : 0.f;
-          const uint4 kv = *reinterpret_cast<const uint4*>(st + at * kGramRegion + off);
+          const uint4 kv = *reinterpret_cast<const uint4*>(kt + u * 16);
           const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
           uint32_t hi[4], lo[4];
 #pragma unroll
@@ -315,82 +330,103 @@ __global__ void __launch_bounds__(kGramThreads, 1)
             const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
             split2(bs * x.x, bs * x.y, hi[e], lo[e]);
           }
-          *reinterpret_cast<uint4*>(st + (2 * NA + at) * kGramRegion + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(st + (2 * NA + 2 + at) * kGramRegion + off) =
-              make_uint4(lo[0], lo[1], lo[2], lo[3]);
+          *reinterpret_cast<uint4*>(ah + u * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(ah + 2 * kGramRegion + u * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&scaled[stage]));
-        if (++stage == kGramStages) { stage = 0; phase ^= 1; }
+        if (lane == 0) mbar_arrive(smem_u32(&conv_full[cs]));
+        if (++rs == kGramRaw) { rs = 0; rph ^= 1; }
+        if (++cs == kGramConv) { cs = 0; cph ^= 1; }
       }
     }
   } else {
-    // ---------------- epilogue: TMEM -> M image (bf16) and b (fp32)
+    // ---------------- epilogue: TMEM -> M image (bf16, staged) and b (fp32 column blocks)
     const int i = warp * 32 + lane;  // accumulator row = key index
+    const int ncb = D / 16;
     int ab = 0;
-    uint32_t aphase = 0;
+    uint32_t aph = 0;
     for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
-      if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[ab]), aphase, abort_flag, a.status))) goto done;
+      if (threadIdx.x == 0) bulk_wait_read0();  // the previous M image store has read the stage
+      const bool ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[ab]), aph, abort_flag, a.status));
+      if (barrier_any(1, 128, !ok || *abort_flag)) goto done;
       tc_fence_after();
       const uint32_t acc = tmem + ((uint32_t)(warp * 32) << 16) + ab * 256;
-      uint8_t* mimg = a.m_img + (size_t)f * NA * D * 128;
-      float* brow = a.b_mat + (size_t)f * D * D + (size_t)i * D;
       for (int c0 = 0; c0 < D; c0 += 16) {
         float v[16];
         tmem_ld16(acc + c0, v);
         tmem_ld_wait();
         if (i < D) {
-          uint8_t* reg = mimg + (size_t)(c0 / 64) * D * 128;
+          uint8_t* reg = mstage + (c0 >> 6) * D * 128;
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const int col = (c0 % 64) + 8 * h;
             uint4 o;
             o.x = pack_bf16(v[8 * h + 0] * a.m_scale, v[8 * h + 1] * a.m_scale);
             o.y = pack_bf16(v[8 * h + 2] * a.m_scale, v[8 * h + 3] * a.m_scale);
             o.z = pack_bf16(v[8 * h + 4] * a.m_scale, v[8 * h + 5] * a.m_scale);
             o.w = pack_bf16(v[8 * h + 6] * a.m_scale, v[8 * h + 7] * a.m_scale);
-            *reinterpret_cast<uint4*>(reg + sw128_off(i, col)) = o;
+            *reinterpret_cast<uint4*>(reg + sw128_off(i, (c0 & 63) + 8 * h)) = o;
           }
         }
       }
-      for (int c0 = 0; c0 < D; c0 += 16) {
+      for (int cb = 0; cb < ncb; ++cb) {
         float v[16];
-        tmem_ld16(acc + NA * 64 + c0, v);
+        tmem_ld16(acc + NA * 64 + 16 * cb, v);
         tmem_ld_wait();
         if (i < D) {
+          float4* dst = reinterpret_cast<float4*>(a.b_blk + (((size_t)f * ncb + cb) * D + i) * 16);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<float4*>(brow + c0 + 4 * q) =
-                make_float4(v[4 * q] * a.b_scale, v[4 * q + 1] * a.b_scale, v[4 * q + 2] * a.b_scale,
-                            v[4 * q + 3] * a.b_scale);
+            dst[q] = make_float4(v[4 * q] * a.b_scale, v[4 * q + 1] * a.b_scale, v[4 * q + 2] * a.b_scale,
+                                 v[4 * q + 3] * a.b_scale);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(&accempty[ab]));
-      if (++ab == 2) { ab = 0; aphase ^= 1; }
+      if (++ab == 2) { ab = 0; aph ^= 1; }
+      fence_proxy_async_smem();
+      named_barrier(1, 128);
+      if (threadIdx.x == 0) {
+        bulk_s2g(a.m_img + (size_t)f * NA * D * 128, smem_u32(mstage), NA * D * 128);
+        bulk_commit();
+      }
     }
   }
 done:
-  if (warp == 9 && lane == 0) {  // every MMA this CTA issued has completed
+  if (threadIdx.x == 0) bulk_wait0();  // M image stores complete
+  if (warp == 13 && lane == 0) {  // every MMA this CTA issued has completed
     mma_commit(smem_u32(mma_done));
     wait_bounded(smem_u32(mma_done), 0, 500000000ull);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 13) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
 }
 
 // =============================================================================
-// scan: S_t = g_t (S_{t-1} - M_t S_{t-1}) + b_t per head, frame by frame.
+// scan: S_t[:, J] = g_t (S_{t-1}[:, J] - M_t S_{t-1}[:, J]) + b_t[:, J], frame by frame.
+//
+// Columns of the state evolve independently, so each head is split over D/16
+// CTAs, CTA c owning the value columns J = [16c, 16c + 16): no communication.
+// Per frame: P = M_t S_{t-1}[:, J] on the tensor core (A = the M_t image, B =
+// the state block as bf16 hi + lo), then the update in fp32 registers (thread
+// i = state row i).  M_t and the b_t block stream in through a 4-deep ring of
+// bulk copies; the new state block goes back to the read-out's S_t image with
+// bulk stores (hi / lo, NA atoms, rows 16c .. 16c + 15 of each).
 // =============================================================================
+constexpr int kScanStages = 4;
+constexpr int kScanThreads = 192;         // 4 epilogue, 1 copy, 1 MMA warps
+constexpr int kScanMStage = 2 * 128 * 128;  // M image: 2 atoms x 128 rows x 128 B
+constexpr int kScanBStage = 128 * 64;       // b block: up to 128 rows x 16 floats
+constexpr int kScanImg = 4 * 16 * 128;      // state block image: hi/lo x 2 atoms x 16 rows x 128 B
+
 struct ScanArgs {
   const uint8_t* m_img;
-  const float* b_mat;
+  const float* b_blk;
   const float* g;
   const float* state_in;
   uint8_t* s_img;
@@ -403,34 +439,39 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int NA = a.NA, D = a.D, T = a.T;
-  // A image (S^T hi/lo): [hl][atom] regions of 128 rows; M stages: [stage][atom] of D rows
-  uint8_t* img = smem;
-  uint8_t* mst = smem + 2 * NA * kImgRegion;
-  const int m_stage_bytes = NA * D * 128;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(mst + kScanStages * m_stage_bytes);
-  uint64_t* mfull = bars;
-  uint64_t* mempty = bars + kScanStages;
-  uint64_t* accfull = bars + 2 * kScanStages;
-  uint64_t* sready = accfull + 1;
+  const int ncb = D / 16, KS = D / 16;
+  uint8_t* mring = smem;
+  uint8_t* bring = mring + kScanStages * kScanMStage;
+  uint8_t* img = bring + kScanStages * kScanBStage;  // 2 buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(img + 2 * kScanImg);
+  uint64_t* full = bars;
+  uint64_t* empty = full + kScanStages;
+  uint64_t* pfull = empty + kScanStages;
+  uint64_t* sready = pfull + 1;
   uint64_t* mma_done = sready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  const long long bh = blockIdx.x;
+  const long long bh = blockIdx.x / ncb;
+  const int cb = blockIdx.x % ncb;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kScanStages; ++s) {
-      mbar_init(smem_u32(&mfull[s]), 1);
-      mbar_init(smem_u32(&mempty[s]), 1);
+      mbar_init(smem_u32(&full[s]), 1);
+      mbar_init(smem_u32(&empty[s]), 5);  // the MMA's commit + the 4 epilogue warps (b read)
     }
-    mbar_init(smem_u32(accfull), 1);
+    mbar_init(smem_u32(pfull), 1);
     mbar_init(smem_u32(sready), 1);
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 9) {
-    tmem_alloc(smem_u32(tmem_slot), 128);
+  // M image rows D..127 (never copied in) must be finite: zero them once.
+  for (int idx = threadIdx.x; idx < kScanStages * kScanMStage / 16; idx += blockDim.x)
+    reinterpret_cast<uint4*>(mring)[idx] = make_uint4(0, 0, 0, 0);
+  fence_proxy_async_smem();
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 32);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -438,142 +479,154 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
-    // ---------------- copy M_t images in
+  if (warp == 4) {
+    // ---------------- copies in: M_t image (NA atoms of D rows) and the b_t block
     if (lane == 0) {
       Ring<kScanStages> r;
       for (int t = 0; t < T; ++t) {
-        if (!wait_or_abort(smem_u32(&mempty[r.stage]), r.phase ^ 1, abort_flag, a.status)) break;
-        const uint32_t fb = smem_u32(&mfull[r.stage]);
-        mbar_arrive_expect_tx(fb, m_stage_bytes);
-        const uint8_t* src = a.m_img + (size_t)(bh * T + t) * m_stage_bytes;
+        if (!wait_or_abort(smem_u32(&empty[r.stage]), r.phase ^ 1, abort_flag, a.status)) break;
+        const long long f = bh * T + t;
+        const uint32_t fb = smem_u32(&full[r.stage]);
+        mbar_arrive_expect_tx(fb, NA * D * 128 + D * 64);
+        const uint8_t* src = a.m_img + (size_t)f * NA * D * 128;
         for (int at = 0; at < NA; ++at)
-          bulk_g2s(smem_u32(mst + r.stage * m_stage_bytes + at * D * 128), src + at * D * 128, D * 128, fb);
+          bulk_g2s(smem_u32(mring + r.stage * kScanMStage + at * 128 * 128), src + at * D * 128, D * 128, fb);
+        bulk_g2s(smem_u32(bring + r.stage * kScanBStage), a.b_blk + ((size_t)f * ncb + cb) * D * 16, D * 64, fb);
         r.mark_issued();
         r.advance();
       }
-      r.drain(mfull);
+      r.drain(full);
     }
-  } else if (warp == 9) {
-    // ---------------- MMA: P^T = S^T M_t
+  } else if (warp == 5) {
+    // ---------------- MMA: P = M_t S_{t-1}[:, J]
     if (lane == 0) {
-      const uint32_t id = idesc_bf16(128, D, 0, 0);
+      const uint32_t id = idesc_bf16(128, 16, 0, 0);
       int stage = 0;
       uint32_t phase = 0;
       for (int t = 0; t < T; ++t) {
         if (!wait_or_abort(smem_u32(sready), t & 1, abort_flag, a.status)) goto done;
-        if (!wait_or_abort(smem_u32(&mfull[stage]), phase, abort_flag, a.status)) goto done;
+        if (!wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status)) goto done;
         tc_fence_after();
-        const uint32_t ms = smem_u32(mst + stage * m_stage_bytes);
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const int at = kk / 4;
-          const uint32_t ko = (kk % 4) * 32;
-          const uint64_t bdesc = smem_desc(ms + at * D * 128 + ko, 16, 1024);
-          mma_bf16(tmem, smem_desc(smem_u32(img + at * kImgRegion) + ko, 16, 1024), bdesc, id, kk > 0 ? 1u : 0u);
-          mma_bf16(tmem, smem_desc(smem_u32(img + (NA + at) * kImgRegion) + ko, 16, 1024), bdesc, id, 1u);
+        const uint32_t ms = smem_u32(mring + stage * kScanMStage);
+        const uint32_t sb = smem_u32(img + (t & 1) * kScanImg);
+        for (int kk = 0; kk < KS; ++kk) {
+          const uint32_t ao = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
+          const uint32_t bo = (kk >> 2) * (16 * 128) + (kk & 3) * 32;
+          const uint64_t ad = smem_desc(ms + ao, 16, 1024);
+          mma_bf16(tmem, ad, smem_desc(sb + bo, 16, 1024), id, kk > 0 ? 1u : 0u);
+          mma_bf16(tmem, ad, smem_desc(sb + 2 * 16 * 128 + bo, 16, 1024), id, 1u);
         }
-        mma_commit(smem_u32(&mempty[stage]));
-        mma_commit(smem_u32(accfull));
+        mma_commit(smem_u32(pfull));
+        mma_commit(smem_u32(&empty[stage]));
         if (++stage == kScanStages) { stage = 0; phase ^= 1; }
       }
     }
   } else {
-    // ---------------- epilogue (8 warps): thread owns column j of S, half of its rows
-    const int q = warp & 3, half = warp >> 2;
-    const int j = q * 32 + lane;
-    const int Dh = D / 2;
-    const int i0 = half * Dh;
-    const bool active = j < D;
-    float s[64], bn[64];
+    // ---------------- epilogue (4 warps): thread i owns row i of the column block
+    const int i = threadIdx.x;
+    const bool row = i < D;
+    float x[16];
 #pragma unroll
-    for (int ii = 0; ii < 64; ++ii) {
-      s[ii] = 0.f;
-      bn[ii] = 0.f;
+    for (int j = 0; j < 16; ++j) x[j] = 0.f;
+    if (row && a.state_in) {
+      const float4* si = reinterpret_cast<const float4*>(a.state_in + ((size_t)bh * D + i) * D + 16 * cb);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 w = si[q];
+        x[4 * q] = w.x;
+        x[4 * q + 1] = w.y;
+        x[4 * q + 2] = w.z;
+        x[4 * q + 3] = w.w;
+      }
     }
-    if (active && a.state_in) {
-      const float* si = a.state_in + (size_t)bh * D * D;
+    // state block image (B operand, K-major: row n = value column 16cb + n, k = i)
+    auto write_img = [&](uint8_t* im) {
+      if (!row) return;
+      uint8_t* hi = im + (i >> 6) * (16 * 128);
+      uint8_t* lo = hi + 2 * 16 * 128;
 #pragma unroll
-      for (int ii = 0; ii < 64; ++ii)
-        if (ii < Dh) s[ii] = si[(size_t)(i0 + ii) * D + j];
-    }
-    auto load_b = [&](int t) {
-      const float* bp = a.b_mat + (size_t)(bh * T + t) * D * D;
-#pragma unroll
-      for (int ii = 0; ii < 64; ++ii)
-        if (ii < Dh && active) bn[ii] = __ldg(bp + (size_t)(i0 + ii) * D + j);
-    };
-    // S^T image row j, columns [i0, i0 + Dh): hi and lo parts
-    auto write_img = [&]() {
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        if (c * 8 < Dh) {
-          const int col = i0 + c * 8;
-          const int at = col / 64;
-          uint32_t hi[4], lo[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) split2(s[c * 8 + 2 * e], s[c * 8 + 2 * e + 1], hi[e], lo[e]);
-          const uint32_t off = sw128_off(j, col % 64);
-          *reinterpret_cast<uint4*>(img + at * kImgRegion + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
-          *reinterpret_cast<uint4*>(img + (NA + at) * kImgRegion + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
-        }
+      for (int n = 0; n < 16; n += 2) {
+        uint32_t hv, lv;
+        split2(x[n], x[n + 1], hv, lv);
+        const uint32_t o0 = sw128_off(n, i & 63), o1 = sw128_off(n + 1, i & 63);
+        *reinterpret_cast<uint16_t*>(hi + o0) = (uint16_t)(hv & 0xFFFF);
+        *reinterpret_cast<uint16_t*>(hi + o1) = (uint16_t)(hv >> 16);
+        *reinterpret_cast<uint16_t*>(lo + o0) = (uint16_t)(lv & 0xFFFF);
+        *reinterpret_cast<uint16_t*>(lo + o1) = (uint16_t)(lv >> 16);
       }
     };
-    write_img();  // S_0 (zeros for rows j >= D)
+    write_img(img);  // S_{-1} into buffer 0
     fence_proxy_async_smem();
-    named_barrier(1, 256);
+    if (barrier_any(1, 128, *abort_flag)) goto done;
     if (threadIdx.x == 0) mbar_arrive(smem_u32(sready));
-    if (T > 0) load_b(0);
+    int stage = 0;
+    uint32_t phase = 0;
+    float gnext = T > 0 ? __ldg(a.g + bh * T) : 0.f;
     for (int t = 0; t < T; ++t) {
       const long long f = bh * T + t;
-      const float gt = __ldg(a.g + f);
-      const bool ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(accfull), t & 1, abort_flag, a.status));
-      if (ok) {
+      const float gt = gnext;
+      if (t + 1 < T) gnext = __ldg(a.g + f + 1);
+      const bool ok = wait_or_abort(smem_u32(pfull), t & 1, abort_flag, a.status) &&
+                      wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
+      if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        const uint32_t acc = tmem + ((uint32_t)(q * 32) << 16) + i0;
+        float p[16];
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), p);
+        float bv[16];
+        if (row) {
+          const float4* bp = reinterpret_cast<const float4*>(bring + stage * kScanBStage + i * 64);
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 16) {
-          if (c0 < Dh) {
-            float p[16];
-            tmem_ld16(acc + c0, p);
-            tmem_ld_wait();
-#pragma unroll
-            for (int u = 0; u < 16; ++u)
-              if (c0 + u < Dh) s[c0 + u] = fmaf(gt, s[c0 + u] - p[u], bn[c0 + u]);
+          for (int q = 0; q < 4; ++q) {
+            const float4 w = bp[q];
+            bv[4 * q] = w.x;
+            bv[4 * q + 1] = w.y;
+            bv[4 * q + 2] = w.z;
+            bv[4 * q + 3] = w.w;
           }
         }
-        if (t + 1 < T) load_b(t + 1);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+        if (row) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) x[j] = fmaf(gt, x[j] - p[j], bv[j]);
+        }
       }
-      tc_fence_before();
-      if (threadIdx.x == 0) bulk_wait_read0();  // the previous S image copy has read smem
-      if (barrier_any(1, 256, !ok || *abort_flag)) goto done;
-      write_img();
+      if (++stage == kScanStages) { stage = 0; phase ^= 1; }
+      // the store of S_{t-2} (same buffer) has finished reading it
+      if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      if (barrier_any(1, 128, !__all_sync(0xffffffffu, ok) || *abort_flag)) goto done;
+      uint8_t* im = img + ((t + 1) & 1) * kScanImg;
+      write_img(im);
       fence_proxy_async_smem();
-      named_barrier(1, 256);
+      named_barrier(1, 128);
       if (threadIdx.x == 0) {
-        uint8_t* dst = a.s_img + (size_t)f * 2 * NA * D * 128;
-        for (int r = 0; r < 2 * NA; ++r) bulk_s2g(dst + (size_t)r * D * 128, smem_u32(img + r * kImgRegion), D * 128);
+        uint8_t* dst = a.s_img + (size_t)f * 2 * NA * D * 128 + (size_t)16 * cb * 128;
+        for (int hl = 0; hl < 2; ++hl)
+          for (int at = 0; at < NA; ++at)
+            bulk_s2g(dst + (size_t)(hl * NA + at) * D * 128, smem_u32(im + (hl * 2 + at) * 16 * 128), 16 * 128);
         bulk_commit();
         mbar_arrive(smem_u32(sready));
       }
     }
-    if (active && a.state_out) {
-      float* so = a.state_out + (size_t)bh * D * D;
+    if (row && a.state_out) {
+      float4* so = reinterpret_cast<float4*>(a.state_out + ((size_t)bh * D + i) * D + 16 * cb);
 #pragma unroll
-      for (int ii = 0; ii < 64; ++ii)
-        if (ii < Dh) so[(size_t)(i0 + ii) * D + j] = s[ii];
+      for (int q = 0; q < 4; ++q) so[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     }
   }
 done:
-  if (threadIdx.x == 0) bulk_wait0();  // S image copies complete
-  if (warp == 9 && lane == 0) {
+  if (threadIdx.x == 0) bulk_wait0();  // state image stores complete
+  if (warp == 5 && lane == 0) {
     mma_commit(smem_u32(mma_done));
     wait_bounded(smem_u32(mma_done), 0, 500000000ull);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == 5) {
     tc_fence_after();
-    tmem_dealloc(tmem, 128);
+    tmem_dealloc(tmem, 32);
   }
 }
 
@@ -782,8 +835,10 @@ constexpr int kBarBytes = 256;
 // shared memory so that two of them never share an SM.
 constexpr int kOneCtaPerSm = 116 * 1024;
 int at_least_half(int b) { return b > kOneCtaPerSm ? b : kOneCtaPerSm; }
-int gram_smem(int NA) { return at_least_half(kGramStages * (2 * NA + 4) * kGramRegion + kBarBytes + 1024); }
-int scan_smem(int NA, int D) { return 2 * NA * kImgRegion + kScanStages * NA * D * 128 + kBarBytes + 1024; }
+int gram_smem(int NA, int D) {
+  return kGramRaw * kRawStage + kGramConv * kConvStage + NA * D * 128 + kBarBytes + 1024;
+}
+int scan_smem() { return kScanStages * (kScanMStage + kScanBStage) + 2 * kScanImg + kBarBytes + 1024; }
 int out_smem(int NA, int nb) {
   return at_least_half(nb * 2 * NA * kImgRegion + kOutQStages * NA * kOutTok * 128 + NA * kOutTok * 128 + kBarBytes +
                        1024);
@@ -819,7 +874,7 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
     return kCuda;
 
   {
-    const int smem = gram_smem(NA);
+    const int smem = gram_smem(NA, p.D);
     if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
     GramArgs ga{p.beta, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale, p.key_scale, p.status};
@@ -829,12 +884,12 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   {
-    const int smem = scan_smem(NA, p.D);
+    const int smem = scan_smem();
     if (cudaFuncSetAttribute(tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
     ScanArgs sa{m_img, b_mat, p.g, p.state_in, s_img, p.state_out, p.T, p.D, NA, p.status};
     ProfScope ps(st, "tc_scan");
-    tc_scan_kernel<<<(unsigned)p.BH(), kScanThreads, smem, st>>>(sa);
+    tc_scan_kernel<<<(unsigned)(p.BH() * (p.D / 16)), kScanThreads, smem, st>>>(sa);
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   {
