@@ -36,8 +36,7 @@ using namespace ptx;
 constexpr int kGramTok = 64;                   // tokens per gram stage
 constexpr int kGramRegion = kGramTok * 128;    // one 64-column atom of a stage
 constexpr int kGramThreads = 448;              // 4 epilogue, 8 convert, 1 TMA, 1 MMA warps
-constexpr int kImgRegion = 128 * 128;          // one atom of a 128-row operand image
-constexpr int kOutTok = 128;                   // tokens per read-out tile (MMA N)
+constexpr int kOutTok = 128;                   // tokens per read-out tile (MMA M)
 constexpr int kOutQStages = 2;
 constexpr int kOutAcc = 4;                     // TMEM accumulators in flight
 constexpr int kOutThreads = 192;               // 4 epilogue, 1 TMA, 1 MMA warps
@@ -310,18 +309,29 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     int rs = 0, cs = 0;
     uint32_t rph = 0, cph = 0;
     const int units = NA * kGramTok * 8;  // 16-byte chunks of K per tile
+    // This thread's chunks lie in tile rows r0 and r0 + 32; their beta values are
+    // loaded one tile ahead so the load latency stays off the critical path.
+    const int r0 = ct >> 3;
+    auto beta_at = [&](long long f, int c, int rw) {
+      const int s = c * kGramTok + rw;
+      return (f < a.nitems && s < S) ? __ldg(a.beta + f * S + s) : 0.f;
+    };
+    long long fn = blockIdx.x;
+    int cn = 0;
+    float bn0 = beta_at(fn, 0, r0), bn1 = beta_at(fn, 0, r0 + 32);
     for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
-      const float* bf = a.beta + f * S;
       for (int c = 0; c < nchunks; ++c) {
+        const float b0 = bn0, b1 = bn1;
+        if (++cn == nchunks) { cn = 0; fn += gridDim.x; }
+        bn0 = beta_at(fn, cn, r0);
+        bn1 = beta_at(fn, cn, r0 + 32);
         const bool ok = wait_or_abort(smem_u32(&raw_full[rs]), rph, abort_flag, a.status) &&
                         wait_or_abort(smem_u32(&conv_empty[cs]), cph ^ 1, abort_flag, a.status);
         if (!__all_sync(0xffffffffu, ok)) goto done;
         const uint8_t* kt = raw + rs * kRawStage;
         uint8_t* ah = conv + cs * kConvStage;
-        for (int u = ct; u < units; u += 256) {
-          const int row = (u >> 3) & (kGramTok - 1);
-          const int s = c * kGramTok + row;
-          const float bs = s < S ? __ldg(bf + s) : 0.f;
+        for (int u = ct, rr = 0; u < units; u += 256, ++rr) {
+          const float bs = (rr & 1) ? b1 : b0;
           const uint4 kv = *reinterpret_cast<const uint4*>(kt + u * 16);
           const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
           uint32_t hi[4], lo[4];
@@ -413,8 +423,8 @@ done:
 // Columns of the state evolve independently, so each head is split over D/16
 // CTAs, CTA c owning the value columns J = [16c, 16c + 16): no communication.
 // Per frame: P = M_t S_{t-1}[:, J] on the tensor core (A = the M_t image, B =
-// the state block as bf16 hi + lo), then the update in fp32 registers (thread
-// i = state row i).  M_t and the b_t block stream in through a 4-deep ring of
+// the state block as bf16 hi and lo side by side, N = 32, the two halves summed
+// in the epilogue), then the update in fp32 registers (thread i = state row i).  M_t and the b_t block stream in through a 4-deep ring of
 // bulk copies; the new state block goes back to the read-out's S_t image with
 // bulk stores (hi / lo, NA atoms, rows 16c .. 16c + 15 of each).
 // =============================================================================
@@ -422,7 +432,7 @@ constexpr int kScanStages = 4;
 constexpr int kScanThreads = 192;         // 4 epilogue, 1 copy, 1 MMA warps
 constexpr int kScanMStage = 2 * 128 * 128;  // M image: 2 atoms x 128 rows x 128 B
 constexpr int kScanBStage = 128 * 64;       // b block: up to 128 rows x 16 floats
-constexpr int kScanImg = 4 * 16 * 128;      // state block image: hi/lo x 2 atoms x 16 rows x 128 B
+constexpr int kScanImg = 2 * 32 * 128;      // state block image: 2 atoms x 32 rows (hi 0-15, lo 16-31) x 128 B
 
 struct ScanArgs {
   const uint8_t* m_img;
@@ -471,7 +481,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     reinterpret_cast<uint4*>(mring)[idx] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 5) {
-    tmem_alloc(smem_u32(tmem_slot), 32);
+    tmem_alloc(smem_u32(tmem_slot), 32);  // P_hi (columns 0-15) and P_lo (16-31)
     tmem_relinquish();
   }
   tc_fence_before();
@@ -500,7 +510,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
   } else if (warp == 5) {
     // ---------------- MMA: P = M_t S_{t-1}[:, J]
     if (lane == 0) {
-      const uint32_t id = idesc_bf16(128, 16, 0, 0);
+      const uint32_t id = idesc_bf16(128, 32, 0, 0);
       int stage = 0;
       uint32_t phase = 0;
       for (int t = 0; t < T; ++t) {
@@ -511,10 +521,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
         const uint32_t sb = smem_u32(img + (t & 1) * kScanImg);
         for (int kk = 0; kk < KS; ++kk) {
           const uint32_t ao = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-          const uint32_t bo = (kk >> 2) * (16 * 128) + (kk & 3) * 32;
-          const uint64_t ad = smem_desc(ms + ao, 16, 1024);
-          mma_bf16(tmem, ad, smem_desc(sb + bo, 16, 1024), id, kk > 0 ? 1u : 0u);
-          mma_bf16(tmem, ad, smem_desc(sb + 2 * 16 * 128 + bo, 16, 1024), id, 1u);
+          const uint32_t bo = (kk >> 2) * (32 * 128) + (kk & 3) * 32;
+          mma_bf16(tmem, smem_desc(ms + ao, 16, 1024), smem_desc(sb + bo, 16, 1024), id, kk > 0 ? 1u : 0u);
         }
         mma_commit(smem_u32(pfull));
         mma_commit(smem_u32(&empty[stage]));
@@ -539,20 +547,19 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
         x[4 * q + 3] = w.w;
       }
     }
-    // state block image (B operand, K-major: row n = value column 16cb + n, k = i)
+    // state block image (B operand, K-major: row n = value column 16cb + n for the
+    // hi part, row 16 + n for the lo part; k = i)
     auto write_img = [&](uint8_t* im) {
       if (!row) return;
-      uint8_t* hi = im + (i >> 6) * (16 * 128);
-      uint8_t* lo = hi + 2 * 16 * 128;
+      uint8_t* at = im + (i >> 6) * (32 * 128);
 #pragma unroll
       for (int n = 0; n < 16; n += 2) {
         uint32_t hv, lv;
         split2(x[n], x[n + 1], hv, lv);
-        const uint32_t o0 = sw128_off(n, i & 63), o1 = sw128_off(n + 1, i & 63);
-        *reinterpret_cast<uint16_t*>(hi + o0) = (uint16_t)(hv & 0xFFFF);
-        *reinterpret_cast<uint16_t*>(hi + o1) = (uint16_t)(hv >> 16);
-        *reinterpret_cast<uint16_t*>(lo + o0) = (uint16_t)(lv & 0xFFFF);
-        *reinterpret_cast<uint16_t*>(lo + o1) = (uint16_t)(lv >> 16);
+        *reinterpret_cast<uint16_t*>(at + sw128_off(n, i & 63)) = (uint16_t)(hv & 0xFFFF);
+        *reinterpret_cast<uint16_t*>(at + sw128_off(n + 1, i & 63)) = (uint16_t)(hv >> 16);
+        *reinterpret_cast<uint16_t*>(at + sw128_off(16 + n, i & 63)) = (uint16_t)(lv & 0xFFFF);
+        *reinterpret_cast<uint16_t*>(at + sw128_off(17 + n, i & 63)) = (uint16_t)(lv >> 16);
       }
     };
     write_img(img);  // S_{-1} into buffer 0
@@ -570,8 +577,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
                       wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        float p[16];
+        float p[16], pl[16];
         tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), p);
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16, pl);
         float bv[16];
         if (row) {
           const float4* bp = reinterpret_cast<const float4*>(bring + stage * kScanBStage + i * 64);
@@ -590,23 +598,23 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
         if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
         if (row) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] = fmaf(gt, x[j] - p[j], bv[j]);
+          for (int j = 0; j < 16; ++j) x[j] = fmaf(gt, x[j] - (p[j] + pl[j]), bv[j]);
         }
+        // S_t goes into the buffer that held S_{t-2}, whose store finished
+        // reading it before S_{t-1} was released to the MMA.
+        write_img(img + ((t + 1) & 1) * kScanImg);
+        fence_proxy_async_smem();
       }
       if (++stage == kScanStages) { stage = 0; phase ^= 1; }
-      // the store of S_{t-2} (same buffer) has finished reading it
-      if (threadIdx.x == 0) asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
       if (barrier_any(1, 128, !__all_sync(0xffffffffu, ok) || *abort_flag)) goto done;
-      uint8_t* im = img + ((t + 1) & 1) * kScanImg;
-      write_img(im);
-      fence_proxy_async_smem();
-      named_barrier(1, 128);
       if (threadIdx.x == 0) {
+        const uint8_t* im = img + ((t + 1) & 1) * kScanImg;
         uint8_t* dst = a.s_img + (size_t)f * 2 * NA * D * 128 + (size_t)16 * cb * 128;
         for (int hl = 0; hl < 2; ++hl)
           for (int at = 0; at < NA; ++at)
-            bulk_s2g(dst + (size_t)(hl * NA + at) * D * 128, smem_u32(im + (hl * 2 + at) * 16 * 128), 16 * 128);
+            bulk_s2g(dst + (size_t)(hl * NA + at) * D * 128, smem_u32(im + at * 32 * 128 + hl * 16 * 128), 16 * 128);
         bulk_commit();
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // the store of S_{t-1} has read its buffer
         mbar_arrive(smem_u32(sready));
       }
     }
@@ -631,12 +639,21 @@ done:
 }
 
 // =============================================================================
-// readout: O_t^T = S_t^T Q_t^T per frame-head and 128-token tile.
+// readout: O_t = Q_t S_t / sqrt(D) per frame-head and 128-token tile.
+//
+// Persistent CTAs.  Per frame-head the S_t image (bf16 hi + lo, the B operand:
+// K-major, row n = value column, D rows) arrives with one bulk copy into one of
+// two buffers; Q tiles of 128 tokens stream through a 2-deep TMA ring; per tile
+// two MMA chains (hi, lo) accumulate O_tile (128 tokens x D) in one of four
+// TMEM accumulators.  Each epilogue warp owns 32 token rows: it scales and
+// rounds them to bf16 into its own slice of a staging tile and TMA-stores the
+// slice, waiting only for its own previous store.
 // =============================================================================
 struct OutArgs {
   const uint8_t* s_img;
+  __nv_bfloat16* out;
   long long nitems;
-  int S, D, NA, n_abuf;
+  int S, D, NA;
   float scale;
   unsigned int* status;
 };
@@ -645,12 +662,13 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     tc_readout_kernel(const __grid_constant__ CUtensorMap mapQ, const __grid_constant__ CUtensorMap mapO, OutArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
-  const int NA = a.NA, D = a.D, S = a.S, NB = a.n_abuf;
-  const int img_bytes = 2 * NA * kImgRegion;           // one S^T image (hi, lo)
-  const int q_bytes = NA * kOutTok * 128;              // one Q tile
+  const int NA = a.NA, D = a.D, S = a.S;
+  const int img_bytes = 2 * NA * D * 128;                 // one S image (hi, lo)
+  const int img_stride = (img_bytes + 1023) & ~1023;
+  const int q_bytes = NA * kOutTok * 128;                 // one Q tile
   uint8_t* imgs = smem;
-  uint8_t* qst = imgs + NB * img_bytes;
-  uint8_t* stg = qst + kOutQStages * q_bytes;          // output staging: NA atoms of 128 rows
+  uint8_t* qst = imgs + 2 * img_stride;
+  uint8_t* stg = qst + kOutQStages * q_bytes;  // output staging: NA atoms of 128 rows x 128 B
   uint64_t* bars = reinterpret_cast<uint64_t*>(stg + NA * kOutTok * 128);
   uint64_t* afull = bars;
   uint64_t* aempty = bars + 2;
@@ -680,11 +698,6 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // S images hold D rows; rows D..127 of every region are zero (they only feed
-  // accumulator rows that are never stored).
-  for (int idx = threadIdx.x; idx < NB * img_bytes / 16; idx += blockDim.x)
-    reinterpret_cast<uint4*>(imgs)[idx] = make_uint4(0, 0, 0, 0);
-  fence_proxy_async_smem();
   if (warp == 5) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
@@ -696,21 +709,19 @@ __global__ void __launch_bounds__(kOutThreads, 1)
   const int ntiles = (S + kOutTok - 1) / kOutTok;
 
   if (warp == 4) {
-    // ---------------- producer: S image per item, Q tiles per tile
+    // ---------------- producer: S image per frame-head, Q tiles per tile
     if (lane == 0) {
       prefetch_tmap(&mapQ);
-      Ring<2> ra;  // S images (NB <= 2 slots in use)
+      Ring<2> ra;
       Ring<kOutQStages> rq;
       bool ok = true;
       for (long long f = blockIdx.x; ok && f < a.nitems; f += gridDim.x) {
         if (!wait_or_abort(smem_u32(&aempty[ra.stage]), ra.phase ^ 1, abort_flag, a.status)) break;
         const uint32_t afb = smem_u32(&afull[ra.stage]);
-        mbar_arrive_expect_tx(afb, 2 * NA * D * 128);
-        const uint8_t* src = a.s_img + (size_t)f * 2 * NA * D * 128;
-        for (int r = 0; r < 2 * NA; ++r)
-          bulk_g2s(smem_u32(imgs + ra.stage * img_bytes + r * kImgRegion), src + (size_t)r * D * 128, D * 128, afb);
+        mbar_arrive_expect_tx(afb, img_bytes);
+        bulk_g2s(smem_u32(imgs + ra.stage * img_stride), a.s_img + (size_t)f * img_bytes, img_bytes, afb);
         ra.mark_issued();
-        if (++ra.stage == NB) { ra.stage = 0; ra.phase ^= 1; }
+        ra.advance();
         for (int tile = 0; tile < ntiles; ++tile) {
           if (!wait_or_abort(smem_u32(&qempty[rq.stage]), rq.phase ^ 1, abort_flag, a.status)) {
             ok = false;
@@ -729,82 +740,82 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       rq.drain(qfull);
     }
   } else if (warp == 5) {
-    // ---------------- MMA
+    // ---------------- MMA: O_tile (128 tokens x D) = Q_tile S_hi + Q_tile S_lo
     if (lane == 0) {
-      const uint32_t id = idesc_bf16(128, kOutTok, 0, 0);
-      int ab = 0;
-      uint32_t aphase = 0;
-      int qs = 0;
-      uint32_t qphase = 0;
-      int cb = 0;
-      uint32_t cphase = 0;
+      const uint32_t id = idesc_bf16(128, D, 0, 0);
+      int ab = 0, qs = 0, cb = 0;
+      uint32_t aph = 0, qph = 0, cph = 0;
       for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
-        if (!wait_or_abort(smem_u32(&afull[ab]), aphase, abort_flag, a.status)) goto done;
-        const uint32_t im = smem_u32(imgs + ab * img_bytes);
+        if (!wait_or_abort(smem_u32(&afull[ab]), aph, abort_flag, a.status)) goto done;
+        const uint32_t im = smem_u32(imgs + ab * img_stride);
         for (int tile = 0; tile < ntiles; ++tile) {
-          if (!wait_or_abort(smem_u32(&accempty[cb]), cphase ^ 1, abort_flag, a.status)) goto done;
-          if (!wait_or_abort(smem_u32(&qfull[qs]), qphase, abort_flag, a.status)) goto done;
+          if (!wait_or_abort(smem_u32(&accempty[cb]), cph ^ 1, abort_flag, a.status)) goto done;
+          if (!wait_or_abort(smem_u32(&qfull[qs]), qph, abort_flag, a.status)) goto done;
           tc_fence_after();
           const uint32_t qb = smem_u32(qst + qs * q_bytes);
-          const uint32_t acc = tmem + cb * kOutTok;
+          const uint32_t acc = tmem + cb * 128;
           for (int kk = 0; kk < D / 16; ++kk) {
-            const int at = kk / 4;
-            const uint32_t ko = (kk % 4) * 32;
-            const uint64_t bdesc = smem_desc(qb + at * kOutTok * 128 + ko, 16, 1024);
-            mma_bf16(acc, smem_desc(im + at * kImgRegion + ko, 16, 1024), bdesc, id, kk > 0 ? 1u : 0u);
-            mma_bf16(acc, smem_desc(im + (NA + at) * kImgRegion + ko, 16, 1024), bdesc, id, 1u);
+            const uint32_t ko = (kk >> 2) * (kOutTok * 128) + (kk & 3) * 32;
+            const uint32_t so = (kk >> 2) * (D * 128) + (kk & 3) * 32;
+            const uint64_t ad = smem_desc(qb + ko, 16, 1024);
+            mma_bf16(acc, ad, smem_desc(im + so, 16, 1024), id, kk > 0 ? 1u : 0u);
+            mma_bf16(acc, ad, smem_desc(im + NA * D * 128 + so, 16, 1024), id, 1u);
           }
           mma_commit(smem_u32(&qempty[qs]));
           mma_commit(smem_u32(&accfull[cb]));
-          if (++qs == kOutQStages) { qs = 0; qphase ^= 1; }
-          if (++cb == kOutAcc) { cb = 0; cphase ^= 1; }
+          if (++qs == kOutQStages) { qs = 0; qph ^= 1; }
+          if (++cb == kOutAcc) { cb = 0; cph ^= 1; }
         }
         mma_commit(smem_u32(&aempty[ab]));
-        if (++ab == NB) { ab = 0; aphase ^= 1; }
+        if (++ab == 2) { ab = 0; aph ^= 1; }
       }
     }
   } else {
-    // ---------------- epilogue: thread = output column j, 128 tokens per tile
-    const int j = warp * 32 + lane;
+    // ---------------- epilogue: warp w owns token rows 32w .. 32w + 31 of each tile
+    const int row = warp * 32 + lane;
     int cb = 0;
-    uint32_t cphase = 0;
+    uint32_t cph = 0;
     for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
       for (int tile = 0; tile < ntiles; ++tile) {
-        if (threadIdx.x == 0) bulk_wait_read0();  // staging buffer free again
-        if (barrier_any(1, 128, *abort_flag)) goto done;
-        const bool ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[cb]), cphase, abort_flag, a.status));
-        if (ok) {
-          tc_fence_after();
-          const uint32_t acc = tmem + ((uint32_t)(warp * 32) << 16) + cb * kOutTok;
-          uint8_t* sreg = stg + (j / 64) * kOutTok * 128;
-          for (int c0 = 0; c0 < kOutTok; c0 += 16) {
-            float v[16];
-            tmem_ld16(acc + c0, v);
-            tmem_ld_wait();
-            if (j < D) {
+        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[cb]), cph, abort_flag, a.status))) goto done;
+        tc_fence_after();
+        if (lane == 0) bulk_wait_read0();  // this warp's previous store has read its slice
+        __syncwarp();
+        const uint32_t acc = tmem + ((uint32_t)(warp * 32) << 16) + cb * 128;
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          float v[32];
+          tmem_ld16(acc + c0, *reinterpret_cast<float(*)[16]>(&v[0]));
+          if (c0 + 16 < D) tmem_ld16(acc + c0 + 16, *reinterpret_cast<float(*)[16]>(&v[16]));
+          tmem_ld_wait();
+          uint8_t* reg = stg + (c0 >> 6) * (kOutTok * 128);
 #pragma unroll
-              for (int u = 0; u < 16; ++u)
-                *reinterpret_cast<__nv_bfloat16*>(sreg + sw128_off(c0 + u, j % 64)) =
-                    __float2bfloat16_rn(v[u] * a.scale);
+          for (int h = 0; h < 4; ++h) {
+            if (c0 + 8 * h < D) {
+              uint4 o;
+              o.x = pack_bf16(v[8 * h + 0] * a.scale, v[8 * h + 1] * a.scale);
+              o.y = pack_bf16(v[8 * h + 2] * a.scale, v[8 * h + 3] * a.scale);
+              o.z = pack_bf16(v[8 * h + 4] * a.scale, v[8 * h + 5] * a.scale);
+              o.w = pack_bf16(v[8 * h + 6] * a.scale, v[8 * h + 7] * a.scale);
+              *reinterpret_cast<uint4*>(reg + sw128_off(row, (c0 & 63) + 8 * h)) = o;
             }
           }
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&accempty[cb]));
         }
-        if (++cb == kOutAcc) { cb = 0; cphase ^= 1; }
+        tc_fence_before();
         fence_proxy_async_smem();
-        if (barrier_any(1, 128, !ok || *abort_flag)) goto done;
-        if (threadIdx.x == 0) {
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(&accempty[cb]));
           for (int at = 0; at < NA; ++at)
-            tma_store_3d(&mapO, smem_u32(stg + at * kOutTok * 128), 64 * at, tile * kOutTok, (int)f);
+            tma_store_3d(&mapO, smem_u32(stg + at * (kOutTok * 128) + warp * 32 * 128), 64 * at,
+                         tile * kOutTok + warp * 32, (int)f);
           bulk_commit();
         }
+        if (++cb == kOutAcc) { cb = 0; cph ^= 1; }
       }
     }
   }
 done:
-  if (threadIdx.x == 0) bulk_wait0();  // output stores complete
+  if (warp < 4 && lane == 0) bulk_wait0();  // this warp's output stores are complete
   if (warp == 5 && lane == 0) {
     mma_commit(smem_u32(mma_done));
     wait_bounded(smem_u32(mma_done), 0, 500000000ull);
@@ -831,19 +842,15 @@ int num_sms() {
 
 constexpr int kBarBytes = 256;
 
-// Kernels that allocate all 512 TMEM columns ask for more than half of the SM's
-// shared memory so that two of them never share an SM.
-constexpr int kOneCtaPerSm = 116 * 1024;
-int at_least_half(int b) { return b > kOneCtaPerSm ? b : kOneCtaPerSm; }
+// Every kernel here asks for more than half of the SM's shared memory, so two of
+// them never share an SM (the gram and read-out kernels allocate all of TMEM).
 int gram_smem(int NA, int D) {
   return kGramRaw * kRawStage + kGramConv * kConvStage + NA * D * 128 + kBarBytes + 1024;
 }
 int scan_smem() { return kScanStages * (kScanMStage + kScanBStage) + 2 * kScanImg + kBarBytes + 1024; }
-int out_smem(int NA, int nb) {
-  return at_least_half(nb * 2 * NA * kImgRegion + kOutQStages * NA * kOutTok * 128 + NA * kOutTok * 128 + kBarBytes +
-                       1024);
+int out_smem(int NA, int D) {
+  return 2 * ((2 * NA * D * 128 + 1023) & ~1023) + (kOutQStages + 1) * NA * kOutTok * 128 + kBarBytes + 1024;
 }
-constexpr int kMaxSmem = 227 * 1024;
 
 }  // namespace
 
@@ -870,7 +877,7 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
 
   CUtensorMap mapK, mapV, mapQ, mapO;
   if (!make_map(&mapK, p.k, p.D, p.S, F, kGramTok) || !make_map(&mapV, p.v, p.D, p.S, F, kGramTok) ||
-      !make_map(&mapQ, p.q, p.D, p.S, F, kOutTok) || !make_map(&mapO, p.out, p.D, p.S, F, kOutTok))
+      !make_map(&mapQ, p.q, p.D, p.S, F, kOutTok) || !make_map(&mapO, p.out, p.D, p.S, F, 32))
     return kCuda;
 
   {
@@ -893,11 +900,10 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   {
-    const int nb = out_smem(NA, 2) <= kMaxSmem ? 2 : 1;
-    const int smem = out_smem(NA, nb);
+    const int smem = out_smem(NA, p.D);
     if (cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
-    OutArgs oa{s_img, F, p.S, p.D, NA, nb, p.out_scale, p.status};
+    OutArgs oa{s_img, static_cast<__nv_bfloat16*>(p.out), F, p.S, p.D, NA, p.out_scale, p.status};
     const unsigned grid = (unsigned)(F < nsm ? F : nsm);
     ProfScope ps(st, "tc_readout");
     tc_readout_kernel<<<grid, kOutThreads, smem, st>>>(mapQ, mapO, oa);
