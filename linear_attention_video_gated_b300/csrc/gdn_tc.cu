@@ -511,19 +511,25 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     // ---------------- MMA: P = M_t S_{t-1}[:, J]
     if (lane == 0) {
       const uint32_t id = idesc_bf16(128, 32, 0, 0);
+      // Descriptors of stage 0 / buffer 0; the other stages and buffers only move
+      // the start address (a 16-byte-unit field, well inside its 14 bits here).
+      uint64_t ad0[8], bd0[8];
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) {
+        ad0[kk] = smem_desc(smem_u32(mring) + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
+        bd0[kk] = smem_desc(smem_u32(img) + (kk >> 2) * (32 * 128) + (kk & 3) * 32, 16, 1024);
+      }
       int stage = 0;
       uint32_t phase = 0;
       for (int t = 0; t < T; ++t) {
-        if (!wait_or_abort(smem_u32(sready), t & 1, abort_flag, a.status)) goto done;
         if (!wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status)) goto done;
+        if (!wait_or_abort(smem_u32(sready), t & 1, abort_flag, a.status)) goto done;
         tc_fence_after();
-        const uint32_t ms = smem_u32(mring + stage * kScanMStage);
-        const uint32_t sb = smem_u32(img + (t & 1) * kScanImg);
-        for (int kk = 0; kk < KS; ++kk) {
-          const uint32_t ao = (kk >> 2) * (128 * 128) + (kk & 3) * 32;
-          const uint32_t bo = (kk >> 2) * (32 * 128) + (kk & 3) * 32;
-          mma_bf16(tmem, smem_desc(ms + ao, 16, 1024), smem_desc(sb + bo, 16, 1024), id, kk > 0 ? 1u : 0u);
-        }
+        const uint64_t ao = (uint64_t)((stage * kScanMStage) >> 4);
+        const uint64_t bo = (uint64_t)(((t & 1) * kScanImg) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          if (kk < KS) mma_bf16(tmem, ad0[kk] + ao, bd0[kk] + bo, id, kk > 0 ? 1u : 0u);
         mma_commit(smem_u32(pfull));
         mma_commit(smem_u32(&empty[stage]));
         if (++stage == kScanStages) { stage = 0; phase ^= 1; }
@@ -609,10 +615,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
       if (barrier_any(1, 128, !__all_sync(0xffffffffu, ok) || *abort_flag)) goto done;
       if (threadIdx.x == 0) {
         const uint8_t* im = img + ((t + 1) & 1) * kScanImg;
-        uint8_t* dst = a.s_img + (size_t)f * 2 * NA * D * 128 + (size_t)16 * cb * 128;
-        for (int hl = 0; hl < 2; ++hl)
-          for (int at = 0; at < NA; ++at)
-            bulk_s2g(dst + (size_t)(hl * NA + at) * D * 128, smem_u32(im + at * 32 * 128 + hl * 16 * 128), 16 * 128);
+        bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(im), NA * 32 * 128);
         bulk_commit();
         asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // the store of S_{t-1} has read its buffer
         mbar_arrive(smem_u32(sready));
@@ -642,8 +645,8 @@ done:
 // readout: O_t = Q_t S_t / sqrt(D) per frame-head and 128-token tile.
 //
 // Persistent CTAs.  Per frame-head the S_t image (bf16 hi + lo, the B operand:
-// K-major, row n = value column, D rows) arrives with one bulk copy into one of
-// two buffers; Q tiles of 128 tokens stream through a 2-deep TMA ring; per tile
+// K-major, row n = value column, D rows) is gathered from the scan's column
+// blocks (2 KB bulk copies) into one of two buffers; Q tiles of 128 tokens stream through a 2-deep TMA ring; per tile
 // two MMA chains (hi, lo) accumulate O_tile (128 tokens x D) in one of four
 // TMEM accumulators.  Each epilogue warp owns 32 token rows: it scales and
 // rounds them to bf16 into its own slice of a staging tile and TMA-stores the
@@ -719,7 +722,13 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         if (!wait_or_abort(smem_u32(&aempty[ra.stage]), ra.phase ^ 1, abort_flag, a.status)) break;
         const uint32_t afb = smem_u32(&afull[ra.stage]);
         mbar_arrive_expect_tx(afb, img_bytes);
-        bulk_g2s(smem_u32(imgs + ra.stage * img_stride), a.s_img + (size_t)f * img_bytes, img_bytes, afb);
+        // block cb of the scan = [atom][hi 16 rows | lo 16 rows][128 B]
+        const uint8_t* src = a.s_img + (size_t)f * img_bytes;
+        for (int cb = 0; cb < D / 16; ++cb)
+          for (int at = 0; at < NA; ++at)
+            for (int hl = 0; hl < 2; ++hl)
+              bulk_g2s(smem_u32(imgs + ra.stage * img_stride + (hl * NA + at) * D * 128 + cb * 16 * 128),
+                       src + ((size_t)cb * NA + at) * (32 * 128) + hl * 16 * 128, 16 * 128, afb);
         ra.mark_issued();
         ra.advance();
         for (int tile = 0; tile < ntiles; ++tile) {
