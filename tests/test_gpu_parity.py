@@ -141,6 +141,26 @@ def test_repeat_calls_are_deterministic(mode):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+@pytest.mark.parametrize("shape", [(1, 20, 13, 880, 112), (2, 3, 9, 300, 64), (1, 1, 4, 129, 16), (1, 9, 5, 200, 128)])
+def test_sequential_equals_split_bitwise(shape):
+    """The sequential and split forms agree bit for bit, each run on a workspace
+    filled with NaN bit patterns, so a read of scratch that no kernel has written
+    (a transition term or a state block read before it is stored) cannot go
+    unnoticed."""
+    B, H, T, S, D = shape
+    wl = synth.WORKLOADS["short"].with_(B=B, H=H, T=T, S=S, D=D, seed=777 + D)
+    x = synth.full(wl)
+    ins = parity.upload(wl, x)
+    S0 = torch.from_numpy(np.stack([np.stack([synth.state(wl, b, h) for h in range(H)]) for b in range(B)])).cuda()
+    results = []
+    for mode in (0, 2):
+        need = binding.gdn_workspace_bytes(B, H, T, S, D, binding.GDN_BF16, mode)
+        ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+        results.append(run(*ins, state_in=S0, mode=mode, workspace=ws))
+    a, b = results
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
 def test_plain_entry_matches_explicit_workspace():
     wl, x = _small_bf16(T=5)
     ins = parity.upload(wl, x)
