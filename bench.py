@@ -222,9 +222,10 @@ def _fill_head(wl, b, h, hq, hk, hv, hg, hb):
 
 # ----------------------------------------------------------------- arms
 
-def config_of(wl, mode) -> dict:
+def config_of(wl, mode, gate_logits=False) -> dict:
+    gates = ", gates from logits (fused gate prologue)" if gate_logits else ""
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} T={wl.T} S={wl.S} D={wl.D} {wl.dtype} I/O, fp32 state, "
-                        f"single call over all frames",
+                        f"single call over all frames{gates}",
             "B": wl.B, "H": wl.H, "T": wl.T, "S": wl.S, "D": wl.D,
             "mode": {0: "sequential", 1: "prefix", 2: "split", 3: "cluster"}[mode],
             "l2": f"no flush: inputs larger than L2 ({alg_bytes(wl) / 1e9:.1f} GB moved per step vs 126 MB L2)"}
@@ -270,7 +271,7 @@ def ours_arm(args, rank, world, local_rank):
     hq, hk, hv = (torch.empty(shape, dtype=hdt, pin_memory=True) for _ in range(3))
     hg = torch.empty((wl.B, wl.H, wl.T), dtype=torch.float32, pin_memory=True)
     hb = torch.empty((wl.B, wl.H, wl.T, wl.S), dtype=torch.float32, pin_memory=True)
-    synth.fill_io(wl, hq.numpy(), hk.numpy(), hv.numpy(), hg.numpy(), hb.numpy())
+    synth.fill_io(wl, hq.numpy(), hk.numpy(), hv.numpy(), hg.numpy(), hb.numpy(), logits=args.gate_logits)
     if wl.dtype == "bf16":
         hq, hk, hv = (t.view(torch.bfloat16) for t in (hq, hk, hv))
     q, k, v = (t.to(dev) for t in (hq, hk, hv))
@@ -282,10 +283,12 @@ def ours_arm(args, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     sp = stream.cuda_stream
 
+    entry = binding.gdn_frame_fwd_from_logits if args.gate_logits else binding.gdn_frame_fwd_ex
+
     def step(qq=q, kk=k, vv=v, gg=g, bb=beta, oo=out, so=st_out):
-        rc = binding.gdn_frame_fwd_ex(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), gg.data_ptr(), bb.data_ptr(),
-                                      None, oo.data_ptr(), so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype,
-                                      mode, ws.data_ptr(), need, sp)
+        rc = entry(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), gg.data_ptr(), bb.data_ptr(),
+                   None, oo.data_ptr(), so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype,
+                   mode, ws.data_ptr(), need, sp)
         if rc != 0:
             raise binding.GDNError(rc, "gdn_frame_fwd_ex")
 
@@ -387,7 +390,7 @@ def ours_arm(args, rank, world, local_rank):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-                "config": config_of(wl, mode),
+                "config": config_of(wl, mode, args.gate_logits),
                 "roofline_pct": 100.0 * call_gbs / pk["hbm_gbs"],
                 "call_achieved_gbs": call_gbs,
                 "tflops": alg_flops(wl) / (ms / 1e3) / 1e12,
@@ -405,6 +408,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="minute", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3])
+    ap.add_argument("--gate-logits", action="store_true",
+                    help="pass g and beta as logits (gdn_frame_fwd_from_logits)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--no-cpu-baseline", action="store_true")

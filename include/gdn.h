@@ -133,6 +133,23 @@ int gdn_frame_fwd_ex(const void* q, const void* k, const void* v,
                      void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gdn_frame_fwd_from_logits -- gdn_frame_fwd_ex with the gate computations fused
+ * into the scan's kernels (the pages fuse the "GDN scan and gate ops"; zhichai.net
+ * summary, the paragraph after training Stage 4).  g_logit [B,H,T] and
+ * beta_logit [B,H,T,S] hold raw float32 logits; where the kernels load them they
+ * become the decay g = exp(-softplus(g_logit)) = 1 / (1 + e^g_logit), in (0, 1),
+ * and the delta-rule weight beta = sigmoid(beta_logit), in (0, 1).  The pages do
+ * not state the gates' parameterisation: these are the maps the one-minute
+ * workload's gates are drawn through.  Everything else (arguments, workspace,
+ * modes, errors) is as gdn_frame_fwd_ex.
+ */
+int gdn_frame_fwd_from_logits(const void* q, const void* k, const void* v,
+                              const float* g_logit, const float* beta_logit, const float* state_in,
+                              void* out, float* state_out,
+                              int B, int H, int T, int S, int D, int dtype, int mode,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * gdn_last_error -- synchronises `stream`, then returns and clears the
  * device-side status word: GDN_OK, GDN_ERR_TIMEOUT (a kernel's bounded wait on
  * an mbarrier or a flag gave up; its results are invalid), or GDN_ERR_CUDA

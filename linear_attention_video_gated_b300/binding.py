@@ -27,6 +27,8 @@ _SIGS = {
     "gdn_frame_fwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "gdn_frame_fwd_ex": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                               ctypes.c_size_t, _P]),
+    "gdn_frame_fwd_from_logits": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
+                                       ctypes.c_size_t, _P]),
     "gdn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
     "gdn_frame_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "gdn_noalloc_scratch_bytes": (ctypes.c_size_t, []),
@@ -75,6 +77,12 @@ def gdn_frame_fwd_ex(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, 
                                   workspace, workspace_bytes, stream)
 
 
+def gdn_frame_fwd_from_logits(q, k, v, g_logit, beta_logit, state_in, out, state_out, B, H, T, S, D, dtype, mode,
+                              workspace, workspace_bytes, stream) -> int:
+    return lib().gdn_frame_fwd_from_logits(q, k, v, g_logit, beta_logit, state_in, out, state_out, B, H, T, S, D,
+                                           dtype, mode, workspace, workspace_bytes, stream)
+
+
 def gdn_frame_fwd_noalloc(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, stream) -> int:
     return lib().gdn_frame_fwd_noalloc(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, stream)
 
@@ -120,7 +128,7 @@ def _ptr(t):
 
 
 def frame_fwd(q, k, v, g, beta, state_in=None, out=None, state_out=None, mode=None,
-              workspace=None, stream=None, want_state=True):
+              workspace=None, stream=None, want_state=True, gate_logits=False):
     """Runs the forward scan on torch CUDA tensors through the C ABI.
 
     q, k, v: [B,H,T,S,D] float32 or bfloat16, contiguous; g: [B,H,T] float32;
@@ -129,6 +137,8 @@ def frame_fwd(q, k, v, g, beta, state_in=None, out=None, state_out=None, mode=No
     mode=None calls gdn_frame_fwd (library-managed scratch); mode=0/1/2/3
     (sequential, prefix, split, cluster) calls gdn_frame_fwd_ex with ``workspace``
     (a uint8 CUDA tensor, allocated if None).
+    gate_logits=True passes g and beta as raw logits to gdn_frame_fwd_from_logits
+    (mode None then means the sequential form).
     Returns (out, state_out).  Raises GDNError on a non-zero status.
     """
     import torch
@@ -156,6 +166,8 @@ def frame_fwd(q, k, v, g, beta, state_in=None, out=None, state_out=None, mode=No
     st = strm.cuda_stream
     args = (_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(out), _ptr(state_out),
             B, H, T, S, D, dtype)
+    if gate_logits and mode is None:
+        mode = GDN_MODE_SEQUENTIAL
     if mode is None:
         rc = gdn_frame_fwd(*args, st)
     else:
@@ -166,7 +178,8 @@ def frame_fwd(q, k, v, g, beta, state_in=None, out=None, state_out=None, mode=No
             if strm != cur:
                 workspace.record_stream(strm)
         wbytes = 0 if workspace is None else workspace.numel()
-        rc = gdn_frame_fwd_ex(*args, mode, _ptr(workspace), wbytes, st)
+        fn = gdn_frame_fwd_from_logits if gate_logits else gdn_frame_fwd_ex
+        rc = fn(*args, mode, _ptr(workspace), wbytes, st)
     if rc != 0:
         raise GDNError(rc, "gdn_frame_fwd")
     return out, state_out

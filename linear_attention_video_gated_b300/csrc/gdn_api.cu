@@ -118,6 +118,22 @@ cudaEvent_t prof_event() {
   return e;
 }
 
+// gdn_frame_fwd_ex and gdn_frame_fwd_from_logits: validation, workspace check, launch.
+int forward_ex(const void* q, const void* k, const void* v, const float* g, const float* beta, const float* state_in,
+               void* out, float* state_out, int B, int H, int T, int S, int D, int dtype, int mode, void* workspace,
+               size_t workspace_bytes, void* stream, int gate_logits) {
+  Problem p{};
+  int rc = validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode, &p);
+  if (rc != kOk) return rc;
+  p.gate_logits = gate_logits;
+  const size_t need = workspace_for(p);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return kWorkspace;
+    if (!aligned(workspace, 256)) return kMisaligned;
+  }
+  return forward(p, workspace, static_cast<cudaStream_t>(stream));
+}
+
 }  // namespace
 
 ProfScope::ProfScope(cudaStream_t st, const char* name) : st_(st), idx_(-1) {
@@ -145,15 +161,16 @@ extern "C" {
 int gdn_frame_fwd_ex(const void* q, const void* k, const void* v, const float* g, const float* beta,
                      const float* state_in, void* out, float* state_out, int B, int H, int T, int S, int D,
                      int dtype, int mode, void* workspace, size_t workspace_bytes, void* stream) {
-  Problem p{};
-  int rc = validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode, &p);
-  if (rc != kOk) return rc;
-  const size_t need = workspace_for(p);
-  if (need > 0) {
-    if (!workspace || workspace_bytes < need) return kWorkspace;
-    if (!aligned(workspace, 256)) return kMisaligned;
-  }
-  return forward(p, workspace, static_cast<cudaStream_t>(stream));
+  return gdn::forward_ex(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode, workspace,
+                         workspace_bytes, stream, 0);
+}
+
+int gdn_frame_fwd_from_logits(const void* q, const void* k, const void* v, const float* g_logit,
+                              const float* beta_logit, const float* state_in, void* out, float* state_out, int B,
+                              int H, int T, int S, int D, int dtype, int mode, void* workspace,
+                              size_t workspace_bytes, void* stream) {
+  return gdn::forward_ex(q, k, v, g_logit, beta_logit, state_in, out, state_out, B, H, T, S, D, dtype, mode,
+                         workspace, workspace_bytes, stream, 1);
 }
 
 int gdn_frame_fwd(const void* q, const void* k, const void* v, const float* g, const float* beta,

@@ -83,6 +83,7 @@ struct FusedArgs {
   __nv_bfloat16* out;
   float* state_out;
   int T, S, D, NC, NA;
+  int gate_logits;
   float m_scale, b_scale, o_scale;
   unsigned int* status;
 };
@@ -426,7 +427,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, 1)
       const float* bf = a.beta + f * S;
       for (int ch = 0; ch < nkc; ++ch) {
         const int s = ch * kKTok + tok;
-        const float bs = s < S ? __ldg(bf + s) : 0.f;
+        const float bs = s < S ? beta_of(__ldg(bf + s), a.gate_logits) : 0.f;
         if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&kfull[ks]), kph, abort_flag, a.status))) goto done;
         uint8_t* st = kring + ks * C::kKStage;
         uint8_t* bg = st + C::kBgOff;
@@ -600,7 +601,7 @@ __global__ void __launch_bounds__(Cfg<W>::kThreads, 1)
     for (int t = 0; t < T; ++t) {
       if (t + 1 < T && !gram_epi(t + 1, bnext)) goto done;
       const long long f = bh * T + t;
-      const float gt = __ldg(a.g + f);
+      const float gt = decay_of(__ldg(a.g + f), a.gate_logits);
       const bool ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(pfull), t & 1, abort_flag, a.status));
       if (ok) {
         tc_fence_after();
@@ -702,6 +703,7 @@ int launch_fused(const Problem& p, const CUtensorMap& mapK, const CUtensorMap& m
                p.D,
                NC,
                (p.D + 63) / 64,
+               p.gate_logits,
                p.key_scale * p.key_scale,
                p.key_scale,
                p.out_scale,

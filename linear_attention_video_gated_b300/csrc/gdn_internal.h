@@ -32,6 +32,7 @@ struct Problem {
   int B, H, T, S, D;
   int dtype;  // gdn_dtype_t
   int mode;   // gdn_mode_t
+  int gate_logits;  // 1: g and beta hold raw logits, mapped by decay_of / beta_of where loaded
   float key_scale;  // 1/sqrt(D*S)
   float out_scale;  // 1/sqrt(D)
   unsigned int* status;  // device-side status word (first error wins)
@@ -43,6 +44,13 @@ struct Problem {
 enum Status {
   kOk = 0, kInvalidArg = 1, kUnsupported = 2, kMisaligned = 3, kCuda = 4, kTimeout = 5, kWorkspace = 6
 };
+
+// The gate prologue fused into the kernels (gdn_frame_fwd_from_logits): raw
+// logits x become the per-frame decay g = exp(-softplus(x)) = 1 / (1 + e^x) and
+// the per-token delta-rule weight beta = sigmoid(x) = 1 / (1 + e^-x) where the
+// kernels load them.
+__device__ __forceinline__ float decay_of(float x, int logits) { return logits ? 1.f / (1.f + expf(x)) : x; }
+__device__ __forceinline__ float beta_of(float x, int logits) { return logits ? 1.f / (1.f + expf(-x)) : x; }
 
 // Records a device-side error in the status word; the first error wins.
 __device__ __forceinline__ void report_device_error(unsigned int* status, unsigned int code) {

@@ -36,7 +36,7 @@ __device__ __forceinline__ void from_f32(__nv_bfloat16& d, float x) { d = __floa
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads) gram_kernel(const TIn* __restrict__ k, const TIn* __restrict__ v,
                                                         const float* __restrict__ beta, float* __restrict__ Mws,
-                                                        float* __restrict__ bws, int S, int D, float ck) {
+                                                        float* __restrict__ bws, int S, int D, float ck, int logits) {
   extern __shared__ float smem[];
   float* sA = smem;             // [kTok][D]  beta * k
   float* sX = smem + kTok * D;  // [kTok][D]  k or v
@@ -60,7 +60,7 @@ __global__ void __launch_bounds__(kThreads) gram_kernel(const TIn* __restrict__ 
       float a = 0.f, x = 0.f;
       if (s < n) {
         const long long o = (long long)(s0 + s) * D + (idx % D);
-        a = bf[s0 + s] * to_f32(kf[o]);
+        a = beta_of(bf[s0 + s], logits) * to_f32(kf[o]);
         x = to_f32(xf[o]);
       }
       sA[idx] = a;
@@ -154,7 +154,8 @@ __device__ void affine_step(float* sX, const float* sM, const float* __restrict_
 // Sequential scan: one CTA per head.
 __global__ void __launch_bounds__(kThreads) scan_kernel(const float* __restrict__ Mws, const float* __restrict__ bws,
                                                         const float* __restrict__ g, const float* state_in,
-                                                        float* __restrict__ Sws, float* state_out, int T, int D) {
+                                                        float* __restrict__ Sws, float* state_out, int T, int D,
+                                                        int logits) {
   extern __shared__ float smem[];
   float* sS = smem;          // [D][D]
   float* sM = smem + D * D;  // [D][D]
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const float* __restrict_
     const long long f = bh * T + t;
     for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) sM[idx] = Mws[f * D * D + idx];
     __syncthreads();
-    affine_step(sS, sM, bws + f * D * D, g[f], D, D, 0, Sws + f * D * D);
+    affine_step(sS, sM, bws + f * D * D, decay_of(g[f], logits), D, D, 0, Sws + f * D * D);
   }
   if (state_out)
     for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) state_out[bh * D * D + idx] = sS[idx];
@@ -176,7 +177,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const float* __restrict_
 // starting from [I | 0].  One CTA per (head, chunk).
 __global__ void __launch_bounds__(kThreads) compose_kernel(const float* __restrict__ Mws, const float* __restrict__ bws,
                                                            const float* __restrict__ g, float* __restrict__ maps,
-                                                           int T, int D, int nchunks) {
+                                                           int T, int D, int nchunks, int logits) {
   extern __shared__ float smem[];
   float* sX = smem;              // [D][2D]
   float* sM = smem + 2 * D * D;  // [D][D]
@@ -192,7 +193,7 @@ __global__ void __launch_bounds__(kThreads) compose_kernel(const float* __restri
     const long long f = bh * T + t;
     for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) sM[idx] = Mws[f * D * D + idx];
     __syncthreads();
-    affine_step(sX, sM, bws + f * D * D, g[f], D, 2 * D, D, nullptr);
+    affine_step(sX, sM, bws + f * D * D, decay_of(g[f], logits), D, 2 * D, D, nullptr);
   }
   float* dst = maps + (bh * nchunks + c) * 2 * D * D;
   for (int idx = threadIdx.x; idx < 2 * D * D; idx += blockDim.x) dst[idx] = sX[idx];
@@ -260,7 +261,8 @@ __global__ void __launch_bounds__(kThreads) boundary_kernel(const float* __restr
 // Prefix mode, pass 3: replay each chunk from its true initial state, writing S_t.
 __global__ void __launch_bounds__(kThreads) replay_kernel(const float* __restrict__ Mws, const float* __restrict__ bws,
                                                           const float* __restrict__ g, const float* __restrict__ starts,
-                                                          float* __restrict__ Sws, int T, int D, int nchunks) {
+                                                          float* __restrict__ Sws, int T, int D, int nchunks,
+                                                          int logits) {
   extern __shared__ float smem[];
   float* sS = smem;
   float* sM = smem + D * D;
@@ -274,7 +276,7 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const float* __restric
     const long long f = bh * T + t;
     for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) sM[idx] = Mws[f * D * D + idx];
     __syncthreads();
-    affine_step(sS, sM, bws + f * D * D, g[f], D, D, 0, Sws + f * D * D);
+    affine_step(sS, sM, bws + f * D * D, decay_of(g[f], logits), D, D, 0, Sws + f * D * D);
   }
 }
 
@@ -358,7 +360,8 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
   {
     ProfScope pg(st, "simt_gram");
     gram_kernel<TIn><<<dim3((unsigned)p.BHT(), 2), kThreads, gram_smem, st>>>(
-        static_cast<const TIn*>(p.k), static_cast<const TIn*>(p.v), p.beta, Mws, bws, p.S, D, p.key_scale);
+        static_cast<const TIn*>(p.k), static_cast<const TIn*>(p.v), p.beta, Mws, bws, p.S, D, p.key_scale,
+        p.gate_logits);
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
 
@@ -368,7 +371,8 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
       return kCuda;
     {
       ProfScope ps(st, "simt_scan");
-      scan_kernel<<<(unsigned)p.BH(), kThreads, smem, st>>>(Mws, bws, p.g, p.state_in, Sws, p.state_out, p.T, D);
+      scan_kernel<<<(unsigned)p.BH(), kThreads, smem, st>>>(Mws, bws, p.g, p.state_in, Sws, p.state_out, p.T, D,
+                                                             p.gate_logits);
     }
     if (cudaGetLastError() != cudaSuccess) return kCuda;
   } else {
@@ -379,7 +383,8 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
       return kCuda;
     {
       ProfScope pc(st, "simt_compose");
-      compose_kernel<<<(unsigned)(p.BH() * L.nchunks), kThreads, csmem, st>>>(Mws, bws, p.g, maps, p.T, D, L.nchunks);
+      compose_kernel<<<(unsigned)(p.BH() * L.nchunks), kThreads, csmem, st>>>(Mws, bws, p.g, maps, p.T, D, L.nchunks,
+                                                                               p.gate_logits);
     }
     if (cudaGetLastError() != cudaSuccess) return kCuda;
     if (cudaFuncSetAttribute(boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem) !=
@@ -396,7 +401,7 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
     {
       ProfScope pr(st, "simt_replay");
       replay_kernel<<<(unsigned)(p.BH() * L.nchunks), kThreads, rsmem, st>>>(Mws, bws, p.g, starts, Sws, p.T, D,
-                                                                            L.nchunks);
+                                                                            L.nchunks, p.gate_logits);
     }
     if (cudaGetLastError() != cudaSuccess) return kCuda;
   }

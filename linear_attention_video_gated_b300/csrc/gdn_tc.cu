@@ -180,6 +180,7 @@ constexpr int kConvStage = 4 * kGramRegion;  // AH atoms (2) then AL atoms (2): 
 
 struct GramArgs {
   const float* beta;
+  int gate_logits;
   uint8_t* m_img;  // F x NA x D rows x 128 B
   float* b_blk;    // F x (D/16) x D x 16
   long long nitems;
@@ -314,14 +315,18 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     const int r0 = ct >> 3;
     auto beta_at = [&](long long f, int c, int rw) {
       const int s = c * kGramTok + rw;
-      return (f < a.nitems && s < S) ? __ldg(a.beta + f * S + s) : 0.f;
+      // raw value, mapped when used: mapping here would wait for the load
+      return (f < a.nitems && s < S) ? __ldg(a.beta + f * S + s) : -INFINITY;
     };
     long long fn = blockIdx.x;
     int cn = 0;
+    // beta of token rows r0 and r0 + 32: raw values loaded one tile ahead, mapped
+    // (rows past S, loaded as -inf, give 0) after the current tile is converted.
+    auto mapped = [&](float x) { return x == -INFINITY ? 0.f : beta_of(x, a.gate_logits); };
     float bn0 = beta_at(fn, 0, r0), bn1 = beta_at(fn, 0, r0 + 32);
+    float b0 = mapped(bn0), b1 = mapped(bn1);
     for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
       for (int c = 0; c < nchunks; ++c) {
-        const float b0 = bn0, b1 = bn1;
         if (++cn == nchunks) { cn = 0; fn += gridDim.x; }
         bn0 = beta_at(fn, cn, r0);
         bn1 = beta_at(fn, cn, r0 + 32);
@@ -348,6 +353,8 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&conv_full[cs]));
         if (++rs == kGramRaw) { rs = 0; rph ^= 1; }
         if (++cs == kGramConv) { cs = 0; cph ^= 1; }
+        b0 = mapped(bn0);
+        b1 = mapped(bn1);
       }
     }
   } else {
@@ -438,6 +445,7 @@ struct ScanArgs {
   const uint8_t* m_img;
   const float* b_blk;
   const float* g;
+  int gate_logits;
   const float* state_in;
   uint8_t* s_img;
   float* state_out;
@@ -471,7 +479,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
       mbar_init(smem_u32(&empty[s]), 5);  // the MMA's commit + the 4 epilogue warps (b read)
     }
     mbar_init(smem_u32(pfull), 1);
-    mbar_init(smem_u32(sready), 1);
+    mbar_init(smem_u32(sready), 4);  // each epilogue warp, once its rows of the state image are written
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -511,6 +519,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     // ---------------- MMA: P = M_t S_{t-1}[:, J]
     if (lane == 0) {
       const uint32_t id = idesc_bf16(128, 32, 0, 0);
+      // the state block of frame u (image buffer (u + 1) & 1) to global memory, laid
+      // out as in shared memory
+      auto store_block = [&](int u) {
+        const long long f = bh * T + u;
+        bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(img + ((u + 1) & 1) * kScanImg),
+                 NA * 32 * 128);
+        bulk_commit();
+      };
       // Descriptors of stage 0 / buffer 0; the other stages and buffers only move
       // the start address (a 16-byte-unit field, well inside its 14 bits here).
       uint64_t ad0[8], bd0[8];
@@ -530,9 +546,16 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           if (kk < KS) mma_bf16(tmem, ad0[kk] + ao, bd0[kk] + bo, id, kk > 0 ? 1u : 0u);
+        if (t >= 1) store_block(t - 1);
+        // The store of S_{t-2} has read its buffer, which S_t may now overwrite.
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         mma_commit(smem_u32(pfull));
         mma_commit(smem_u32(&empty[stage]));
         if (++stage == kScanStages) { stage = 0; phase ^= 1; }
+      }
+      if (T > 0) {
+        if (!wait_or_abort(smem_u32(sready), T & 1, abort_flag, a.status)) goto done;
+        store_block(T - 1);
       }
     }
   } else {
@@ -570,14 +593,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     };
     write_img(img);  // S_{-1} into buffer 0
     fence_proxy_async_smem();
-    if (barrier_any(1, 128, *abort_flag)) goto done;
-    if (threadIdx.x == 0) mbar_arrive(smem_u32(sready));
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(sready));
     int stage = 0;
     uint32_t phase = 0;
-    float gnext = T > 0 ? __ldg(a.g + bh * T) : 0.f;
+    float gnext = T > 0 ? __ldg(a.g + bh * T) : 0.f;  // raw; mapped when used
     for (int t = 0; t < T; ++t) {
       const long long f = bh * T + t;
-      const float gt = gnext;
+      const float gt = decay_of(gnext, a.gate_logits);
       if (t + 1 < T) gnext = __ldg(a.g + f + 1);
       const bool ok = wait_or_abort(smem_u32(pfull), t & 1, abort_flag, a.status) &&
                       wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
@@ -606,20 +629,15 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) x[j] = fmaf(gt, x[j] - (p[j] + pl[j]), bv[j]);
         }
-        // S_t goes into the buffer that held S_{t-2}, whose store finished
-        // reading it before S_{t-1} was released to the MMA.
+        // S_t goes into the buffer of S_{t-2}, whose store has read it (the MMA
+        // thread waited for that before committing pfull(t)).
         write_img(img + ((t + 1) & 1) * kScanImg);
         fence_proxy_async_smem();
       }
       if (++stage == kScanStages) { stage = 0; phase ^= 1; }
-      if (barrier_any(1, 128, !__all_sync(0xffffffffu, ok) || *abort_flag)) goto done;
-      if (threadIdx.x == 0) {
-        const uint8_t* im = img + ((t + 1) & 1) * kScanImg;
-        bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(im), NA * 32 * 128);
-        bulk_commit();
-        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");  // the store of S_{t-1} has read its buffer
-        mbar_arrive(smem_u32(sready));
-      }
+      if (!__all_sync(0xffffffffu, ok)) goto done;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(sready));
     }
     if (row && a.state_out) {
       float4* so = reinterpret_cast<float4*>(a.state_out + ((size_t)bh * D + i) * D + 16 * cb);
@@ -628,8 +646,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     }
   }
 done:
-  if (threadIdx.x == 0) bulk_wait0();  // state image stores complete
   if (warp == 5 && lane == 0) {
+    bulk_wait0();  // state block stores complete
     mma_commit(smem_u32(mma_done));
     wait_bounded(smem_u32(mma_done), 0, 500000000ull);
   }
@@ -893,7 +911,8 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
     const int smem = gram_smem(NA, p.D);
     if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
-    GramArgs ga{p.beta, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale, p.key_scale, p.status};
+    GramArgs ga{p.beta, p.gate_logits, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale, p.key_scale,
+                p.status};
     const unsigned grid = (unsigned)(F < nsm ? F : nsm);
     ProfScope ps(st, "tc_gram");
     tc_gram_kernel<<<grid, kGramThreads, smem, st>>>(mapK, mapV, ga);
@@ -903,7 +922,7 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
     const int smem = scan_smem();
     if (cudaFuncSetAttribute(tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
-    ScanArgs sa{m_img, b_mat, p.g, p.state_in, s_img, p.state_out, p.T, p.D, NA, p.status};
+    ScanArgs sa{m_img, b_mat, p.g, p.gate_logits, p.state_in, s_img, p.state_out, p.T, p.D, NA, p.status};
     ProfScope ps(st, "tc_scan");
     tc_scan_kernel<<<(unsigned)(p.BH() * (p.D / 16)), kScanThreads, smem, st>>>(sa);
   }

@@ -132,6 +132,32 @@ def _draw(rng: np.random.Generator, dist: tuple, n: int) -> np.ndarray:
     raise ValueError(f"unknown distribution {dist}")
 
 
+def _logits(rng: np.random.Generator, dist: tuple, n: int) -> np.ndarray:
+    """The N(0,1) draws the gate distributions map through, as float32 logits."""
+    if dist[0] not in ("exp_neg_softplus_normal", "sigmoid_normal"):
+        raise ValueError(f"{dist} is not drawn through a logit")
+    return rng.standard_normal(n).astype(np.float32)
+
+
+def gate_logit(wl: Workload, b: int, h: int, t: int) -> np.float32:
+    """Per-frame decay logit for (b,h,t): the same draw gate() maps, float32."""
+    return _logits(_rng(wl.seed, TID["g"], b, h, t), wl.g_dist, 1)[0]
+
+
+def beta_logit(wl: Workload, b: int, h: int, t: int) -> np.ndarray:
+    """Per-token beta logits for frame (b,h,t): the same draws beta() maps, float32."""
+    return _logits(_rng(wl.seed, TID["beta"], b, h, t), wl.beta_dist, wl.S)
+
+
+def logits_full(wl: Workload) -> dict:
+    """g and beta logits of every frame: {"g_logit": [B,H,T], "beta_logit": [B,H,T,S]}."""
+    gl = np.array([[[gate_logit(wl, b, h, t) for t in range(wl.T)] for h in range(wl.H)] for b in range(wl.B)],
+                  dtype=np.float32).reshape(wl.B, wl.H, wl.T)
+    bl = np.array([[[beta_logit(wl, b, h, t) for t in range(wl.T)] for h in range(wl.H)] for b in range(wl.B)],
+                  dtype=np.float32).reshape(wl.B, wl.H, wl.T, wl.S)
+    return {"g_logit": gl, "beta_logit": bl}
+
+
 def gate(wl: Workload, b: int, h: int, t: int) -> np.float32:
     """Per-frame decay g for (b,h,t): one draw, float32."""
     return _draw(_rng(wl.seed, TID["g"], b, h, t), wl.g_dist, 1)[0]
@@ -176,7 +202,8 @@ def _threads() -> int:
 
 
 def fill_io(wl: Workload, q: np.ndarray, k: np.ndarray, v: np.ndarray,
-            g: np.ndarray, bt: np.ndarray, t0: int = 0, b0: int = 0, threads: int | None = None) -> None:
+            g: np.ndarray, bt: np.ndarray, t0: int = 0, b0: int = 0, threads: int | None = None,
+            logits: bool = False) -> None:
     """Fill caller-owned host arrays with frames [t0, t0 + q.shape[2]) of batch
     indices [b0, b0 + q.shape[0]), every head.
 
@@ -195,8 +222,8 @@ def fill_io(wl: Workload, q: np.ndarray, k: np.ndarray, v: np.ndarray,
         for name, dst in (("q", q), ("k", k), ("v", v)):
             x = frame_raw(wl, name, b, h, t)
             dst[bb, h, tt] = bf16_bits(x) if wl.dtype == "bf16" else x
-        g[bb, h, tt] = gate(wl, b, h, t)
-        bt[bb, h, tt] = beta(wl, b, h, t)
+        g[bb, h, tt] = gate_logit(wl, b, h, t) if logits else gate(wl, b, h, t)
+        bt[bb, h, tt] = beta_logit(wl, b, h, t) if logits else beta(wl, b, h, t)
 
     with ThreadPoolExecutor(nthreads) as ex:
         for _ in ex.map(one, jobs, chunksize=max(1, len(jobs) // (16 * nthreads))):

@@ -128,6 +128,39 @@ def frame_fwd(q, k, v, g, beta, state_in=None):
 
 
 # ----------------------------------------------------------------------------
+# Gate prologue: raw logits -> decay g and delta-rule weight beta.
+#
+# The pages fuse unnamed "gate ops" with the GDN scan (zhichai.net summary, the
+# paragraph after training Stage 4) without stating their form.  The library's
+# logit entry point takes the plainest parameterisation that keeps each gate in
+# (0, 1) and matches how the workloads draw them: g = exp(-softplus(x)) for the
+# decay (a positive forgetting rate), beta = sigmoid(x) for the write strength.
+# ----------------------------------------------------------------------------
+
+def softplus(x):
+    """log(1 + e^x), written so that neither branch overflows."""
+    x = np.asarray(x, F64)
+    return np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x)))
+
+
+def decay_from_logit(x):
+    """g = exp(-softplus(x)), in (0, 1)."""
+    return np.exp(-softplus(x))
+
+
+def beta_from_logit(x):
+    """beta = sigmoid(x) = 1 / (1 + e^-x), in (0, 1); e^-x computed where it cannot overflow."""
+    x = np.asarray(x, F64)
+    e = np.exp(-np.abs(x))
+    return np.where(x >= 0, 1.0 / (1.0 + e), e / (1.0 + e))
+
+
+def frame_fwd_from_logits(q, k, v, g_logit, beta_logit, state_in=None):
+    """The forward scan with its gates given as logits: the gate prologue, then frame_fwd."""
+    return frame_fwd(q, k, v, decay_from_logit(g_logit), beta_from_logit(beta_logit), state_in)
+
+
+# ----------------------------------------------------------------------------
 # Affine-map forms, used only to cross-check the scan.
 # ----------------------------------------------------------------------------
 

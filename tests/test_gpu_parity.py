@@ -82,6 +82,37 @@ def test_edge_shapes(case, mode):
     parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"edge {case} mode={mode}", strict=False)
 
 
+# (dtype, B, H, T, S, D): gates given as logits (the fused gate prologue)
+LOGIT_CASES = [
+    ("bf16", 1, 20, 21, 880, 112),
+    ("bf16", 1, 2, 5, 17, 32),
+    ("bf16", 2, 1, 4, 129, 48),
+    ("bf16", 1, 1, 9, 64, 128),
+    ("f32", 2, 2, 5, 33, 128),
+    ("f32", 1, 1, 3, 100, 112),
+]
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("case", LOGIT_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_gate_logits(case, mode):
+    """gdn_frame_fwd_from_logits: g and beta computed from raw logits inside the
+    kernels, against the oracle's gate prologue followed by its scan."""
+    dt, B, H, T, S, D = case
+    if mode == 3 and dt != "bf16":
+        pytest.skip("the cluster form is bf16 only")
+    wl = synth.WORKLOADS["short"].with_(B=B, H=H, T=T, S=S, D=D, dtype=dt, seed=4000 + 7 * S + D)
+    x = synth.full(wl)
+    lg = synth.logits_full(wl)
+    q, k, v, _, _ = parity.upload(wl, x)
+    gl = torch.from_numpy(lg["g_logit"]).cuda()
+    bl = torch.from_numpy(lg["beta_logit"]).cuda()
+    out, st = run(q, k, v, gl, bl, mode=mode, gate_logits=True)
+    ro, rs = oracle.frame_fwd_from_logits(x["q"], x["k"], x["v"], lg["g_logit"], lg["beta_logit"])
+    strict = (B, H, T, S, D) == (1, 20, 21, 880, 112)
+    parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"logits {case} mode={mode}", strict=strict)
+
+
 def _small_bf16(T=21, H=3, S=300, D=112):
     wl = synth.WORKLOADS["short"].with_(H=H, T=T, S=S, D=D)
     return wl, synth.full(wl)
