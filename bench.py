@@ -348,19 +348,22 @@ def ours_arm(args, rank, world, local_rank):
                     if pk["source"] == "measured" else "fallback 6.4 TB/s"}
     call_gbs = alg_bytes(wl) / (ms / 1e3) / 1e9
 
-    # end to end through the C ABI from pinned host buffers
+    # end to end through the C ABI from pinned host buffers: gdn_frame_fwd_host,
+    # which overlaps the copies of one chunk of frames with the kernels of another
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and not args.gate_logits:
         ho = torch.empty(shape, dtype=tdt, pin_memory=True)
         hs = torch.empty((wl.B, wl.H, wl.D, wl.D), dtype=torch.float32, pin_memory=True)
         n_e2e = max(2, min(args.steps, args.e2e_steps))
+        hneed = binding.gdn_host_workspace_bytes(wl.B, wl.H, wl.T, wl.S, wl.D, dtype, args.e2e_chunk)
+        hws = torch.empty(max(hneed, 1), dtype=torch.uint8, device=dev)
 
         def e2e_step():
-            for d_, h_ in ((q, hq), (k, hk), (v, hv), (g, hg), (beta, hb)):
-                d_.copy_(h_, non_blocking=True)
-            step()
-            ho.copy_(out, non_blocking=True)
-            hs.copy_(st_out, non_blocking=True)
+            rc = binding.gdn_frame_fwd_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), hg.data_ptr(),
+                                            hb.data_ptr(), None, ho.data_ptr(), hs.data_ptr(), wl.B, wl.H, wl.T,
+                                            wl.S, wl.D, dtype, args.e2e_chunk, hws.data_ptr(), hneed, sp)
+            if rc != 0:
+                raise binding.GDNError(rc, "gdn_frame_fwd_host")
 
         e2e_step()
         torch.cuda.synchronize()
@@ -379,7 +382,8 @@ def ours_arm(args, rank, world, local_rank):
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
         d2h = ho.numel() * ho.element_size() + hs.numel() * hs.element_size()
         e2e = {"value": wl.tokens * world / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": n_e2e}
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": n_e2e,
+               "api": f"gdn_frame_fwd_host, {args.e2e_chunk}-frame chunks, pinned host buffers"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -412,6 +416,7 @@ def main():
                     help="pass g and beta as logits (gdn_frame_fwd_from_logits)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-chunk", type=int, default=32, help="frames per chunk of the host-buffer entry point")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     args = ap.parse_args()

@@ -150,6 +150,39 @@ int gdn_frame_fwd_from_logits(const void* q, const void* k, const void* v,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gdn_frame_fwd_host -- the forward scan over inputs and outputs in HOST memory.
+ * (No counterpart on the pages: a streaming runtime around the scan.)
+ *   q, k, v, g, beta, state_in, out, state_out : host pointers with the layouts of
+ *       gdn_frame_fwd; page-locked (pinned) memory lets the copies overlap the
+ *       kernels, pageable memory works but serialises them.  state_in / state_out
+ *       may be NULL as in gdn_frame_fwd.
+ *   chunk_frames : frames per chunk (>= 1).  The frames are processed chunk by
+ *       chunk, the state carried from one chunk to the next on the device as in a
+ *       chunk-causal rollout (the bilibili SANA-WM article, second key point), so
+ *       the result equals gdn_frame_fwd's bit for bit.  The copies in of chunk
+ *       c + 1, the kernels of chunk c and the copies out of chunk c - 1 run at the
+ *       same time: the kernels on `stream`, the copies on two streams the call
+ *       creates and releases.
+ *   workspace : DEVICE memory of at least gdn_host_workspace_bytes() bytes,
+ *       256-byte aligned, owned by the caller: two chunk buffers of every tensor,
+ *       the carried state and one chunk call's scratch.
+ * Asynchronous like gdn_frame_fwd: the host buffers must stay valid and unchanged
+ * until `stream` reaches the end of the call (synchronise the stream before reading
+ * out / state_out).  Returns GDN_OK, GDN_ERR_INVALID_ARG (bad counts, NULL inputs,
+ * chunk_frames < 1), GDN_ERR_UNSUPPORTED (D), GDN_ERR_WORKSPACE, GDN_ERR_MISALIGNED
+ * (workspace) or GDN_ERR_CUDA.
+ */
+int gdn_frame_fwd_host(const void* q, const void* k, const void* v,
+                       const float* g, const float* beta, const float* state_in,
+                       void* out, float* state_out,
+                       int B, int H, int T, int S, int D, int dtype, int chunk_frames,
+                       void* workspace, size_t workspace_bytes, void* stream);
+
+/* gdn_host_workspace_bytes -- device workspace gdn_frame_fwd_host needs (0 for
+ * arguments it rejects). */
+size_t gdn_host_workspace_bytes(int B, int H, int T, int S, int D, int dtype, int chunk_frames);
+
+/*
  * gdn_last_error -- synchronises `stream`, then returns and clears the
  * device-side status word: GDN_OK, GDN_ERR_TIMEOUT (a kernel's bounded wait on
  * an mbarrier or a flag gave up; its results are invalid), or GDN_ERR_CUDA

@@ -30,6 +30,9 @@ _SIGS = {
     "gdn_frame_fwd_from_logits": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                                        ctypes.c_size_t, _P]),
     "gdn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
+    "gdn_frame_fwd_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_size_t,
+                                _P]),
+    "gdn_host_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
     "gdn_frame_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "gdn_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "gdn_last_error": (_I, [_P]),
@@ -81,6 +84,16 @@ def gdn_frame_fwd_from_logits(q, k, v, g_logit, beta_logit, state_in, out, state
                               workspace, workspace_bytes, stream) -> int:
     return lib().gdn_frame_fwd_from_logits(q, k, v, g_logit, beta_logit, state_in, out, state_out, B, H, T, S, D,
                                            dtype, mode, workspace, workspace_bytes, stream)
+
+
+def gdn_frame_fwd_host(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, chunk_frames,
+                       workspace, workspace_bytes, stream) -> int:
+    return lib().gdn_frame_fwd_host(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, chunk_frames,
+                                    workspace, workspace_bytes, stream)
+
+
+def gdn_host_workspace_bytes(B, H, T, S, D, dtype, chunk_frames) -> int:
+    return lib().gdn_host_workspace_bytes(B, H, T, S, D, dtype, chunk_frames)
 
 
 def gdn_frame_fwd_noalloc(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, stream) -> int:
@@ -182,4 +195,34 @@ def frame_fwd(q, k, v, g, beta, state_in=None, out=None, state_out=None, mode=No
         rc = fn(*args, mode, _ptr(workspace), wbytes, st)
     if rc != 0:
         raise GDNError(rc, "gdn_frame_fwd")
+    return out, state_out
+
+
+def frame_fwd_host(q, k, v, g, beta, state_in=None, chunk_frames=32, workspace=None, stream=None, out=None,
+                   state_out=None):
+    """gdn_frame_fwd_host on torch CPU tensors (pinned for overlap): q, k, v
+    [B,H,T,S,D] float32 or bfloat16, g [B,H,T], beta [B,H,T,S], state_in [B,H,D,D]
+    or None.  ``workspace`` is a uint8 CUDA tensor (allocated if None).  Waits for
+    the stream and returns (out, state_out) as CPU tensors."""
+    import torch
+
+    B, H, T, S, D = q.shape
+    dtype = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}[q.dtype]
+    for t in (q, k, v, g, beta) + (() if state_in is None else (state_in,)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("gdn_frame_fwd_host takes contiguous host tensors")
+    if out is None:
+        out = torch.empty(tuple(q.shape), dtype=q.dtype, pin_memory=q.is_pinned())
+    if state_out is None:
+        state_out = torch.empty((B, H, D, D), dtype=torch.float32, pin_memory=q.is_pinned())
+    need = gdn_host_workspace_bytes(B, H, T, S, D, dtype, chunk_frames)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device="cuda")
+    strm = stream if stream is not None else torch.cuda.current_stream()
+    rc = gdn_frame_fwd_host(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(out),
+                            _ptr(state_out), B, H, T, S, D, dtype, chunk_frames, _ptr(workspace),
+                            workspace.numel(), strm.cuda_stream)
+    if rc != 0:
+        raise GDNError(rc, "gdn_frame_fwd_host")
+    strm.synchronize()
     return out, state_out

@@ -136,6 +136,14 @@ int forward_ex(const void* q, const void* k, const void* v, const float* g, cons
 
 }  // namespace
 
+int check_args(const void* q, const void* k, const void* v, const float* g, const float* beta,
+               const float* state_in, void* out, float* state_out, int B, int H, int T, int S, int D, int dtype,
+               int mode, Problem* p) {
+  return validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode, p);
+}
+size_t scratch_bytes(const Problem& p) { return workspace_for(p); }
+int run_forward(const Problem& p, void* ws, cudaStream_t st) { return forward(p, ws, st); }
+
 ProfScope::ProfScope(cudaStream_t st, const char* name) : st_(st), idx_(-1) {
   std::lock_guard<std::mutex> lock(g_prof_mu);
   if (!g_prof_on) return;

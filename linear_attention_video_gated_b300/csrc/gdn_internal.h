@@ -57,6 +57,16 @@ __device__ __forceinline__ void report_device_error(unsigned int* status, unsign
   atomicCAS(status, 0u, code);
 }
 
+// ---- argument checks and dispatch (gdn_api.cu), for the other C-ABI files -------
+// Validates the arguments of a forward call and fills `p` (returns a Status).
+int check_args(const void* q, const void* k, const void* v, const float* g, const float* beta,
+               const float* state_in, void* out, float* state_out, int B, int H, int T, int S, int D, int dtype,
+               int mode, Problem* p);
+// Scratch bytes the call `p` needs.
+size_t scratch_bytes(const Problem& p);
+// Enqueues the call on `st` (scratch `ws` of scratch_bytes(p) bytes).
+int run_forward(const Problem& p, void* ws, cudaStream_t st);
+
 // ---- SIMT path (float32 arithmetic; used for float32 I/O) --------------------
 size_t simt_workspace_bytes(const Problem& p, int mode);
 int simt_forward(const Problem& p, void* ws, cudaStream_t st);

@@ -104,3 +104,28 @@ def test_no_gpu_call_fails_loudly_not_silently(lib):
         pytest.skip("GPU present")
     # with no device, a valid-looking call must report a CUDA error, never succeed
     assert binding.gdn_last_error(None) == 4
+
+
+def _host(B=1, H=2, T=3, S=17, D=32, dtype=1, chunk=2, ptr=A16, ws=A16, wsb=1 << 40):
+    return binding.gdn_frame_fwd_host(ptr, ptr, ptr, ptr, ptr, None, ptr, None, B, H, T, S, D, dtype, chunk, ws, wsb,
+                                      None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(chunk=0), 1), (dict(chunk=-3), 1), (dict(B=0), 1), (dict(T=-1), 1), (dict(dtype=7), 1),
+    (dict(D=24), 2), (dict(D=144), 2), (dict(ptr=None), 1),
+    (dict(ws=None), 6), (dict(wsb=16), 6), (dict(ws=A16 + 16), 3),
+])
+def test_host_entry_validation_rejects(lib, kw, code):
+    assert _host(**kw) == code
+
+
+def test_host_workspace_bytes(lib):
+    a = binding.gdn_host_workspace_bytes(1, 20, 961, 880, 112, 1, 32)
+    assert a > 0 and a == binding.gdn_host_workspace_bytes(1, 20, 961, 880, 112, 1, 32)
+    # two chunk buffers of q, k, v, out dominate: grows with the chunk, capped by T
+    assert binding.gdn_host_workspace_bytes(1, 20, 961, 880, 112, 1, 64) > a
+    assert binding.gdn_host_workspace_bytes(1, 20, 10, 880, 112, 1, 64) == \
+        binding.gdn_host_workspace_bytes(1, 20, 10, 880, 112, 1, 10)
+    assert binding.gdn_host_workspace_bytes(1, 20, 961, 880, 112, 1, 0) == 0
+    assert binding.gdn_host_workspace_bytes(1, 20, 961, 880, 24, 1, 32) == 0
