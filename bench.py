@@ -261,6 +261,8 @@ def ours_arm(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     wl = synth.WORKLOADS[args.workload]
+    if args.frames:
+        wl = wl.with_(T=min(args.frames, wl.T))
     mode = args.mode
     dtype = binding.GDN_BF16 if wl.dtype == "bf16" else binding.GDN_F32
     tdt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
@@ -412,6 +414,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="minute", choices=sorted(synth.WORKLOADS))
     ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3])
+    ap.add_argument("--frames", type=int, default=None,
+                    help="run the workload's first N frames only (small cases for profiling)")
     ap.add_argument("--gate-logits", action="store_true",
                     help="pass g and beta as logits (gdn_frame_fwd_from_logits)")
     ap.add_argument("--no-e2e", action="store_true")
