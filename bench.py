@@ -222,8 +222,10 @@ def _fill_head(wl, b, h, hq, hk, hv, hg, hb):
 
 # ----------------------------------------------------------------- arms
 
-def config_of(wl, mode, gate_logits=False) -> dict:
+def config_of(wl, mode, gate_logits=False, relu_linear=False) -> dict:
     gates = ", gates from logits (fused gate prologue)" if gate_logits else ""
+    if relu_linear:
+        gates = ", cumulative ReLU linear attention baseline (no decay, no delta rule)"
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} T={wl.T} S={wl.S} D={wl.D} {wl.dtype} I/O, fp32 state, "
                         f"single call over all frames{gates}",
             "B": wl.B, "H": wl.H, "T": wl.T, "S": wl.S, "D": wl.D,
@@ -288,9 +290,14 @@ def ours_arm(args, rank, world, local_rank):
     entry = binding.gdn_frame_fwd_from_logits if args.gate_logits else binding.gdn_frame_fwd_ex
 
     def step(qq=q, kk=k, vv=v, gg=g, bb=beta, oo=out, so=st_out):
-        rc = entry(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), gg.data_ptr(), bb.data_ptr(),
-                   None, oo.data_ptr(), so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype,
-                   mode, ws.data_ptr(), need, sp)
+        if args.relu_linear:
+            rc = binding.gdn_relu_linear_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), None, oo.data_ptr(),
+                                             so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype, mode,
+                                             ws.data_ptr(), need, sp)
+        else:
+            rc = entry(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), gg.data_ptr(), bb.data_ptr(),
+                       None, oo.data_ptr(), so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype,
+                       mode, ws.data_ptr(), need, sp)
         if rc != 0:
             raise binding.GDNError(rc, "gdn_frame_fwd_ex")
 
@@ -353,7 +360,7 @@ def ours_arm(args, rank, world, local_rank):
     # end to end through the C ABI from pinned host buffers: gdn_frame_fwd_host,
     # which overlaps the copies of one chunk of frames with the kernels of another
     e2e = None
-    if not args.no_e2e and not args.gate_logits:
+    if not args.no_e2e and not args.gate_logits and not args.relu_linear:
         ho = torch.empty(shape, dtype=tdt, pin_memory=True)
         hs = torch.empty((wl.B, wl.H, wl.D, wl.D), dtype=torch.float32, pin_memory=True)
         n_e2e = max(2, min(args.steps, args.e2e_steps))
@@ -396,7 +403,7 @@ def ours_arm(args, rank, world, local_rank):
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                 "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-                "config": config_of(wl, mode, args.gate_logits),
+                "config": config_of(wl, mode, args.gate_logits, args.relu_linear),
                 "roofline_pct": 100.0 * call_gbs / pk["hbm_gbs"],
                 "call_achieved_gbs": call_gbs,
                 "tflops": alg_flops(wl) / (ms / 1e3) / 1e12,
@@ -418,6 +425,8 @@ def main():
                     help="run the workload's first N frames only (small cases for profiling)")
     ap.add_argument("--gate-logits", action="store_true",
                     help="pass g and beta as logits (gdn_frame_fwd_from_logits)")
+    ap.add_argument("--relu-linear", action="store_true",
+                    help="time the cumulative ReLU linear attention baseline (gdn_relu_linear_fwd)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-chunk", type=int, default=32, help="frames per chunk of the host-buffer entry point")

@@ -150,6 +150,23 @@ int gdn_frame_fwd_from_logits(const void* q, const void* k, const void* v,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gdn_relu_linear_fwd -- the baseline the pages contrast GDN with: SANA-Video's
+ * cumulative ReLU-based linear attention (zhichai.net summary, section 1, the
+ * paragraph on SANA-Video; bilibili article, third key point), run through the
+ * same kernels.  Per head, with no decay, no delta-rule correction and no gates:
+ *     S_t = S_{t-1} + relu(K_t)^T V_t / sqrt(D*S),   O_t = relu(Q_t) S_t / sqrt(D).
+ * (The pages give no formula; this is the plainest reading with the GDN scan's
+ * own scalings, so the two differ only in the decay, the delta rule and the
+ * feature map.)  Arguments, layouts, workspace (gdn_workspace_bytes with the same
+ * mode) and errors as gdn_frame_fwd_ex without g and beta; GDN_MODE_CLUSTER is not
+ * offered (GDN_ERR_UNSUPPORTED).
+ */
+int gdn_relu_linear_fwd(const void* q, const void* k, const void* v, const float* state_in,
+                        void* out, float* state_out,
+                        int B, int H, int T, int S, int D, int dtype, int mode,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * gdn_frame_fwd_host -- the forward scan over inputs and outputs in HOST memory.
  * (No counterpart on the pages: a streaming runtime around the scan.)
  *   q, k, v, g, beta, state_in, out, state_out : host pointers with the layouts of
@@ -189,6 +206,18 @@ size_t gdn_host_workspace_bytes(int B, int H, int T, int S, int D, int dtype, in
  * (the stream reported an error).
  */
 int gdn_last_error(void* stream);
+
+/*
+ * gdn_selftest_wait_timeout -- exercises the library's failure detection without
+ * a fault (no counterpart on the pages).  Enqueues on `stream` one kernel whose
+ * thread waits, with the bounded wait every kernel here uses, on a barrier that
+ * nothing arrives on; after timeout_us microseconds (1 .. 10,000,000) it gives
+ * up, records GDN_ERR_TIMEOUT in the device status word and returns normally.
+ * The next gdn_last_error(stream) then reports GDN_ERR_TIMEOUT (and clears it),
+ * and the context stays usable.  Returns GDN_OK, GDN_ERR_INVALID_ARG (timeout out
+ * of range) or GDN_ERR_CUDA.
+ */
+int gdn_selftest_wait_timeout(unsigned int timeout_us, void* stream);
 
 /* gdn_status_string -- a static, human-readable name for a status code. */
 const char* gdn_status_string(int status);

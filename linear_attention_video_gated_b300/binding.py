@@ -30,12 +30,14 @@ _SIGS = {
     "gdn_frame_fwd_from_logits": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P,
                                        ctypes.c_size_t, _P]),
     "gdn_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
+    "gdn_relu_linear_fwd": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
     "gdn_frame_fwd_host": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_size_t,
                                 _P]),
     "gdn_host_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
     "gdn_frame_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "gdn_noalloc_scratch_bytes": (ctypes.c_size_t, []),
     "gdn_last_error": (_I, [_P]),
+    "gdn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "gdn_status_string": (ctypes.c_char_p, [_I]),
     "gdn_version": (_I, []),
     "gdn_profile_begin": (_I, []),
@@ -96,6 +98,12 @@ def gdn_host_workspace_bytes(B, H, T, S, D, dtype, chunk_frames) -> int:
     return lib().gdn_host_workspace_bytes(B, H, T, S, D, dtype, chunk_frames)
 
 
+def gdn_relu_linear_fwd(q, k, v, state_in, out, state_out, B, H, T, S, D, dtype, mode, workspace, workspace_bytes,
+                        stream) -> int:
+    return lib().gdn_relu_linear_fwd(q, k, v, state_in, out, state_out, B, H, T, S, D, dtype, mode, workspace,
+                                     workspace_bytes, stream)
+
+
 def gdn_frame_fwd_noalloc(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, stream) -> int:
     return lib().gdn_frame_fwd_noalloc(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, stream)
 
@@ -110,6 +118,10 @@ def gdn_workspace_bytes(B, H, T, S, D, dtype, mode) -> int:
 
 def gdn_last_error(stream) -> int:
     return lib().gdn_last_error(stream)
+
+
+def gdn_selftest_wait_timeout(timeout_us, stream) -> int:
+    return lib().gdn_selftest_wait_timeout(timeout_us, stream)
 
 
 def gdn_status_string(status: int) -> str:
@@ -225,4 +237,24 @@ def frame_fwd_host(q, k, v, g, beta, state_in=None, chunk_frames=32, workspace=N
     if rc != 0:
         raise GDNError(rc, "gdn_frame_fwd_host")
     strm.synchronize()
+    return out, state_out
+
+
+def relu_linear_fwd(q, k, v, state_in=None, mode=GDN_MODE_SEQUENTIAL, workspace=None, stream=None):
+    """gdn_relu_linear_fwd on torch CUDA tensors (layouts as frame_fwd).  Returns (out, state_out)."""
+    import torch
+
+    B, H, T, S, D = q.shape
+    dtype = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}[q.dtype]
+    out = torch.empty_like(q)
+    state_out = torch.empty((B, H, D, D), dtype=torch.float32, device=q.device)
+    need = gdn_workspace_bytes(B, H, T, S, D, dtype, mode)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    strm = stream if stream is not None else torch.cuda.current_stream(q.device)
+    rc = gdn_relu_linear_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(state_in), _ptr(out), _ptr(state_out), B, H, T, S, D,
+                             dtype, mode, _ptr(workspace), 0 if workspace is None else workspace.numel(),
+                             strm.cuda_stream)
+    if rc != 0:
+        raise GDNError(rc, "gdn_relu_linear_fwd")
     return out, state_out

@@ -33,7 +33,7 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // Validates everything that can be checked on the host.  Fills `p`.
 int validate(const void* q, const void* k, const void* v, const float* g, const float* beta,
              const float* state_in, void* out, float* state_out, int B, int H, int T, int S, int D, int dtype,
-             int mode, Problem* p) {
+             int mode, Problem* p, bool need_gates = true) {
   if (B < 1 || H < 1 || T < 0 || S < 1 || D < 1) return kInvalidArg;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return kInvalidArg;
   if (mode < GDN_MODE_SEQUENTIAL || mode > GDN_MODE_CLUSTER) return kInvalidArg;
@@ -45,7 +45,8 @@ int validate(const void* q, const void* k, const void* v, const float* g, const 
   if ((long long)B * H > (1LL << 31) - 1 || bht > (1LL << 31) - 1) return kInvalidArg;
   if ((long long)S * D > (1LL << 31) - 1) return kInvalidArg;
   if (T > 0) {
-    if (!q || !k || !v || !g || !beta || !out) return kInvalidArg;
+    if (!q || !k || !v || !out) return kInvalidArg;
+    if (need_gates && (!g || !beta)) return kInvalidArg;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16)) return kMisaligned;
     if (!aligned(g, 4) || !aligned(beta, 4)) return kMisaligned;
   }
@@ -138,10 +139,11 @@ int forward_ex(const void* q, const void* k, const void* v, const float* g, cons
 
 int check_args(const void* q, const void* k, const void* v, const float* g, const float* beta,
                const float* state_in, void* out, float* state_out, int B, int H, int T, int S, int D, int dtype,
-               int mode, Problem* p) {
-  return validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode, p);
+               int mode, Problem* p, bool need_gates) {
+  return validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode, p, need_gates);
 }
 size_t scratch_bytes(const Problem& p) { return workspace_for(p); }
+unsigned int* device_status_word() { return status_word(); }
 int run_forward(const Problem& p, void* ws, cudaStream_t st) { return forward(p, ws, st); }
 
 ProfScope::ProfScope(cudaStream_t st, const char* name) : st_(st), idx_(-1) {
@@ -171,6 +173,22 @@ int gdn_frame_fwd_ex(const void* q, const void* k, const void* v, const float* g
                      int dtype, int mode, void* workspace, size_t workspace_bytes, void* stream) {
   return gdn::forward_ex(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode, workspace,
                          workspace_bytes, stream, 0);
+}
+
+int gdn_relu_linear_fwd(const void* q, const void* k, const void* v, const float* state_in, void* out,
+                        float* state_out, int B, int H, int T, int S, int D, int dtype, int mode, void* workspace,
+                        size_t workspace_bytes, void* stream) {
+  if (mode == GDN_MODE_CLUSTER) return GDN_ERR_UNSUPPORTED;
+  Problem p{};
+  int rc = validate(q, k, v, nullptr, nullptr, state_in, out, state_out, B, H, T, S, D, dtype, mode, &p, false);
+  if (rc != kOk) return rc;
+  p.variant = kReluLinear;
+  const size_t need = workspace_for(p);
+  if (need > 0) {
+    if (!workspace || workspace_bytes < need) return kWorkspace;
+    if (!aligned(workspace, 256)) return kMisaligned;
+  }
+  return forward(p, workspace, static_cast<cudaStream_t>(stream));
 }
 
 int gdn_frame_fwd_from_logits(const void* q, const void* k, const void* v, const float* g_logit,

@@ -33,6 +33,7 @@ struct Problem {
   int dtype;  // gdn_dtype_t
   int mode;   // gdn_mode_t
   int gate_logits;  // 1: g and beta hold raw logits, mapped by decay_of / beta_of where loaded
+  int variant;      // kGdn, or kReluLinear: the cumulative ReLU linear attention baseline
   float key_scale;  // 1/sqrt(D*S)
   float out_scale;  // 1/sqrt(D)
   unsigned int* status;  // device-side status word (first error wins)
@@ -52,6 +53,14 @@ enum Status {
 __device__ __forceinline__ float decay_of(float x, int logits) { return logits ? 1.f / (1.f + expf(x)) : x; }
 __device__ __forceinline__ float beta_of(float x, int logits) { return logits ? 1.f / (1.f + expf(-x)) : x; }
 
+// Recurrence computed by the kernels.  kReluLinear is the SANA-Video baseline the
+// pages contrast GDN with (cumulative ReLU-based linear attention): no decay
+// (g = 1), no delta-rule correction (the M_t term dropped, beta = 1), ReLU
+// applied to queries and keys:  S_t = S_{t-1} + relu(K_t)~^T V_t,
+// O_t = relu(Q_t) S_t / sqrt(D), with the same 1/sqrt(D*S) key scale.
+enum Variant { kGdn = 0, kReluLinear = 1 };
+__device__ __forceinline__ float relu_if(float x, int variant) { return variant == kReluLinear ? fmaxf(x, 0.f) : x; }
+
 // Records a device-side error in the status word; the first error wins.
 __device__ __forceinline__ void report_device_error(unsigned int* status, unsigned int code) {
   atomicCAS(status, 0u, code);
@@ -61,11 +70,13 @@ __device__ __forceinline__ void report_device_error(unsigned int* status, unsign
 // Validates the arguments of a forward call and fills `p` (returns a Status).
 int check_args(const void* q, const void* k, const void* v, const float* g, const float* beta,
                const float* state_in, void* out, float* state_out, int B, int H, int T, int S, int D, int dtype,
-               int mode, Problem* p);
+               int mode, Problem* p, bool need_gates = true);
 // Scratch bytes the call `p` needs.
 size_t scratch_bytes(const Problem& p);
 // Enqueues the call on `st` (scratch `ws` of scratch_bytes(p) bytes).
 int run_forward(const Problem& p, void* ws, cudaStream_t st);
+// Device address of the status word on the current device (nullptr on failure).
+unsigned int* device_status_word();
 
 // ---- SIMT path (float32 arithmetic; used for float32 I/O) --------------------
 size_t simt_workspace_bytes(const Problem& p, int mode);

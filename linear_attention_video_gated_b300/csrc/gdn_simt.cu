@@ -36,7 +36,8 @@ __device__ __forceinline__ void from_f32(__nv_bfloat16& d, float x) { d = __floa
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads) gram_kernel(const TIn* __restrict__ k, const TIn* __restrict__ v,
                                                         const float* __restrict__ beta, float* __restrict__ Mws,
-                                                        float* __restrict__ bws, int S, int D, float ck, int logits) {
+                                                        float* __restrict__ bws, int S, int D, float ck, int logits,
+                                                        int variant) {
   extern __shared__ float smem[];
   float* sA = smem;             // [kTok][D]  beta * k
   float* sX = smem + kTok * D;  // [kTok][D]  k or v
@@ -60,7 +61,8 @@ __global__ void __launch_bounds__(kThreads) gram_kernel(const TIn* __restrict__ 
       float a = 0.f, x = 0.f;
       if (s < n) {
         const long long o = (long long)(s0 + s) * D + (idx % D);
-        a = beta_of(bf[s0 + s], logits) * to_f32(kf[o]);
+        const float bt = variant == kReluLinear ? 1.f : beta_of(bf[s0 + s], logits);
+        a = bt * relu_if(to_f32(kf[o]), variant);
         x = to_f32(xf[o]);
       }
       sA[idx] = a;
@@ -155,7 +157,7 @@ __device__ void affine_step(float* sX, const float* sM, const float* __restrict_
 __global__ void __launch_bounds__(kThreads) scan_kernel(const float* __restrict__ Mws, const float* __restrict__ bws,
                                                         const float* __restrict__ g, const float* state_in,
                                                         float* __restrict__ Sws, float* state_out, int T, int D,
-                                                        int logits) {
+                                                        int logits, int variant) {
   extern __shared__ float smem[];
   float* sS = smem;          // [D][D]
   float* sM = smem + D * D;  // [D][D]
@@ -165,9 +167,10 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const float* __restrict_
   __syncthreads();
   for (int t = 0; t < T; ++t) {
     const long long f = bh * T + t;
-    for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) sM[idx] = Mws[f * D * D + idx];
+    for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x)
+      sM[idx] = variant == kReluLinear ? 0.f : Mws[f * D * D + idx];
     __syncthreads();
-    affine_step(sS, sM, bws + f * D * D, decay_of(g[f], logits), D, D, 0, Sws + f * D * D);
+    affine_step(sS, sM, bws + f * D * D, (variant == kReluLinear ? 1.f : decay_of(g[f], logits)), D, D, 0, Sws + f * D * D);
   }
   if (state_out)
     for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) state_out[bh * D * D + idx] = sS[idx];
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(kThreads) scan_kernel(const float* __restrict_
 // starting from [I | 0].  One CTA per (head, chunk).
 __global__ void __launch_bounds__(kThreads) compose_kernel(const float* __restrict__ Mws, const float* __restrict__ bws,
                                                            const float* __restrict__ g, float* __restrict__ maps,
-                                                           int T, int D, int nchunks, int logits) {
+                                                           int T, int D, int nchunks, int logits, int variant) {
   extern __shared__ float smem[];
   float* sX = smem;              // [D][2D]
   float* sM = smem + 2 * D * D;  // [D][D]
@@ -191,9 +194,10 @@ __global__ void __launch_bounds__(kThreads) compose_kernel(const float* __restri
   __syncthreads();
   for (int t = t0; t < t1; ++t) {
     const long long f = bh * T + t;
-    for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) sM[idx] = Mws[f * D * D + idx];
+    for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x)
+      sM[idx] = variant == kReluLinear ? 0.f : Mws[f * D * D + idx];
     __syncthreads();
-    affine_step(sX, sM, bws + f * D * D, decay_of(g[f], logits), D, 2 * D, D, nullptr);
+    affine_step(sX, sM, bws + f * D * D, (variant == kReluLinear ? 1.f : decay_of(g[f], logits)), D, 2 * D, D, nullptr);
   }
   float* dst = maps + (bh * nchunks + c) * 2 * D * D;
   for (int idx = threadIdx.x; idx < 2 * D * D; idx += blockDim.x) dst[idx] = sX[idx];
@@ -262,7 +266,7 @@ __global__ void __launch_bounds__(kThreads) boundary_kernel(const float* __restr
 __global__ void __launch_bounds__(kThreads) replay_kernel(const float* __restrict__ Mws, const float* __restrict__ bws,
                                                           const float* __restrict__ g, const float* __restrict__ starts,
                                                           float* __restrict__ Sws, int T, int D, int nchunks,
-                                                          int logits) {
+                                                          int logits, int variant) {
   extern __shared__ float smem[];
   float* sS = smem;
   float* sM = smem + D * D;
@@ -274,16 +278,17 @@ __global__ void __launch_bounds__(kThreads) replay_kernel(const float* __restric
   __syncthreads();
   for (int t = t0; t < t1; ++t) {
     const long long f = bh * T + t;
-    for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) sM[idx] = Mws[f * D * D + idx];
+    for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x)
+      sM[idx] = variant == kReluLinear ? 0.f : Mws[f * D * D + idx];
     __syncthreads();
-    affine_step(sS, sM, bws + f * D * D, decay_of(g[f], logits), D, D, 0, Sws + f * D * D);
+    affine_step(sS, sM, bws + f * D * D, (variant == kReluLinear ? 1.f : decay_of(g[f], logits)), D, D, 0, Sws + f * D * D);
   }
 }
 
 // O_t = Q_t S_t * co for a tile of kOutRows tokens.  grid = (frame-heads, token tiles).
 template <typename TIn>
 __global__ void __launch_bounds__(kThreads) readout_kernel(const TIn* __restrict__ q, const float* __restrict__ Sws,
-                                                           TIn* __restrict__ out, int S, int D, float co) {
+                                                           TIn* __restrict__ out, int S, int D, float co, int variant) {
   extern __shared__ float smem[];
   float* sS = smem;          // [D][D]
   float* sQ = smem + D * D;  // [kOutRows][D]
@@ -293,7 +298,7 @@ __global__ void __launch_bounds__(kThreads) readout_kernel(const TIn* __restrict
   for (int idx = threadIdx.x; idx < D * D; idx += blockDim.x) sS[idx] = Sws[f * D * D + idx];
   for (int idx = threadIdx.x; idx < kOutRows * D; idx += blockDim.x) {
     const int s = idx / D;
-    sQ[idx] = s < n ? to_f32(q[(f * S + s0 + s) * D + idx % D]) : 0.f;
+    sQ[idx] = s < n ? relu_if(to_f32(q[(f * S + s0 + s) * D + idx % D]), variant) : 0.f;
   }
   __syncthreads();
   const int ntj = D / 4;
@@ -361,7 +366,7 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
     ProfScope pg(st, "simt_gram");
     gram_kernel<TIn><<<dim3((unsigned)p.BHT(), 2), kThreads, gram_smem, st>>>(
         static_cast<const TIn*>(p.k), static_cast<const TIn*>(p.v), p.beta, Mws, bws, p.S, D, p.key_scale,
-        p.gate_logits);
+        p.gate_logits, p.variant);
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
 
@@ -372,7 +377,7 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
     {
       ProfScope ps(st, "simt_scan");
       scan_kernel<<<(unsigned)p.BH(), kThreads, smem, st>>>(Mws, bws, p.g, p.state_in, Sws, p.state_out, p.T, D,
-                                                             p.gate_logits);
+                                                             p.gate_logits, p.variant);
     }
     if (cudaGetLastError() != cudaSuccess) return kCuda;
   } else {
@@ -384,7 +389,7 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
     {
       ProfScope pc(st, "simt_compose");
       compose_kernel<<<(unsigned)(p.BH() * L.nchunks), kThreads, csmem, st>>>(Mws, bws, p.g, maps, p.T, D, L.nchunks,
-                                                                               p.gate_logits);
+                                                                               p.gate_logits, p.variant);
     }
     if (cudaGetLastError() != cudaSuccess) return kCuda;
     if (cudaFuncSetAttribute(boundary_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem) !=
@@ -401,7 +406,7 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
     {
       ProfScope pr(st, "simt_replay");
       replay_kernel<<<(unsigned)(p.BH() * L.nchunks), kThreads, rsmem, st>>>(Mws, bws, p.g, starts, Sws, p.T, D,
-                                                                            L.nchunks, p.gate_logits);
+                                                                            L.nchunks, p.gate_logits, p.variant);
     }
     if (cudaGetLastError() != cudaSuccess) return kCuda;
   }
@@ -413,7 +418,7 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
   {
     ProfScope po(st, "simt_readout");
     readout_kernel<TIn><<<dim3((unsigned)p.BHT(), (p.S + kOutRows - 1) / kOutRows), kThreads, osmem, st>>>(
-        static_cast<const TIn*>(p.q), Sws, static_cast<TIn*>(p.out), p.S, D, p.out_scale);
+        static_cast<const TIn*>(p.q), Sws, static_cast<TIn*>(p.out), p.S, D, p.out_scale, p.variant);
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   return kOk;

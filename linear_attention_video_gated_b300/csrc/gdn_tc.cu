@@ -39,7 +39,7 @@ constexpr int kGramThreads = 448;              // 4 epilogue, 8 convert, 1 TMA, 
 constexpr int kOutTok = 128;                   // tokens per read-out tile (MMA M)
 constexpr int kOutQStages = 2;
 constexpr int kOutAcc = 4;                     // TMEM accumulators in flight
-constexpr int kOutThreads = 192;               // 4 epilogue, 1 TMA, 1 MMA warps
+constexpr int kOutThreads = 320;               // 4 epilogue, 1 TMA, 1 MMA, 4 query-prep warps
 
 __host__ __device__ inline int num_atoms(int D) { return (D + 63) / 64; }
 
@@ -181,6 +181,7 @@ constexpr int kConvStage = 4 * kGramRegion;  // AH atoms (2) then AL atoms (2): 
 struct GramArgs {
   const float* beta;
   int gate_logits;
+  int variant;
   uint8_t* m_img;  // F x NA x D rows x 128 B
   float* b_blk;    // F x (D/16) x D x 16
   long long nitems;
@@ -316,13 +317,16 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     auto beta_at = [&](long long f, int c, int rw) {
       const int s = c * kGramTok + rw;
       // raw value, mapped when used: mapping here would wait for the load
-      return (f < a.nitems && s < S) ? __ldg(a.beta + f * S + s) : -INFINITY;
+      if (!(f < a.nitems && s < S)) return -INFINITY;
+      return a.variant == kReluLinear ? 1.f : __ldg(a.beta + f * S + s);
     };
     long long fn = blockIdx.x;
     int cn = 0;
     // beta of token rows r0 and r0 + 32: raw values loaded one tile ahead, mapped
     // (rows past S, loaded as -inf, give 0) after the current tile is converted.
-    auto mapped = [&](float x) { return x == -INFINITY ? 0.f : beta_of(x, a.gate_logits); };
+    auto mapped = [&](float x) {
+      return x == -INFINITY ? 0.f : (a.variant == kReluLinear ? x : beta_of(x, a.gate_logits));
+    };
     float bn0 = beta_at(fn, 0, r0), bn1 = beta_at(fn, 0, r0 + 32);
     float b0 = mapped(bn0), b1 = mapped(bn1);
     for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
@@ -343,7 +347,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-            split2(bs * x.x, bs * x.y, hi[e], lo[e]);
+            split2(bs * relu_if(x.x, a.variant), bs * relu_if(x.y, a.variant), hi[e], lo[e]);
           }
           *reinterpret_cast<uint4*>(ah + u * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(ah + 2 * kGramRegion + u * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
@@ -446,6 +450,7 @@ struct ScanArgs {
   const float* b_blk;
   const float* g;
   int gate_logits;
+  int variant;
   const float* state_in;
   uint8_t* s_img;
   float* state_out;
@@ -597,11 +602,12 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     if (lane == 0) mbar_arrive(smem_u32(sready));
     int stage = 0;
     uint32_t phase = 0;
-    float gnext = T > 0 ? __ldg(a.g + bh * T) : 0.f;  // raw; mapped when used
+    const bool relu_lin = a.variant == kReluLinear;  // g = 1, no delta-rule term
+    float gnext = (T > 0 && !relu_lin) ? __ldg(a.g + bh * T) : 0.f;  // raw; mapped when used
     for (int t = 0; t < T; ++t) {
       const long long f = bh * T + t;
-      const float gt = decay_of(gnext, a.gate_logits);
-      if (t + 1 < T) gnext = __ldg(a.g + f + 1);
+      const float gt = relu_lin ? 1.f : decay_of(gnext, a.gate_logits);
+      if (t + 1 < T && !relu_lin) gnext = __ldg(a.g + f + 1);
       const bool ok = wait_or_abort(smem_u32(pfull), t & 1, abort_flag, a.status) &&
                       wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
       if (__all_sync(0xffffffffu, ok)) {
@@ -627,7 +633,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
         if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
         if (row) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] = fmaf(gt, x[j] - (p[j] + pl[j]), bv[j]);
+          for (int j = 0; j < 16; ++j) x[j] = relu_lin ? x[j] + bv[j] : fmaf(gt, x[j] - (p[j] + pl[j]), bv[j]);
         }
         // S_t goes into the buffer of S_{t-2}, whose store has read it (the MMA
         // thread waited for that before committing pfull(t)).
@@ -672,6 +678,7 @@ done:
 // =============================================================================
 struct OutArgs {
   const uint8_t* s_img;
+  int variant;  // kReluLinear: relu(Q) is applied to each Q tile in shared memory
   __nv_bfloat16* out;
   long long nitems;
   int S, D, NA;
@@ -698,8 +705,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
   uint64_t* accfull = qempty + kOutQStages;
   uint64_t* accempty = accfull + kOutAcc;
   uint64_t* mma_done = accempty + kOutAcc;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  uint64_t* qready = mma_done + 1;  // kReluLinear: the tile's relu(Q) is in place
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(qready + kOutQStages);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const bool relu_q = a.variant == kReluLinear;
 
   const int warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -710,6 +719,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     for (int s = 0; s < kOutQStages; ++s) {
       mbar_init(smem_u32(&qfull[s]), 1);
       mbar_init(smem_u32(&qempty[s]), 1);
+      mbar_init(smem_u32(&qready[s]), 4);
     }
     for (int b = 0; b < kOutAcc; ++b) {
       mbar_init(smem_u32(&accfull[b]), 1);
@@ -777,7 +787,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         const uint32_t im = smem_u32(imgs + ab * img_stride);
         for (int tile = 0; tile < ntiles; ++tile) {
           if (!wait_or_abort(smem_u32(&accempty[cb]), cph ^ 1, abort_flag, a.status)) goto done;
-          if (!wait_or_abort(smem_u32(&qfull[qs]), qph, abort_flag, a.status)) goto done;
+          if (!wait_or_abort(smem_u32(relu_q ? &qready[qs] : &qfull[qs]), qph, abort_flag, a.status)) goto done;
           tc_fence_after();
           const uint32_t qb = smem_u32(qst + qs * q_bytes);
           const uint32_t acc = tmem + cb * 128;
@@ -795,6 +805,31 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         }
         mma_commit(smem_u32(&aempty[ab]));
         if (++ab == 2) { ab = 0; aph ^= 1; }
+      }
+    }
+  } else if (warp >= 6) {
+    // ---------------- query prep (kReluLinear only): relu(Q) in place, tile by tile
+    if (relu_q) {
+      const int pt = threadIdx.x - 192;  // 0 .. 127
+      int qs = 0;
+      uint32_t qph = 0;
+      const __nv_bfloat162 zero = __floats2bfloat162_rn(0.f, 0.f);
+      for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+        for (int tile = 0; tile < ntiles; ++tile) {
+          if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&qfull[qs]), qph, abort_flag, a.status))) goto done;
+          uint4* qt = reinterpret_cast<uint4*>(qst + qs * q_bytes);
+          for (int idx = pt; idx < q_bytes / 16; idx += 128) {
+            uint4 w = qt[idx];
+            __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) h[e] = __hmax2(h[e], zero);
+            qt[idx] = w;
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&qready[qs]));
+          if (++qs == kOutQStages) { qs = 0; qph ^= 1; }
+        }
       }
     }
   } else {
@@ -911,8 +946,8 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
     const int smem = gram_smem(NA, p.D);
     if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
-    GramArgs ga{p.beta, p.gate_logits, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale, p.key_scale,
-                p.status};
+    GramArgs ga{p.beta, p.gate_logits, p.variant, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale,
+                p.key_scale, p.status};
     const unsigned grid = (unsigned)(F < nsm ? F : nsm);
     ProfScope ps(st, "tc_gram");
     tc_gram_kernel<<<grid, kGramThreads, smem, st>>>(mapK, mapV, ga);
@@ -922,7 +957,7 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
     const int smem = scan_smem();
     if (cudaFuncSetAttribute(tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
-    ScanArgs sa{m_img, b_mat, p.g, p.gate_logits, p.state_in, s_img, p.state_out, p.T, p.D, NA, p.status};
+    ScanArgs sa{m_img, b_mat, p.g, p.gate_logits, p.variant, p.state_in, s_img, p.state_out, p.T, p.D, NA, p.status};
     ProfScope ps(st, "tc_scan");
     tc_scan_kernel<<<(unsigned)(p.BH() * (p.D / 16)), kScanThreads, smem, st>>>(sa);
   }
@@ -931,7 +966,7 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
     const int smem = out_smem(NA, p.D);
     if (cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
-    OutArgs oa{s_img, static_cast<__nv_bfloat16*>(p.out), F, p.S, p.D, NA, p.out_scale, p.status};
+    OutArgs oa{s_img, p.variant, static_cast<__nv_bfloat16*>(p.out), F, p.S, p.D, NA, p.out_scale, p.status};
     const unsigned grid = (unsigned)(F < nsm ? F : nsm);
     ProfScope ps(st, "tc_readout");
     tc_readout_kernel<<<grid, kOutThreads, smem, st>>>(mapQ, mapO, oa);

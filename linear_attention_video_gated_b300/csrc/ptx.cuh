@@ -59,13 +59,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Returns false (and the
-// caller must abandon its work) if it did not within kWaitTimeoutNs.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// caller must abandon its work) if it did not within `limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitTimeoutNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0 && globaltimer() - t0 > kWaitTimeoutNs) return false;
+    if ((i & 63) == 0 && globaltimer() - t0 > limit_ns) return false;
   }
 }
 

@@ -10,4 +10,5 @@ from .gdn_oracle import (  # noqa: F401
     scan_hillis_steele, scan_blelloch_exclusive, fold_random_bracketing,
     spectral_norm_sym, states_from_maps,
     softplus, decay_from_logit, beta_from_logit, frame_fwd_from_logits,
+    relu, relu_linear_head, relu_linear_fwd,
 )

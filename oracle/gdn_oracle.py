@@ -161,6 +161,47 @@ def frame_fwd_from_logits(q, k, v, g_logit, beta_logit, state_in=None):
 
 
 # ----------------------------------------------------------------------------
+# Baseline: SANA-Video's cumulative ReLU-based linear attention.
+#
+# The pages contrast GDN with its predecessor's "cumulative ReLU-based linear
+# attention": a recurrent state that only accumulates, with no decay and no
+# delta-rule correction (zhichai.net summary, section 1, the paragraph on
+# SANA-Video; bilibili article, third key point).  They give no formula; the
+# plainest reading with the GDN scan's own scalings (so the two differ only in
+# the decay, the delta rule and the feature map) is
+#     S_t = S_{t-1} + relu(K_t)^T V_t / sqrt(D*S),   O_t = relu(Q_t) S_t / sqrt(D),
+# with no normaliser (none is mentioned).
+# ----------------------------------------------------------------------------
+
+def relu(x):
+    return np.maximum(np.asarray(x, F64), 0.0)
+
+
+def relu_linear_head(q, k, v, S0=None):
+    """The cumulative ReLU linear attention of one head: q, k, v [T, S, D]; S0 [D, D] or None."""
+    q, k, v = (np.asarray(a, F64) for a in (q, k, v))
+    T, S, D = k.shape
+    St = np.zeros((D, D), F64) if S0 is None else np.array(S0, F64)
+    out = np.zeros((T, S, D), F64)
+    for t in range(T):
+        St = St + (relu(k[t]) * key_scale(D, S)).T @ v[t]
+        out[t] = (relu(q[t]) @ St) * out_scale(D)
+    return out, St
+
+
+def relu_linear_fwd(q, k, v, state_in=None):
+    """Whole-tensor form of relu_linear_head: [B,H,T,S,D] inputs, (out, state_out)."""
+    B, H, T, S, D = np.shape(k)
+    out = np.zeros((B, H, T, S, D), F64)
+    st = np.zeros((B, H, D, D), F64)
+    for b in range(B):
+        for h in range(H):
+            S0 = None if state_in is None else state_in[b, h]
+            out[b, h], st[b, h] = relu_linear_head(q[b, h], k[b, h], v[b, h], S0)
+    return out, st
+
+
+# ----------------------------------------------------------------------------
 # Affine-map forms, used only to cross-check the scan.
 # ----------------------------------------------------------------------------
 

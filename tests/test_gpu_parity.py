@@ -113,6 +113,42 @@ def test_gate_logits(case, mode):
     parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"logits {case} mode={mode}", strict=strict)
 
 
+# (dtype, B, H, T, S, D, nonzero initial state): the cumulative ReLU linear attention baseline
+RELU_CASES = [
+    ("bf16", 1, 20, 21, 880, 112, False),
+    ("bf16", 1, 2, 5, 17, 32, True),
+    ("bf16", 2, 1, 4, 129, 48, False),
+    ("bf16", 1, 1, 9, 64, 128, True),
+    ("f32", 2, 2, 5, 33, 128, True),
+    ("f32", 1, 1, 3, 100, 112, False),
+]
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+@pytest.mark.parametrize("case", RELU_CASES, ids=lambda c: "-".join(map(str, c)))
+def test_relu_linear_baseline(case, mode):
+    """gdn_relu_linear_fwd against the oracle's cumulative ReLU linear attention."""
+    dt, B, H, T, S, D, nz = case
+    base = synth.WORKLOADS["short" if dt == "bf16" else "tiny"]
+    wl = base.with_(B=B, H=H, T=T, S=S, D=D, seed=5000 + 3 * S + D)
+    x = synth.full(wl)
+    q, k, v, _, _ = parity.upload(wl, x)
+    S0 = np.stack([np.stack([synth.state(wl, b, h, 0.3) for h in range(H)]) for b in range(B)]) if nz else None
+    out, st = binding.relu_linear_fwd(q, k, v, state_in=None if S0 is None else torch.from_numpy(S0).cuda(),
+                                      mode=mode)
+    torch.cuda.synchronize()
+    parity.check_status()
+    ro, rs = oracle.relu_linear_fwd(x["q"], x["k"], x["v"], S0)
+    parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"relu-linear {case} mode={mode}", strict=False)
+
+
+def test_relu_linear_rejects_the_cluster_form():
+    wl = synth.WORKLOADS["short"].with_(H=1, T=2, S=16, D=16)
+    q, k, v, _, _ = parity.upload(wl, synth.full(wl))
+    with pytest.raises(binding.GDNError):
+        binding.relu_linear_fwd(q, k, v, mode=3)
+
+
 def _small_bf16(T=21, H=3, S=300, D=112):
     wl = synth.WORKLOADS["short"].with_(H=H, T=T, S=S, D=D)
     return wl, synth.full(wl)
