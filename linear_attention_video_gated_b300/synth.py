@@ -30,7 +30,7 @@ from dataclasses import dataclass, field
 import numpy as np
 
 # Tensor ids mixed into the Philox key.
-TID = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "state": 6}
+TID = {"q": 1, "k": 2, "v": 3, "g": 4, "beta": 5, "state": 6, "dout": 7, "dstate": 8}
 
 
 @dataclass(frozen=True)
@@ -109,7 +109,8 @@ def round_to_dtype(x: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def frame_raw(wl: Workload, name: str, b: int, h: int, t: int) -> np.ndarray:
-    """q/k/v frame (b,h,t): [S, D] float32 N(0,1) draws, before dtype rounding."""
+    """q/k/v (or dout, the gradient a loss sends back into the output) frame
+    (b,h,t): [S, D] float32 N(0,1) draws, before dtype rounding."""
     rng = _rng(wl.seed, TID[name], b, h, t)
     return rng.standard_normal((wl.S, wl.D), dtype=np.float32)
 
@@ -174,6 +175,20 @@ def state(wl: Workload, b: int, h: int, scale: float = 0.1) -> np.ndarray:
     return (scale * rng.standard_normal((wl.D, wl.D))).astype(np.float32)
 
 
+def dstate(wl: Workload, b: int, h: int, scale: float = 0.1) -> np.ndarray:
+    """A gradient for the final state of (b,h): [D, D] float32, N(0, scale^2)."""
+    rng = _rng(wl.seed, TID["dstate"], b, h, 0)
+    return (scale * rng.standard_normal((wl.D, wl.D))).astype(np.float32)
+
+
+def head_dout(wl: Workload, b: int, h: int, t0: int = 0, t1: int | None = None) -> np.ndarray:
+    """Output gradients of one head for frames [t0, t1): [T', S, D] float32 (dtype-rounded)."""
+    t1 = wl.T if t1 is None else t1
+    if t1 <= t0:
+        return np.zeros((0, wl.S, wl.D), np.float32)
+    return np.stack([frame(wl, "dout", b, h, t) for t in range(t0, t1)])
+
+
 def head(wl: Workload, b: int, h: int, t0: int = 0, t1: int | None = None) -> dict:
     """All inputs of one head for frames [t0, t1), float32 arrays (dtype-rounded).
 
@@ -195,6 +210,12 @@ def full(wl: Workload) -> dict:
     hs = [[head(wl, b, h) for h in range(wl.H)] for b in range(wl.B)]
     return {key: np.stack([np.stack([hs[b][h][key] for h in range(wl.H)]) for b in range(wl.B)])
             for key in ("q", "k", "v", "g", "beta")}
+
+
+def full_grads(wl: Workload) -> dict:
+    """dout [B,H,T,S,D] and dstate [B,H,D,D] float32 arrays (small workloads only)."""
+    return {"dout": np.stack([np.stack([head_dout(wl, b, h) for h in range(wl.H)]) for b in range(wl.B)]),
+            "dstate": np.stack([np.stack([dstate(wl, b, h) for h in range(wl.H)]) for b in range(wl.B)])}
 
 
 def _threads() -> int:
