@@ -167,6 +167,66 @@ int gdn_relu_linear_fwd(const void* q, const void* k, const void* v, const float
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * gdn_frame_bwd -- the gradients of gdn_frame_fwd with respect to all of its
+ * inputs, for training.  The pages train the model with this layer (zhichai.net
+ * SANA-WM summary, training pipeline, Stages 1-4) but give no backward pass: it
+ * is the forward definition differentiated.  Per head, with U_t the gradient with
+ * respect to the state after frame t and M_t = K~_t^T diag(beta_t) K~_t:
+ *     U_{T-1} = dstate_out + Q_{T-1}^T dO_{T-1} / sqrt(D)
+ *     U_{t-1} = Q_{t-1}^T dO_{t-1} / sqrt(D) + g_t (U_t - M_t U_t)
+ *     dstate_in = g_0 (U_0 - M_0 U_0)
+ * (the forward's affine map, adjoint, from the last frame to the first), and per
+ * frame, with P = K~_t S_{t-1} and dR = K~_t U_t:
+ *     dQ_t = dO_t S_t^T / sqrt(D)
+ *     dV_t = diag(beta_t) dR
+ *     dbeta_t[s] = <dR_s, V_s - g_t P_s>
+ *     dK_t = ( diag(beta_t)(V_t - g_t P) U_t^T - g_t diag(beta_t) dR S_{t-1}^T ) / sqrt(D*S)
+ *     dg_t = <U_t, S_{t-1}> - sum_s beta_t[s] <dR_s, P_s>
+ *   q, k, v, g, beta, state_in : the forward call's inputs, as gdn_frame_fwd takes
+ *       them (the states S_t are recomputed, not passed in).
+ *   dout       : [B,H,T,S,D] `dtype`, the gradient of the loss with respect to out.
+ *   dstate_out : [B,H,D,D] float32, the gradient with respect to state_out, or NULL
+ *                (zeros: the final state does not enter the loss).
+ *   dq, dk, dv : [B,H,T,S,D] `dtype`, written (bf16 results rounded to nearest even).
+ *   dg         : [B,H,T] float32, written.
+ *   dbeta      : [B,H,T,S] float32, written.
+ *   dstate_in  : [B,H,D,D] float32, written, or NULL (not written).
+ *   workspace  : device memory of at least gdn_bwd_workspace_bytes() bytes,
+ *                256-byte aligned, owned by the caller; not read before it is
+ *                written.  Four D x D float32 matrices per frame-head (M_t, the
+ *                read-out term, S_t, U_t) and one float per 32 tokens.
+ * All pointers are device pointers with the alignment rules of the conventions
+ * (dq, dk, dv, dout, dstate_* 16 bytes; dg, dbeta 4 bytes).  No output may overlap
+ * an input or another output.  Arithmetic is float32 on CUDA cores for both
+ * dtypes.  T = 0 copies dstate_out to dstate_in (zeros if NULL) and touches
+ * nothing else.  Returns as gdn_frame_fwd_ex (GDN_ERR_INVALID_ARG for a NULL
+ * gradient output other than dstate_in).
+ */
+int gdn_frame_bwd(const void* q, const void* k, const void* v,
+                  const float* g, const float* beta, const float* state_in,
+                  const void* dout, const float* dstate_out,
+                  void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dstate_in,
+                  int B, int H, int T, int S, int D, int dtype,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * gdn_frame_bwd_from_logits -- gdn_frame_bwd for gdn_frame_fwd_from_logits: the
+ * gates are given as logits, and dg_logit / dbeta_logit receive the gradients of
+ * the logits (the chain rule through g = exp(-softplus(x)), dg/dx = -g (1 - g),
+ * and beta = sigmoid(y), dbeta/dy = beta (1 - beta), applied inside the kernels).
+ */
+int gdn_frame_bwd_from_logits(const void* q, const void* k, const void* v,
+                              const float* g_logit, const float* beta_logit, const float* state_in,
+                              const void* dout, const float* dstate_out,
+                              void* dq, void* dk, void* dv, float* dg_logit, float* dbeta_logit,
+                              float* dstate_in, int B, int H, int T, int S, int D, int dtype,
+                              void* workspace, size_t workspace_bytes, void* stream);
+
+/* gdn_bwd_workspace_bytes -- workspace gdn_frame_bwd needs (0 for T = 0 and for
+ * arguments it rejects). */
+size_t gdn_bwd_workspace_bytes(int B, int H, int T, int S, int D, int dtype);
+
+/*
  * gdn_frame_fwd_host -- the forward scan over inputs and outputs in HOST memory.
  * (No counterpart on the pages: a streaming runtime around the scan.)
  *   q, k, v, g, beta, state_in, out, state_out : host pointers with the layouts of

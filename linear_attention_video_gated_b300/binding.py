@@ -36,6 +36,9 @@ _SIGS = {
     "gdn_host_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I, _I]),
     "gdn_frame_fwd_noalloc": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     "gdn_noalloc_scratch_bytes": (ctypes.c_size_t, []),
+    "gdn_frame_bwd": (_I, [_P] * 14 + [_I] * 6 + [_P, ctypes.c_size_t, _P]),
+    "gdn_frame_bwd_from_logits": (_I, [_P] * 14 + [_I] * 6 + [_P, ctypes.c_size_t, _P]),
+    "gdn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "gdn_last_error": (_I, [_P]),
     "gdn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "gdn_status_string": (ctypes.c_char_p, [_I]),
@@ -110,6 +113,24 @@ def gdn_frame_fwd_noalloc(q, k, v, g, beta, state_in, out, state_out, B, H, T, S
 
 def gdn_noalloc_scratch_bytes() -> int:
     return lib().gdn_noalloc_scratch_bytes()
+
+
+def gdn_frame_bwd(q, k, v, g, beta, state_in, dout, dstate_out, dq, dk, dv, dg, dbeta, dstate_in, B, H, T, S, D,
+                  dtype, workspace, workspace_bytes, stream) -> int:
+    return lib().gdn_frame_bwd(q, k, v, g, beta, state_in, dout, dstate_out, dq, dk, dv, dg, dbeta, dstate_in, B, H,
+                               T, S, D, dtype, workspace, workspace_bytes, stream)
+
+
+def gdn_frame_bwd_from_logits(q, k, v, g_logit, beta_logit, state_in, dout, dstate_out, dq, dk, dv, dg_logit,
+                              dbeta_logit, dstate_in, B, H, T, S, D, dtype, workspace, workspace_bytes,
+                              stream) -> int:
+    return lib().gdn_frame_bwd_from_logits(q, k, v, g_logit, beta_logit, state_in, dout, dstate_out, dq, dk, dv,
+                                           dg_logit, dbeta_logit, dstate_in, B, H, T, S, D, dtype, workspace,
+                                           workspace_bytes, stream)
+
+
+def gdn_bwd_workspace_bytes(B, H, T, S, D, dtype) -> int:
+    return lib().gdn_bwd_workspace_bytes(B, H, T, S, D, dtype)
 
 
 def gdn_workspace_bytes(B, H, T, S, D, dtype, mode) -> int:
@@ -258,3 +279,37 @@ def relu_linear_fwd(q, k, v, state_in=None, mode=GDN_MODE_SEQUENTIAL, workspace=
     if rc != 0:
         raise GDNError(rc, "gdn_relu_linear_fwd")
     return out, state_out
+
+
+def frame_bwd(q, k, v, g, beta, dout, state_in=None, dstate_out=None, gate_logits=False, workspace=None,
+              stream=None, want_dstate_in=True):
+    """gdn_frame_bwd (or gdn_frame_bwd_from_logits with gate_logits=True) on torch
+    CUDA tensors: the forward's inputs (layouts as frame_fwd), dout like q, and
+    dstate_out [B,H,D,D] float32 or None.  Returns a dict of dq, dk, dv (dtype of q),
+    dg [B,H,T], dbeta [B,H,T,S] and dstate_in [B,H,D,D] (None unless want_dstate_in);
+    with gate_logits the dg and dbeta entries are the logits' gradients."""
+    import torch
+
+    B, H, T, S, D = q.shape
+    dtype = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}[q.dtype]
+    for name, t in (("k", k), ("v", v), ("dout", dout)):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous() or not t.is_cuda:
+            raise ValueError(f"{name}: expected a contiguous CUDA tensor like q")
+    if tuple(g.shape) != (B, H, T) or tuple(beta.shape) != (B, H, T, S):
+        raise ValueError("g must be [B,H,T] and beta [B,H,T,S]")
+    out = {"dq": torch.empty_like(q), "dk": torch.empty_like(q), "dv": torch.empty_like(q),
+           "dg": torch.empty((B, H, T), dtype=torch.float32, device=q.device),
+           "dbeta": torch.empty((B, H, T, S), dtype=torch.float32, device=q.device),
+           "dstate_in": torch.empty((B, H, D, D), dtype=torch.float32, device=q.device) if want_dstate_in else None}
+    need = gdn_bwd_workspace_bytes(B, H, T, S, D, dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    strm = stream if stream is not None else torch.cuda.current_stream(q.device)
+    fn = gdn_frame_bwd_from_logits if gate_logits else gdn_frame_bwd
+    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(dout), _ptr(dstate_out),
+            _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]),
+            _ptr(out["dstate_in"]), B, H, T, S, D, dtype, _ptr(workspace),
+            0 if workspace is None else workspace.numel(), strm.cuda_stream)
+    if rc != 0:
+        raise GDNError(rc, "gdn_frame_bwd")
+    return out

@@ -14,6 +14,7 @@
 // prefix mode composes (zhichai.net SANA-WM summary, training Stage 3).
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -61,6 +62,12 @@ __device__ __forceinline__ float beta_of(float x, int logits) { return logits ? 
 enum Variant { kGdn = 0, kReluLinear = 1 };
 __device__ __forceinline__ float relu_if(float x, int variant) { return variant == kReluLinear ? fmaxf(x, 0.f) : x; }
 
+// Element loads and stores of the I/O dtypes (float32 arithmetic inside).
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void from_f32(float& d, float x) { d = x; }
+__device__ __forceinline__ void from_f32(__nv_bfloat16& d, float x) { d = __float2bfloat16_rn(x); }
+
 // Records a device-side error in the status word; the first error wins.
 __device__ __forceinline__ void report_device_error(unsigned int* status, unsigned int code) {
   atomicCAS(status, 0u, code);
@@ -81,6 +88,9 @@ unsigned int* device_status_word();
 // ---- SIMT path (float32 arithmetic; used for float32 I/O) --------------------
 size_t simt_workspace_bytes(const Problem& p, int mode);
 int simt_forward(const Problem& p, void* ws, cudaStream_t st);
+// M_t, b_t and the state S_t after every frame (each BHT x D x D float32, frame-head
+// major), by the sequential scan; writes p.state_out when it is not null.
+int simt_states(const Problem& p, float* Mws, float* bws, float* Sws, cudaStream_t st);
 
 // ---- tensor-core path (bf16 I/O) ------------------------------------------------
 size_t tc_workspace_bytes(const Problem& p, int mode);

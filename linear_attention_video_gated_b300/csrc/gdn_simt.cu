@@ -26,11 +26,6 @@ constexpr int kTok = 32;       // tokens staged per gram iteration
 constexpr int kOutRows = 64;   // tokens per readout CTA
 constexpr int kChunk = 16;     // frames per chunk in prefix mode
 
-__device__ __forceinline__ float to_f32(float x) { return x; }
-__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ void from_f32(float& d, float x) { d = x; }
-__device__ __forceinline__ void from_f32(__nv_bfloat16& d, float x) { d = __float2bfloat16_rn(x); }
-
 // C[i][j] = scale * sum_s (beta_s A[s][i]) X[s][j]; which = 0 -> X = K (gives M),
 // which = 1 -> X = V (gives b).  One CTA per (frame-head, which).
 template <typename TIn>
@@ -351,13 +346,12 @@ SimtLayout simt_layout(const Problem& p, int mode) {
   return L;
 }
 
+// The transition terms M_t, b_t of every frame, then the state S_t after every
+// frame (sequential scan, or the prefix form's compose / boundary / replay when
+// `prefix`).  Writes p.state_out when it is not null.
 template <typename TIn>
-int run(const Problem& p, void* ws, cudaStream_t st) {
-  const SimtLayout L = simt_layout(p, p.mode);
-  char* w = static_cast<char*>(ws);
-  float* Mws = reinterpret_cast<float*>(w + L.m_off);
-  float* bws = reinterpret_cast<float*>(w + L.b_off);
-  float* Sws = reinterpret_cast<float*>(w + L.s_off);
+int states(const Problem& p, float* Mws, float* bws, float* Sws, char* w, const SimtLayout& L, bool prefix,
+           cudaStream_t st) {
   const int D = p.D;
   const size_t mat = (size_t)D * D * sizeof(float);
 
@@ -370,7 +364,7 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
 
-  if (p.mode != 1) {  // sequential and split forms are the same three stages here
+  if (!prefix) {
     const size_t smem = 2 * mat;
     if (cudaFuncSetAttribute(scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return kCuda;
@@ -410,6 +404,21 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
     }
     if (cudaGetLastError() != cudaSuccess) return kCuda;
   }
+  return kOk;
+}
+
+template <typename TIn>
+int run(const Problem& p, void* ws, cudaStream_t st) {
+  const SimtLayout L = simt_layout(p, p.mode);
+  char* w = static_cast<char*>(ws);
+  float* Mws = reinterpret_cast<float*>(w + L.m_off);
+  float* bws = reinterpret_cast<float*>(w + L.b_off);
+  float* Sws = reinterpret_cast<float*>(w + L.s_off);
+  const int D = p.D;
+  const size_t mat = (size_t)D * D * sizeof(float);
+  // sequential and split forms are the same three stages here
+  const int rc = states<TIn>(p, Mws, bws, Sws, w, L, p.mode == 1, st);
+  if (rc != kOk) return rc;
 
   const size_t osmem = mat + kOutRows * D * sizeof(float);
   if (cudaFuncSetAttribute(readout_kernel<TIn>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)osmem) !=
@@ -431,6 +440,12 @@ size_t simt_workspace_bytes(const Problem& p, int mode) { return simt_layout(p, 
 int simt_forward(const Problem& p, void* ws, cudaStream_t st) {
   if (p.dtype == 0) return run<float>(p, ws, st);
   return run<__nv_bfloat16>(p, ws, st);
+}
+
+int simt_states(const Problem& p, float* Mws, float* bws, float* Sws, cudaStream_t st) {
+  const SimtLayout L{};  // the sequential scan uses no chunk buffers
+  if (p.dtype == 0) return states<float>(p, Mws, bws, Sws, nullptr, L, false, st);
+  return states<__nv_bfloat16>(p, Mws, bws, Sws, nullptr, L, false, st);
 }
 
 }  // namespace gdn

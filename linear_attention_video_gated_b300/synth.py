@@ -251,6 +251,23 @@ def fill_io(wl: Workload, q: np.ndarray, k: np.ndarray, v: np.ndarray,
             pass
 
 
+def fill_dout(wl: Workload, dst: np.ndarray, t0: int = 0, b0: int = 0, threads: int | None = None) -> None:
+    """Fill a caller-owned host array [B', H, T', S, D] (uint16 bf16 bits or float32)
+    with the output gradients of frames [t0, t0 + T') of batch indices [b0, b0 + B')."""
+    Bn, Hn, Tn = dst.shape[0], dst.shape[1], dst.shape[2]
+    jobs = [(bb, h, tt) for bb in range(Bn) for h in range(Hn) for tt in range(Tn)]
+    nthreads = threads or _threads()
+
+    def one(job):
+        bb, h, tt = job
+        x = frame_raw(wl, "dout", b0 + bb, h, t0 + tt)
+        dst[bb, h, tt] = bf16_bits(x) if wl.dtype == "bf16" else x
+
+    with ThreadPoolExecutor(nthreads) as ex:
+        for _ in ex.map(one, jobs, chunksize=max(1, len(jobs) // (16 * nthreads))):
+            pass
+
+
 def head_sample(wl: Workload, n: int) -> list:
     """n (b, h) heads spread over the workload (first and last always included)."""
     heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]

@@ -74,6 +74,55 @@ def device_inputs(wl, dev="cuda", t0=0, t1=None):
     return q, k, v, g, beta
 
 
+def device_dout(wl, dev="cuda"):
+    """The output gradients of every frame, generated straight into a CUDA tensor
+    one batch index at a time."""
+    tdt = torch_dtype(wl)
+    out = torch.empty((wl.B, wl.H, wl.T, wl.S, wl.D), dtype=tdt, device=dev)
+    hdt = np.uint16 if wl.dtype == "bf16" else np.float32
+    for b in range(wl.B):
+        h = np.empty((1, wl.H, wl.T, wl.S, wl.D), hdt)
+        synth.fill_dout(wl, h, b0=b)
+        t = torch.from_numpy(h)
+        out[b:b + 1].copy_(t.view(torch.bfloat16) if wl.dtype == "bf16" else t)
+    return out
+
+
+GRAD_KEYS = ("dq", "dk", "dv", "dg", "dbeta", "dstate_in")
+F32_GRAD_MAX_ABS_OVER_RMS = 1e-4
+F32_OUT_OF_BF16_CALL_MAX_ABS_OVER_RMS = 1e-3
+
+
+def assert_grad_parity(wl_dtype, gpu, ref, what=""):
+    """Backward-pass bound, per gradient tensor.
+
+    float32 I/O: every gradient within 1e-4 x rms(oracle) (float32 arithmetic
+    from exact inputs: sums of up to ~1e5 products, typical relative error
+    ~sqrt(n) x 2^-24 ~ 2e-5).  bf16 I/O: dq, dk, dv are bf16 outputs and take the
+    forward's bf16 bound with the half-ulp allowance; dg, dbeta and dstate_in are
+    float32 outputs of float32 arithmetic on exact (bf16-valued) inputs and are held
+    to 1e-3 x rms -- far above float32 rounding, far below the effect of a dropped
+    or wrong term."""
+    res = {}
+    for key in GRAD_KEYS:
+        if key not in gpu or gpu[key] is None:
+            continue
+        e = errors(gpu[key], ref[key])
+        res[key] = e
+        assert e["finite"], f"{what} {key}: non-finite values"
+        if e["rms_ref"] == 0:
+            assert e["max_abs"] == 0.0, f"{what} {key}: {e}"
+            continue
+        if wl_dtype == "f32":
+            assert e["max_abs_over_rms"] <= F32_GRAD_MAX_ABS_OVER_RMS, f"{what} {key}: {e}"
+        elif key in ("dq", "dk", "dv"):
+            assert e["max_beyond_half_ulp_over_rms"] <= BF16_MAX_ABS_OVER_RMS, f"{what} {key}: {e}"
+            assert e["rms_err_over_rms"] <= BF16_RMS_ERR_OVER_RMS, f"{what} {key}: {e}"
+        else:
+            assert e["max_abs_over_rms"] <= F32_OUT_OF_BF16_CALL_MAX_ABS_OVER_RMS, f"{what} {key}: {e}"
+    return res
+
+
 def oracle_head(wl, b, h, S0=None):
     x = synth.head(wl, b, h)
     return oracle.scan_head(x["q"], x["k"], x["v"], x["g"], x["beta"], S0)

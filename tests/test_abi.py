@@ -129,3 +129,39 @@ def test_host_workspace_bytes(lib):
         binding.gdn_host_workspace_bytes(1, 20, 10, 880, 112, 1, 10)
     assert binding.gdn_host_workspace_bytes(1, 20, 961, 880, 112, 1, 0) == 0
     assert binding.gdn_host_workspace_bytes(1, 20, 961, 880, 24, 1, 32) == 0
+
+
+def _bwd(B=1, H=2, T=3, S=17, D=32, dtype=1, ptr=A16, dout=A16, dq=A16, dk=A16, dv=A16, dg=A16, dbeta=A16,
+         dstate_out=None, dstate_in=None, state_in=None, ws=A16, wsb=1 << 40, logits=False):
+    fn = binding.gdn_frame_bwd_from_logits if logits else binding.gdn_frame_bwd
+    return fn(ptr, ptr, ptr, ptr, ptr, state_in, dout, dstate_out, dq, dk, dv, dg, dbeta, dstate_in,
+              B, H, T, S, D, dtype, ws, wsb, None)
+
+
+@pytest.mark.parametrize("logits", [False, True])
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), 1), (dict(T=-1), 1), (dict(S=0), 1), (dict(dtype=3), 1), (dict(D=24), 2), (dict(D=144), 2),
+    (dict(ptr=None), 1), (dict(dout=None), 1), (dict(dq=None), 1), (dict(dk=None), 1), (dict(dv=None), 1),
+    (dict(dg=None), 1), (dict(dbeta=None), 1),
+    (dict(dout=MIS), 3), (dict(dq=MIS), 3), (dict(dk=MIS), 3), (dict(dv=MIS), 3), (dict(dg=A16 + 2), 3),
+    (dict(dbeta=A16 + 1), 3), (dict(dstate_out=MIS), 3), (dict(dstate_in=MIS), 3), (dict(state_in=MIS), 3),
+    (dict(ws=None), 6), (dict(wsb=16), 6), (dict(ws=A16 + 16), 3),
+])
+def test_backward_validation_rejects(lib, kw, code, logits):
+    assert _bwd(logits=logits, **kw) == code
+
+
+def test_backward_zero_frames_needs_no_gradient_outputs(lib):
+    """T = 0 with no dstate_in: nothing to compute, nothing touched, no CUDA call."""
+    assert _bwd(T=0, ptr=None, dout=None, dq=None, dk=None, dv=None, dg=None, dbeta=None, ws=None) == 0
+
+
+def test_backward_workspace_bytes(lib):
+    a = binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 112, 1)
+    # four D x D float32 matrices per frame-head plus one float per 32-token tile
+    assert a >= 4 * 20 * 961 * 112 * 112 * 4 + 20 * 961 * 28 * 4
+    assert a == binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 112, 0)
+    assert binding.gdn_bwd_workspace_bytes(1, 20, 0, 880, 112, 1) == 0
+    assert binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 24, 1) == 0
+    assert binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 112, 5) == 0
+    assert binding.gdn_bwd_workspace_bytes(2, 20, 961, 880, 112, 1) > a
