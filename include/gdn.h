@@ -193,13 +193,16 @@ int gdn_relu_linear_fwd(const void* q, const void* k, const void* v, const float
  *   dstate_in  : [B,H,D,D] float32, written, or NULL (not written).
  *   workspace  : device memory of at least gdn_bwd_workspace_bytes() bytes,
  *                256-byte aligned, owned by the caller; not read before it is
- *                written.  Four D x D float32 matrices per frame-head (M_t, the
- *                read-out term, S_t, U_t) and one float per 32 tokens.
+ *                written.  Per frame-head: M_t, the read-out term Q^T dO, S_t and
+ *                U_t (float32 matrices for GDN_F32; for GDN_BF16 M_t as a bf16
+ *                image and S_t, U_t as bf16 hi + lo images) and a few partial sums.
  * All pointers are device pointers with the alignment rules of the conventions
  * (dq, dk, dv, dout, dstate_* 16 bytes; dg, dbeta 4 bytes).  No output may overlap
- * an input or another output.  Arithmetic is float32 on CUDA cores for both
- * dtypes.  T = 0 copies dstate_out to dstate_in (zeros if NULL) and touches
- * nothing else.  Returns as gdn_frame_fwd_ex (GDN_ERR_INVALID_ARG for a NULL
+ * an input or another output.  GDN_F32 computes in float32 on CUDA cores;
+ * GDN_BF16 runs the dense products on the tensor cores (bf16 operands, the states
+ * and state gradients split into bf16 hi + lo parts, float32 accumulation) and
+ * the element-wise steps in float32.  T = 0 copies dstate_out to dstate_in (zeros
+ * if NULL) and touches nothing else.  Returns as gdn_frame_fwd_ex (GDN_ERR_INVALID_ARG for a NULL
  * gradient output other than dstate_in).
  */
 int gdn_frame_bwd(const void* q, const void* k, const void* v,

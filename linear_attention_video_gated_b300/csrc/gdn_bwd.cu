@@ -1,5 +1,7 @@
 // Backward pass of the frame-wise GDN scan (gdn_frame_bwd): the gradients of
-// every input of the forward scan, in float32 on CUDA cores for both I/O dtypes.
+// every input of the forward scan.  This file holds the C ABI, the float32 I/O
+// path (CUDA cores, float32 arithmetic) and the dg reduction both paths share;
+// bf16 I/O runs on the tensor cores (tc_backward in gdn_tc.cu).
 //
 // The pages train the model with this layer but give no backward pass; it is
 // the forward definition differentiated.  With U_t the gradient with respect to
@@ -388,12 +390,7 @@ BwdLayout bwd_layout(const Problem& p) {
   return L;
 }
 
-struct Grads {
-  const void* dout;
-  const float* dstate_out;
-  void *dq, *dk, *dv;
-  float *dg, *dbeta, *dstate_in;
-};
+using Grads = BwdGrads;
 
 template <typename TIn>
 int run_bwd(const Problem& p, const Grads& gr, void* ws, cudaStream_t st) {
@@ -455,13 +452,11 @@ int run_bwd(const Problem& p, const Grads& gr, void* ws, cudaStream_t st) {
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
 
-  {
-    ProfScope ps(st, "bwd_dg_sum");
-    const long long nf = p.BHT();
-    dg_sum_kernel<<<(unsigned)((nf + 255) / 256), 256, 0, st>>>(dg_part, p.g, gr.dg, nf, L.ntiles, p.gate_logits);
-  }
-  if (cudaGetLastError() != cudaSuccess) return kCuda;
-  return kOk;
+  return launch_dg_sum(dg_part, p.g, gr.dg, p.BHT(), L.ntiles, p.gate_logits, st);
+}
+
+size_t workspace_of(const Problem& p) {
+  return p.dtype == GDN_BF16 ? tc_bwd_workspace_bytes(p) : bwd_layout(p).total;
 }
 
 bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
@@ -513,14 +508,24 @@ int frame_bwd(const void* q, const void* k, const void* v, const float* g, const
                                      : cudaMemsetAsync(dstate_in, 0, bytes, st);
     return e == cudaSuccess ? kOk : kCuda;
   }
-  if (!workspace || workspace_bytes < bwd_layout(p).total) return kWorkspace;
+  if (!workspace || workspace_bytes < workspace_of(p)) return kWorkspace;
   if (!aligned(workspace, 256)) return kMisaligned;
   p.status = device_status_word();
   if (!p.status) return kCuda;
-  return dtype == GDN_F32 ? run_bwd<float>(p, gr, workspace, st) : run_bwd<__nv_bfloat16>(p, gr, workspace, st);
+  return dtype == GDN_F32 ? run_bwd<float>(p, gr, workspace, st) : tc_backward(p, gr, workspace, st);
 }
 
 }  // namespace
+
+int launch_dg_sum(const float* dg_part, const float* g, float* dg, long long nframes, int ntiles, int logits,
+                  cudaStream_t st) {
+  {
+    ProfScope ps(st, "bwd_dg_sum");
+    dg_sum_kernel<<<(unsigned)((nframes + 255) / 256), 256, 0, st>>>(dg_part, g, dg, nframes, ntiles, logits);
+  }
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
+
 }  // namespace gdn
 
 using namespace gdn;
@@ -534,7 +539,7 @@ extern "C" size_t gdn_bwd_workspace_bytes(int B, int H, int T, int S, int D, int
   if (check_bwd(d, d, d, fd, fd, nullptr, d, nullptr, const_cast<void*>(d), const_cast<void*>(d),
                 const_cast<void*>(d), fd, fd, nullptr, B, H, T, S, D, dtype, &p, &gr) != kOk)
     return 0;
-  return T == 0 ? 0 : bwd_layout(p).total;
+  return T == 0 ? 0 : workspace_of(p);
 }
 
 extern "C" int gdn_frame_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta,

@@ -96,6 +96,22 @@ int simt_states(const Problem& p, float* Mws, float* bws, float* Sws, cudaStream
 size_t tc_workspace_bytes(const Problem& p, int mode);
 int tc_forward(const Problem& p, void* ws, cudaStream_t st);
 
+// ---- backward pass (gdn_bwd.cu; the bf16 kernels in gdn_tc.cu) -------------------
+struct BwdGrads {
+  const void* dout;
+  const float* dstate_out;
+  void *dq, *dk, *dv;
+  float *dg, *dbeta, *dstate_in;
+};
+// Tensor-core backward (bf16 I/O): workspace bytes, and the call.  Writes dq, dk,
+// dv, dbeta and dstate_in, and per (frame-head, 128-token tile) partial sums of dg
+// into `dg_part` (*ntiles tiles per frame-head), which launch_dg_sum reduces.
+size_t tc_bwd_workspace_bytes(const Problem& p);
+int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st);
+// dg[f] = sum of dg_part[f * ntiles .. + ntiles) (times dg/dlogit for logits).
+int launch_dg_sum(const float* dg_part, const float* g, float* dg, long long nframes, int ntiles, int logits,
+                  cudaStream_t st);
+
 // ---- fused tensor-core path (bf16 I/O, one cluster per head, no scratch) ---------
 bool fused_supported(const Problem& p);
 int fused_forward(const Problem& p, cudaStream_t st);

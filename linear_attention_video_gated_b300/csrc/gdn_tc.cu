@@ -188,6 +188,10 @@ struct GramArgs {
   int S, D, NA;
   float m_scale, b_scale;
   unsigned int* status;
+  // 1: only the b part, with beta = 1 (the backward's Q^T dO: K holds Q, V holds
+  // dO); no M image.  The A operand is then exact in bf16, so its lo part is zero
+  // and its MMA is skipped.
+  int b_only;
 };
 
 __global__ void __launch_bounds__(kGramThreads, 1)
@@ -289,6 +293,11 @@ __global__ void __launch_bounds__(kGramThreads, 1)
 #pragma unroll
           for (int kk = 0; kk < kGramTok / 16; ++kk) {
             const uint32_t off = kk * 2048;
+            if (a.b_only) {
+              mma_bf16(acc + NA * 64, smem_desc(ah + off, kGramRegion, 1024),
+                       smem_desc(rb + NA * kGramRegion + off, kGramRegion, 1024), id2, (c > 0 || kk > 0) ? 1u : 0u);
+              continue;
+            }
             mma_bf16(acc, smem_desc(ah + off, kGramRegion, 1024), smem_desc(rb + off, kGramRegion, 1024), id1,
                      (c > 0 || kk > 0) ? 1u : 0u);
             mma_bf16(acc + NA * 64, smem_desc(al + off, kGramRegion, 1024),
@@ -318,14 +327,14 @@ __global__ void __launch_bounds__(kGramThreads, 1)
       const int s = c * kGramTok + rw;
       // raw value, mapped when used: mapping here would wait for the load
       if (!(f < a.nitems && s < S)) return -INFINITY;
-      return a.variant == kReluLinear ? 1.f : __ldg(a.beta + f * S + s);
+      return (a.variant == kReluLinear || a.b_only) ? 1.f : __ldg(a.beta + f * S + s);
     };
     long long fn = blockIdx.x;
     int cn = 0;
     // beta of token rows r0 and r0 + 32: raw values loaded one tile ahead, mapped
     // (rows past S, loaded as -inf, give 0) after the current tile is converted.
     auto mapped = [&](float x) {
-      return x == -INFINITY ? 0.f : (a.variant == kReluLinear ? x : beta_of(x, a.gate_logits));
+      return x == -INFINITY ? 0.f : ((a.variant == kReluLinear || a.b_only) ? x : beta_of(x, a.gate_logits));
     };
     float bn0 = beta_at(fn, 0, r0), bn1 = beta_at(fn, 0, r0 + 32);
     float b0 = mapped(bn0), b1 = mapped(bn1);
@@ -373,7 +382,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
       if (barrier_any(1, 128, !ok || *abort_flag)) goto done;
       tc_fence_after();
       const uint32_t acc = tmem + ((uint32_t)(warp * 32) << 16) + ab * 256;
-      for (int c0 = 0; c0 < D; c0 += 16) {
+      for (int c0 = 0; c0 < (a.b_only ? 0 : D); c0 += 16) {
         float v[16];
         tmem_ld16(acc + c0, v);
         tmem_ld_wait();
@@ -408,7 +417,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
       if (++ab == 2) { ab = 0; aph ^= 1; }
       fence_proxy_async_smem();
       named_barrier(1, 128);
-      if (threadIdx.x == 0) {
+      if (threadIdx.x == 0 && !a.b_only) {
         bulk_s2g(a.m_img + (size_t)f * NA * D * 128, smem_u32(mstage), NA * D * 128);
         bulk_commit();
       }
@@ -456,6 +465,11 @@ struct ScanArgs {
   float* state_out;
   int T, D, NA;
   unsigned int* status;
+  // 1: the backward pass's state-gradient scan, U_{t-1} = g_t (U_t - M_t U_t) + E_{t-1}
+  // over t = T-1 .. 0.  b_blk holds E; state_in is dS_T and the scan starts from
+  // U_{T-1} = dS_T + E_{T-1}; image slot t receives U_t (t = T-1 .. 0); state_out
+  // receives dS_0 = g_0 (U_0 - M_0 U_0).
+  int reverse;
 };
 
 __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
@@ -506,15 +520,19 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     // ---------------- copies in: M_t image (NA atoms of D rows) and the b_t block
     if (lane == 0) {
       Ring<kScanStages> r;
-      for (int t = 0; t < T; ++t) {
+      for (int j = 0; j < T; ++j) {
         if (!wait_or_abort(smem_u32(&empty[r.stage]), r.phase ^ 1, abort_flag, a.status)) break;
+        const int t = a.reverse ? T - 1 - j : j;
         const long long f = bh * T + t;
+        // the b term of step j: b_t forward, E_{t-1} in reverse (frame 0's block,
+        // unused, stands in for E_{-1})
+        const long long fbk = a.reverse ? bh * T + (t > 0 ? t - 1 : 0) : f;
         const uint32_t fb = smem_u32(&full[r.stage]);
         mbar_arrive_expect_tx(fb, NA * D * 128 + D * 64);
         const uint8_t* src = a.m_img + (size_t)f * NA * D * 128;
         for (int at = 0; at < NA; ++at)
           bulk_g2s(smem_u32(mring + r.stage * kScanMStage + at * 128 * 128), src + at * D * 128, D * 128, fb);
-        bulk_g2s(smem_u32(bring + r.stage * kScanBStage), a.b_blk + ((size_t)f * ncb + cb) * D * 16, D * 64, fb);
+        bulk_g2s(smem_u32(bring + r.stage * kScanBStage), a.b_blk + ((size_t)fbk * ncb + cb) * D * 16, D * 64, fb);
         r.mark_issued();
         r.advance();
       }
@@ -524,10 +542,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     // ---------------- MMA: P = M_t S_{t-1}[:, J]
     if (lane == 0) {
       const uint32_t id = idesc_bf16(128, 32, 0, 0);
-      // the state block of frame u (image buffer (u + 1) & 1) to global memory, laid
-      // out as in shared memory
+      // the state block after step u (image buffer (u + 1) & 1; u = -1 is the
+      // initial state) to global memory, laid out as in shared memory: slot u, or
+      // in reverse slot T - 2 - u (the frame index of the gradient U it holds)
       auto store_block = [&](int u) {
-        const long long f = bh * T + u;
+        const long long f = bh * T + (a.reverse ? T - 2 - u : u);
         bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(img + ((u + 1) & 1) * kScanImg),
                  NA * 32 * 128);
         bulk_commit();
@@ -551,14 +570,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           if (kk < KS) mma_bf16(tmem, ad0[kk] + ao, bd0[kk] + bo, id, kk > 0 ? 1u : 0u);
-        if (t >= 1) store_block(t - 1);
+        if (t >= 1 || a.reverse) store_block(t - 1);
         // The store of S_{t-2} has read its buffer, which S_t may now overwrite.
         asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         mma_commit(smem_u32(pfull));
         mma_commit(smem_u32(&empty[stage]));
         if (++stage == kScanStages) { stage = 0; phase ^= 1; }
       }
-      if (T > 0) {
+      if (T > 0 && !a.reverse) {  // the reverse scan's last result is dS_0 (state_out only)
         if (!wait_or_abort(smem_u32(sready), T & 1, abort_flag, a.status)) goto done;
         store_block(T - 1);
       }
@@ -579,6 +598,17 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
         x[4 * q + 1] = w.y;
         x[4 * q + 2] = w.z;
         x[4 * q + 3] = w.w;
+      }
+    }
+    if (row && a.reverse && T > 0) {  // U_{T-1} = dS_T + E_{T-1}
+      const float4* e = reinterpret_cast<const float4*>(a.b_blk + (((size_t)(bh * T + T - 1) * ncb + cb) * D + i) * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 w = e[q];
+        x[4 * q] += w.x;
+        x[4 * q + 1] += w.y;
+        x[4 * q + 2] += w.z;
+        x[4 * q + 3] += w.w;
       }
     }
     // state block image (B operand, K-major: row n = value column 16cb + n for the
@@ -603,11 +633,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     int stage = 0;
     uint32_t phase = 0;
     const bool relu_lin = a.variant == kReluLinear;  // g = 1, no delta-rule term
-    float gnext = (T > 0 && !relu_lin) ? __ldg(a.g + bh * T) : 0.f;  // raw; mapped when used
-    for (int t = 0; t < T; ++t) {
-      const long long f = bh * T + t;
+    // raw decay of the next step's frame; mapped when used
+    float gnext = (T > 0 && !relu_lin) ? __ldg(a.g + bh * T + (a.reverse ? T - 1 : 0)) : 0.f;
+    for (int t = 0; t < T; ++t) {  // t counts steps; the step's frame is fr
+      const int fr = a.reverse ? T - 1 - t : t;
+      const long long f = bh * T + fr;
       const float gt = relu_lin ? 1.f : decay_of(gnext, a.gate_logits);
-      if (t + 1 < T && !relu_lin) gnext = __ldg(a.g + f + 1);
+      if (t + 1 < T && !relu_lin) gnext = __ldg(a.g + (a.reverse ? f - 1 : f + 1));
+      const bool add_b = !(a.reverse && fr == 0);  // E_{-1} = 0
       const bool ok = wait_or_abort(smem_u32(pfull), t & 1, abort_flag, a.status) &&
                       wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
       if (__all_sync(0xffffffffu, ok)) {
@@ -633,7 +666,8 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
         if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
         if (row) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) x[j] = relu_lin ? x[j] + bv[j] : fmaf(gt, x[j] - (p[j] + pl[j]), bv[j]);
+          for (int j = 0; j < 16; ++j)
+            x[j] = relu_lin ? x[j] + bv[j] : fmaf(gt, x[j] - (p[j] + pl[j]), add_b ? bv[j] : 0.f);
         }
         // S_t goes into the buffer of S_{t-2}, whose store has read it (the MMA
         // thread waited for that before committing pfull(t)).
@@ -684,6 +718,9 @@ struct OutArgs {
   int S, D, NA;
   float scale;
   unsigned int* status;
+  // 1: multiply by S_t^T instead (the backward's dQ = dO S_t^T / sqrt(D)): the
+  // same image read as an MN-major B operand.
+  int transpose_s;
 };
 
 __global__ void __launch_bounds__(kOutThreads, 1)
@@ -779,7 +816,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
   } else if (warp == 5) {
     // ---------------- MMA: O_tile (128 tokens x D) = Q_tile S_hi + Q_tile S_lo
     if (lane == 0) {
-      const uint32_t id = idesc_bf16(128, D, 0, 0);
+      const uint32_t id = idesc_bf16(128, D, 0, a.transpose_s ? 1 : 0);
       int ab = 0, qs = 0, cb = 0;
       uint32_t aph = 0, qph = 0, cph = 0;
       for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
@@ -793,10 +830,13 @@ __global__ void __launch_bounds__(kOutThreads, 1)
           const uint32_t acc = tmem + cb * 128;
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t ko = (kk >> 2) * (kOutTok * 128) + (kk & 3) * 32;
-            const uint32_t so = (kk >> 2) * (D * 128) + (kk & 3) * 32;
             const uint64_t ad = smem_desc(qb + ko, 16, 1024);
-            mma_bf16(acc, ad, smem_desc(im + so, 16, 1024), id, kk > 0 ? 1u : 0u);
-            mma_bf16(acc, ad, smem_desc(im + NA * D * 128 + so, 16, 1024), id, 1u);
+            // K-major: rows = value columns, K-steps of 16 key dims inside an atom;
+            // MN-major (transposed): K-steps of 16 rows (value columns), LBO = atom stride
+            const uint32_t so = a.transpose_s ? kk * 2048 : (kk >> 2) * (D * 128) + (kk & 3) * 32;
+            const uint32_t lbo = a.transpose_s ? D * 128 : 16;
+            mma_bf16(acc, ad, smem_desc(im + so, lbo, 1024), id, kk > 0 ? 1u : 0u);
+            mma_bf16(acc, ad, smem_desc(im + NA * D * 128 + so, lbo, 1024), id, 1u);
           }
           mma_commit(smem_u32(&qempty[qs]));
           mma_commit(smem_u32(&accfull[cb]));
@@ -890,6 +930,342 @@ done:
   }
 }
 
+// =============================================================================
+// Backward pass (gdn_frame_bwd, bf16 I/O).  The forward kernels above supply
+// most of it: the gram (M_t, b_t) and scan (every S_t image) recompute the
+// states; the gram's b-only form gives E_t = Q_t^T dO_t / sqrt(D); the scan's
+// reverse form runs the state gradient U back through the adjoint map; the
+// read-out's transposed form gives dQ = dO S_t^T / sqrt(D).  The kernel below
+// does the rest, per frame-head and 128-token tile (K~ = K / sqrt(D*S)):
+//   P = K~ S_{t-1},  dR = K~ U_t                       (tensor core, hi + lo)
+//   R = beta (V - g P),  dP = -g beta dR,  dV = beta dR,
+//   dbeta_s = <dR_s, V_s - g P_s>,  dg partial = -sum_s beta_s <dR_s, P_s>
+//                                                      (fp32 registers)
+//   dK~ = R U_t^T + dP S_{t-1}^T                       (tensor core: R and dP as
+//                                                       bf16 A operands, the
+//                                                       images read MN-major)
+// plus <U_t, S_{t-1}> from the two images, added to tile 0's dg partial.
+// =============================================================================
+
+// The initial state of every head as a scan block image (bf16 hi + lo), the
+// backward's S_{-1}; zeros when `state` is null.  grid = (heads, D/16); thread =
+// key dim (all 64 * NA positions written, those past D as zeros).
+__global__ void __launch_bounds__(128) tc_state_image_kernel(const float* __restrict__ state,
+                                                             uint8_t* __restrict__ img, int D, int NA) {
+  const long long bh = blockIdx.x;
+  const int cb = blockIdx.y, ncb = gridDim.y, i = threadIdx.x;
+  if (i >= NA * 64) return;
+  float x[16];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) x[n] = (state && i < D) ? state[((size_t)bh * D + i) * D + 16 * cb + n] : 0.f;
+  uint8_t* at = img + ((size_t)bh * ncb + cb) * NA * (32 * 128) + (i >> 6) * (32 * 128);
+#pragma unroll
+  for (int n = 0; n < 16; n += 2) {
+    uint32_t hv, lv;
+    split2(x[n], x[n + 1], hv, lv);
+    *reinterpret_cast<uint16_t*>(at + sw128_off(n, i & 63)) = (uint16_t)(hv & 0xFFFF);
+    *reinterpret_cast<uint16_t*>(at + sw128_off(n + 1, i & 63)) = (uint16_t)(hv >> 16);
+    *reinterpret_cast<uint16_t*>(at + sw128_off(16 + n, i & 63)) = (uint16_t)(lv & 0xFFFF);
+    *reinterpret_cast<uint16_t*>(at + sw128_off(17 + n, i & 63)) = (uint16_t)(lv >> 16);
+  }
+}
+
+constexpr int kKvTok = 128;      // tokens per tile (MMA M)
+constexpr int kKvThreads = 192;  // 4 epilogue, 1 copy, 1 MMA warps
+
+struct KvArgs {
+  const uint8_t* s_img;   // S_t images (F slots, the scan's block layout)
+  const uint8_t* s0_img;  // S_{-1} images (one slot per head)
+  const uint8_t* u_img;   // U_t images (F slots)
+  const float* g;
+  const float* beta;
+  int gate_logits;
+  float* dbeta;
+  float* dg_part;  // [F][ntiles]
+  long long nitems;
+  int T, S, D, NA;
+  float ck;  // 1/sqrt(D*S)
+  unsigned int* status;
+};
+
+// Persistent CTAs over frame-heads; per frame-head the S_{t-1} and U_t images are
+// gathered once, then the tiles run one after another through a single K / V
+// slot: K tile -> (after the first MMAs) dP -> (after the second) dK staging;
+// V tile -> R in place; a third slot stages dV.
+__global__ void __launch_bounds__(kKvThreads, 1)
+    tc_kv_grad_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
+                      const __grid_constant__ CUtensorMap mapdK, const __grid_constant__ CUtensorMap mapdV, KvArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int NA = a.NA, D = a.D, S = a.S, T = a.T, KS = D / 16;
+  const int img_bytes = 2 * NA * D * 128;
+  const int img_stride = (img_bytes + 1023) & ~1023;
+  const int tile_bytes = NA * kKvTok * 128;
+  uint8_t* imgS = smem;
+  uint8_t* imgU = imgS + img_stride;
+  uint8_t* tK = imgU + img_stride;
+  uint8_t* tV = tK + tile_bytes;
+  uint8_t* tdV = tV + tile_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tdV + tile_bytes);
+  uint64_t* ifull = bars;
+  uint64_t* iempty = bars + 1;
+  uint64_t* kfull = bars + 2;
+  uint64_t* kempty = bars + 3;
+  uint64_t* mma1 = bars + 4;
+  uint64_t* epi1 = bars + 5;
+  uint64_t* mma2 = bars + 6;
+  uint64_t* mma_done = bars + 7;
+  float* red = reinterpret_cast<float*>(bars + 8);  // 4 per-warp partial sums
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(ifull), 1);
+    mbar_init(smem_u32(iempty), 1);
+    mbar_init(smem_u32(kfull), 1);
+    mbar_init(smem_u32(kempty), 4);
+    mbar_init(smem_u32(mma1), 1);
+    mbar_init(smem_u32(epi1), 4);
+    mbar_init(smem_u32(mma2), 1);
+    mbar_init(smem_u32(mma_done), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(tmem_slot), 256);  // P, later dK~ (columns 0-127); dR (128-255)
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int ntiles = (S + kKvTok - 1) / kKvTok;
+
+  if (warp == 4) {
+    // ---------------- copies in: the two images per frame-head, K and V per tile
+    if (lane == 0) {
+      prefetch_tmap(&mapK);
+      prefetch_tmap(&mapV);
+      Ring<1> ri, rk;
+      bool ok = true;
+      for (long long f = blockIdx.x; ok && f < a.nitems; f += gridDim.x) {
+        if (!wait_or_abort(smem_u32(iempty), ri.phase ^ 1, abort_flag, a.status)) break;
+        const int t = (int)(f % T);
+        const uint8_t* srcS = t > 0 ? a.s_img + (size_t)(f - 1) * img_bytes : a.s0_img + (size_t)(f / T) * img_bytes;
+        const uint8_t* srcU = a.u_img + (size_t)f * img_bytes;
+        const uint32_t ib = smem_u32(ifull);
+        mbar_arrive_expect_tx(ib, 2 * img_bytes);
+        // block cb of the scan = [atom][hi 16 rows | lo 16 rows][128 B]
+        for (int cb = 0; cb < D / 16; ++cb)
+          for (int at = 0; at < NA; ++at)
+            for (int hl = 0; hl < 2; ++hl) {
+              const size_t so = ((size_t)cb * NA + at) * (32 * 128) + hl * 16 * 128;
+              const uint32_t dof = (hl * NA + at) * D * 128 + cb * 16 * 128;
+              bulk_g2s(smem_u32(imgS + dof), srcS + so, 16 * 128, ib);
+              bulk_g2s(smem_u32(imgU + dof), srcU + so, 16 * 128, ib);
+            }
+        ri.mark_issued();
+        ri.advance();
+        for (int tile = 0; tile < ntiles; ++tile) {
+          if (!wait_or_abort(smem_u32(kempty), rk.phase ^ 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t kb = smem_u32(kfull);
+          mbar_arrive_expect_tx(kb, 2 * tile_bytes);
+          for (int at = 0; at < NA; ++at) {
+            tma_load_3d(smem_u32(tK + at * kKvTok * 128), &mapK, kb, 64 * at, tile * kKvTok, (int)f);
+            tma_load_3d(smem_u32(tV + at * kKvTok * 128), &mapV, kb, 64 * at, tile * kKvTok, (int)f);
+          }
+          rk.mark_issued();
+          rk.advance();
+        }
+      }
+      ri.drain(ifull);
+      rk.drain(kfull);
+    }
+  } else if (warp == 5) {
+    // ---------------- MMAs
+    if (lane == 0) {
+      const uint32_t idK = idesc_bf16(128, D, 0, 0);  // B = image, K-major (K = key dim)
+      const uint32_t idT = idesc_bf16(128, D, 0, 1);  // B = image, MN-major (K = value dim)
+      const uint32_t sS = smem_u32(imgS), sU = smem_u32(imgU), lo = NA * D * 128;
+      const uint32_t aK = smem_u32(tK), aV = smem_u32(tV);
+      uint32_t iph = 0, ph = 0;
+      for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+        if (!wait_or_abort(smem_u32(ifull), iph, abort_flag, a.status)) goto done;
+        for (int tile = 0; tile < ntiles; ++tile) {
+          if (!wait_or_abort(smem_u32(kfull), ph, abort_flag, a.status)) goto done;
+          tc_fence_after();
+          // P = K S_{t-1}, dR = K U_t (the key scale is applied in the epilogue)
+          for (int kk = 0; kk < KS; ++kk) {
+            const uint32_t ko = (kk >> 2) * (kKvTok * 128) + (kk & 3) * 32;
+            const uint32_t so = (kk >> 2) * (D * 128) + (kk & 3) * 32;
+            const uint64_t ad = smem_desc(aK + ko, 16, 1024);
+            mma_bf16(tmem, ad, smem_desc(sS + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem, ad, smem_desc(sS + lo + so, 16, 1024), idK, 1u);
+            mma_bf16(tmem + 128, ad, smem_desc(sU + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + 128, ad, smem_desc(sU + lo + so, 16, 1024), idK, 1u);
+          }
+          mma_commit(smem_u32(mma1));
+          if (!wait_or_abort(smem_u32(epi1), ph, abort_flag, a.status)) goto done;
+          tc_fence_after();
+          // dK~ (unscaled) = R U_t^T + dP S_{t-1}^T, into columns 0-127
+          for (int kk = 0; kk < KS; ++kk) {
+            const uint32_t ko = (kk >> 2) * (kKvTok * 128) + (kk & 3) * 32;
+            const uint32_t mo = kk * 2048;
+            const uint64_t ar = smem_desc(aV + ko, 16, 1024), ap = smem_desc(aK + ko, 16, 1024);
+            mma_bf16(tmem, ar, smem_desc(sU + mo, D * 128, 1024), idT, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem, ar, smem_desc(sU + lo + mo, D * 128, 1024), idT, 1u);
+            mma_bf16(tmem, ap, smem_desc(sS + mo, D * 128, 1024), idT, 1u);
+            mma_bf16(tmem, ap, smem_desc(sS + lo + mo, D * 128, 1024), idT, 1u);
+          }
+          mma_commit(smem_u32(mma2));
+          if (tile == ntiles - 1) mma_commit(smem_u32(iempty));
+          ph ^= 1;
+        }
+        iph ^= 1;
+      }
+    }
+  } else if (warp < 4) {
+    // ---------------- epilogue: thread = token row of the tile
+    const int row = warp * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    uint32_t iph = 0, ph = 0;
+    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+      const float gt = decay_of(__ldg(a.g + f), a.gate_logits);
+      for (int tile = 0; tile < ntiles; ++tile) {
+        const int s = tile * kKvTok + row;
+        const bool valid = s < S;
+        const float b = valid ? beta_of(__ldg(a.beta + f * S + s), a.gate_logits) : 0.f;
+        // the V tile (read here) has landed, and the first MMAs are done
+        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(kfull), ph, abort_flag, a.status) &&
+                                         wait_or_abort(smem_u32(mma1), ph, abort_flag, a.status)))
+          goto done;
+        tc_fence_after();
+        float part = 0.f;
+        if (tile == 0) {
+          // <U_t, S_{t-1}> over the images (positions past D excluded: never written)
+          if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(ifull), iph, abort_flag, a.status))) goto done;
+          const int nch = NA * D * 8;  // 16-byte chunks of one hi (or lo) image
+          for (int c = row; c < nch; c += 128) {
+            const int at = c / (D * 8), r = (c / 8) % D, pc = c % 8;
+            if (64 * at + 8 * (pc ^ (r & 7)) >= D) continue;
+            const uint32_t off = (uint32_t)c * 16;
+            const uint4 sh = *reinterpret_cast<const uint4*>(imgS + off);
+            const uint4 sl = *reinterpret_cast<const uint4*>(imgS + NA * D * 128 + off);
+            const uint4 uh = *reinterpret_cast<const uint4*>(imgU + off);
+            const uint4 ul = *reinterpret_cast<const uint4*>(imgU + NA * D * 128 + off);
+            const uint32_t w[4][4] = {{sh.x, sh.y, sh.z, sh.w}, {sl.x, sl.y, sl.z, sl.w},
+                                      {uh.x, uh.y, uh.z, uh.w}, {ul.x, ul.y, ul.z, ul.w}};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[0][e]));
+              const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[1][e]));
+              const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[2][e]));
+              const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[3][e]));
+              part = fmaf(a0.x + a1.x, b0.x + b1.x, part);
+              part = fmaf(a0.y + a1.y, b0.y + b1.y, part);
+            }
+          }
+        }
+        // element-wise stage, 16 value columns at a time
+        float db = 0.f, dgp = 0.f;
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          float pv[16], rv[16];
+          tmem_ld16(tmem + lane_base + c0, pv);
+          tmem_ld16(tmem + lane_base + 128 + c0, rv);
+          tmem_ld_wait();
+          const uint32_t ab = (c0 >> 6) * (kKvTok * 128);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t off = ab + sw128_off(row, (c0 & 63) + 8 * h);
+            const uint4 vv = *reinterpret_cast<const uint4*>(tV + off);
+            const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
+            uint32_t ro[4], po[4], vo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 v2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[e]));
+              const float p0 = a.ck * pv[8 * h + 2 * e], p1 = a.ck * pv[8 * h + 2 * e + 1];
+              const float d0 = a.ck * rv[8 * h + 2 * e], d1 = a.ck * rv[8 * h + 2 * e + 1];
+              const float r0 = v2.x - gt * p0, r1 = v2.y - gt * p1;
+              db = fmaf(d0, r0, fmaf(d1, r1, db));
+              dgp = fmaf(d0, p0, fmaf(d1, p1, dgp));
+              ro[e] = pack_bf16(b * r0, b * r1);
+              po[e] = pack_bf16(-gt * b * d0, -gt * b * d1);
+              vo[e] = pack_bf16(b * d0, b * d1);
+            }
+            *reinterpret_cast<uint4*>(tV + off) = make_uint4(ro[0], ro[1], ro[2], ro[3]);
+            *reinterpret_cast<uint4*>(tK + off) = make_uint4(po[0], po[1], po[2], po[3]);
+            *reinterpret_cast<uint4*>(tdV + off) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+          }
+        }
+        if (valid) a.dbeta[f * S + s] = a.gate_logits ? db * b * (1.f - b) : db;
+        part -= b * dgp;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (lane == 0) red[warp] = part;
+        tc_fence_before();
+        fence_proxy_async_smem();
+        named_barrier(1, 128);  // every row's R, dP, dV written; partial sums in `red`
+        if (threadIdx.x == 0) a.dg_part[f * ntiles + tile] = (red[0] + red[1]) + (red[2] + red[3]);
+        if (lane == 0) {
+          mbar_arrive(smem_u32(epi1));
+          for (int at = 0; at < NA; ++at)
+            tma_store_3d(&mapdV, smem_u32(tdV + at * (kKvTok * 128) + warp * 32 * 128), 64 * at,
+                         tile * kKvTok + warp * 32, (int)f);
+          bulk_commit();
+        }
+        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(mma2), ph, abort_flag, a.status))) goto done;
+        tc_fence_after();
+        // dK = dK~ / sqrt(D*S) -> bf16 into the K slot (dP has been consumed)
+        for (int c0 = 0; c0 < D; c0 += 16) {
+          float kv[16];
+          tmem_ld16(tmem + lane_base + c0, kv);
+          tmem_ld_wait();
+          const uint32_t ab = (c0 >> 6) * (kKvTok * 128);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint4 o;
+            o.x = pack_bf16(a.ck * kv[8 * h + 0], a.ck * kv[8 * h + 1]);
+            o.y = pack_bf16(a.ck * kv[8 * h + 2], a.ck * kv[8 * h + 3]);
+            o.z = pack_bf16(a.ck * kv[8 * h + 4], a.ck * kv[8 * h + 5]);
+            o.w = pack_bf16(a.ck * kv[8 * h + 6], a.ck * kv[8 * h + 7]);
+            *reinterpret_cast<uint4*>(tK + ab + sw128_off(row, (c0 & 63) + 8 * h)) = o;
+          }
+        }
+        tc_fence_before();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int at = 0; at < NA; ++at)
+            tma_store_3d(&mapdK, smem_u32(tK + at * (kKvTok * 128) + warp * 32 * 128), 64 * at,
+                         tile * kKvTok + warp * 32, (int)f);
+          bulk_commit();
+          bulk_wait_read0();  // this warp's dV and dK rows have left the K and dV slots
+          mbar_arrive(smem_u32(kempty));
+        }
+        __syncwarp();
+        ph ^= 1;
+      }
+      iph ^= 1;
+    }
+  }
+done:
+  if (warp < 4 && lane == 0) bulk_wait0();  // this warp's stores are complete
+  if (warp == 5 && lane == 0) {
+    mma_commit(smem_u32(mma_done));
+    wait_bounded(smem_u32(mma_done), 0, 500000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -909,6 +1285,7 @@ constexpr int kBarBytes = 256;
 int gram_smem(int NA, int D) {
   return kGramRaw * kRawStage + kGramConv * kConvStage + NA * D * 128 + kBarBytes + 1024;
 }
+int kv_smem(int NA, int D) { return 2 * ((2 * NA * D * 128 + 1023) & ~1023) + 3 * NA * kKvTok * 128 + kBarBytes + 1024; }
 int scan_smem() { return kScanStages * (kScanMStage + kScanBStage) + 2 * kScanImg + kBarBytes + 1024; }
 int out_smem(int NA, int D) {
   return 2 * ((2 * NA * D * 128 + 1023) & ~1023) + (kOutQStages + 1) * NA * kOutTok * 128 + kBarBytes + 1024;
@@ -973,6 +1350,123 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   return kOk;
+}
+
+
+// ---------------------------------------------------------------- backward pass
+namespace {
+
+struct TcBwdLayout {
+  size_t m_off, e_off, s_off, u_off, s0_off, dg_off, total;
+  size_t img_bytes;  // one S / U image slot
+  int ntiles;
+};
+
+TcBwdLayout tc_bwd_layout(const Problem& p) {
+  TcBwdLayout L{};
+  const int NA = num_atoms(p.D);
+  const size_t F = (size_t)p.BHT();
+  L.img_bytes = (size_t)2 * NA * p.D * 128;
+  L.ntiles = (p.S + kKvTok - 1) / kKvTok;
+  L.m_off = 0;
+  L.e_off = align_up(L.m_off + F * NA * p.D * 128, 1024);
+  L.s_off = align_up(L.e_off + F * p.D * p.D * 4, 1024);
+  L.u_off = align_up(L.s_off + F * L.img_bytes, 1024);
+  L.s0_off = align_up(L.u_off + F * L.img_bytes, 1024);
+  L.dg_off = align_up(L.s0_off + (size_t)p.BH() * L.img_bytes, 1024);
+  L.total = align_up(L.dg_off + F * L.ntiles * 4, 1024);
+  return L;
+}
+
+}  // namespace
+
+size_t tc_bwd_workspace_bytes(const Problem& p) { return tc_bwd_layout(p).total; }
+
+int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st) {
+  const TcBwdLayout L = tc_bwd_layout(p);
+  const int NA = num_atoms(p.D), D = p.D;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  uint8_t* m_img = w + L.m_off;
+  float* e_blk = reinterpret_cast<float*>(w + L.e_off);
+  uint8_t* s_img = w + L.s_off;
+  uint8_t* u_img = w + L.u_off;
+  uint8_t* s0_img = w + L.s0_off;
+  float* dg_part = reinterpret_cast<float*>(w + L.dg_off);
+  const long long F = p.BHT();
+  const int nsm = num_sms();
+  const unsigned pgrid = (unsigned)(F < nsm ? F : nsm);
+
+  CUtensorMap mapK, mapV, mapQ, mapDO, mapDO128, mapDQ, mapDK, mapDV;
+  if (!make_map(&mapK, p.k, D, p.S, F, kGramTok) || !make_map(&mapV, p.v, D, p.S, F, kGramTok) ||
+      !make_map(&mapQ, p.q, D, p.S, F, kGramTok) || !make_map(&mapDO, gr.dout, D, p.S, F, kGramTok) ||
+      !make_map(&mapDO128, gr.dout, D, p.S, F, kOutTok) || !make_map(&mapDQ, gr.dq, D, p.S, F, 32) ||
+      !make_map(&mapDK, gr.dk, D, p.S, F, 32) || !make_map(&mapDV, gr.dv, D, p.S, F, 32))
+    return kCuda;
+  CUtensorMap mapK128, mapV128;
+  if (!make_map(&mapK128, p.k, D, p.S, F, kKvTok) || !make_map(&mapV128, p.v, D, p.S, F, kKvTok)) return kCuda;
+
+  const int gsmem = gram_smem(NA, D);
+  if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gsmem) != cudaSuccess)
+    return kCuda;
+  const int ssmem = scan_smem();
+  if (cudaFuncSetAttribute(tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ssmem) != cudaSuccess)
+    return kCuda;
+  const unsigned sgrid = (unsigned)(p.BH() * (D / 16));
+
+  // forward states: M_t (image), b_t (into the E blocks), S_t (images)
+  {
+    GramArgs ga{p.beta, p.gate_logits, kGdn, m_img, e_blk, F, p.S, D, NA, p.key_scale * p.key_scale, p.key_scale,
+                p.status, 0};
+    ProfScope ps(st, "tc_gram");
+    tc_gram_kernel<<<pgrid, kGramThreads, gsmem, st>>>(mapK, mapV, ga);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  {
+    ScanArgs sa{m_img, e_blk, p.g, p.gate_logits, kGdn, p.state_in, s_img, nullptr, p.T, D, NA, p.status, 0};
+    ProfScope ps(st, "tc_scan");
+    tc_scan_kernel<<<sgrid, kScanThreads, ssmem, st>>>(sa);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  // E_t = Q_t^T dO_t / sqrt(D) (overwrites b_t, which the scan has consumed)
+  {
+    GramArgs ga{nullptr, 0, kGdn, nullptr, e_blk, F, p.S, D, NA, 0.f, p.out_scale, p.status, 1};
+    ProfScope ps(st, "tc_bwd_qdo");
+    tc_gram_kernel<<<pgrid, kGramThreads, gsmem, st>>>(mapQ, mapDO, ga);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  // U_t for every frame and dS_0, by the reverse scan
+  {
+    ScanArgs sa{m_img, e_blk, p.g, p.gate_logits, kGdn, gr.dstate_out, u_img, gr.dstate_in, p.T, D, NA, p.status, 1};
+    ProfScope ps(st, "tc_bwd_rscan");
+    tc_scan_kernel<<<sgrid, kScanThreads, ssmem, st>>>(sa);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  {
+    ProfScope ps(st, "tc_bwd_s0_image");
+    tc_state_image_kernel<<<dim3((unsigned)p.BH(), D / 16), 128, 0, st>>>(p.state_in, s0_img, D, NA);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  {
+    const int smem = kv_smem(NA, D);
+    if (cudaFuncSetAttribute(tc_kv_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return kCuda;
+    KvArgs ka{s_img, s0_img, u_img, p.g, p.beta, p.gate_logits, gr.dbeta, dg_part, F, p.T, p.S, D, NA,
+              p.key_scale, p.status};
+    ProfScope ps(st, "tc_bwd_kv_grad");
+    tc_kv_grad_kernel<<<pgrid, kKvThreads, smem, st>>>(mapK128, mapV128, mapDK, mapDV, ka);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  // dQ = dO S_t^T / sqrt(D)
+  {
+    const int smem = out_smem(NA, D);
+    if (cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return kCuda;
+    OutArgs oa{s_img, kGdn, static_cast<__nv_bfloat16*>(gr.dq), F, p.S, D, NA, p.out_scale, p.status, 1};
+    ProfScope ps(st, "tc_bwd_q_grad");
+    tc_readout_kernel<<<pgrid, kOutThreads, smem, st>>>(mapDO128, mapDQ, oa);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  return launch_dg_sum(dg_part, p.g, gr.dg, F, L.ntiles, p.gate_logits, st);
 }
 
 }  // namespace gdn

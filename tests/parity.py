@@ -90,19 +90,19 @@ def device_dout(wl, dev="cuda"):
 
 GRAD_KEYS = ("dq", "dk", "dv", "dg", "dbeta", "dstate_in")
 F32_GRAD_MAX_ABS_OVER_RMS = 1e-4
-F32_OUT_OF_BF16_CALL_MAX_ABS_OVER_RMS = 1e-3
 
 
 def assert_grad_parity(wl_dtype, gpu, ref, what=""):
     """Backward-pass bound, per gradient tensor.
 
-    float32 I/O: every gradient within 1e-4 x rms(oracle) (float32 arithmetic
-    from exact inputs: sums of up to ~1e5 products, typical relative error
-    ~sqrt(n) x 2^-24 ~ 2e-5).  bf16 I/O: dq, dk, dv are bf16 outputs and take the
-    forward's bf16 bound with the half-ulp allowance; dg, dbeta and dstate_in are
-    float32 outputs of float32 arithmetic on exact (bf16-valued) inputs and are held
-    to 1e-3 x rms -- far above float32 rounding, far below the effect of a dropped
-    or wrong term."""
+    float32 I/O (CUDA-core float32 arithmetic from exact inputs): every gradient
+    within 1e-4 x rms(oracle) -- sums of up to ~1e5 products, typical relative
+    error ~sqrt(n) x 2^-24 ~ 2e-5.
+    bf16 I/O (tensor cores): dq, dk, dv are bf16 outputs and take the forward's
+    bf16 bound for outputs with the half-ulp allowance.  dg, dbeta and dstate_in
+    are float32 outputs, but computed through bf16 operands (the M_t image, R and
+    dP rounded to bf16, the states and U split hi + lo): like the forward's final
+    state they take max |err| <= 2e-2 x rms and rms(err) <= 5e-3 x rms."""
     res = {}
     for key in GRAD_KEYS:
         if key not in gpu or gpu[key] is None:
@@ -115,11 +115,10 @@ def assert_grad_parity(wl_dtype, gpu, ref, what=""):
             continue
         if wl_dtype == "f32":
             assert e["max_abs_over_rms"] <= F32_GRAD_MAX_ABS_OVER_RMS, f"{what} {key}: {e}"
-        elif key in ("dq", "dk", "dv"):
-            assert e["max_beyond_half_ulp_over_rms"] <= BF16_MAX_ABS_OVER_RMS, f"{what} {key}: {e}"
-            assert e["rms_err_over_rms"] <= BF16_RMS_ERR_OVER_RMS, f"{what} {key}: {e}"
-        else:
-            assert e["max_abs_over_rms"] <= F32_OUT_OF_BF16_CALL_MAX_ABS_OVER_RMS, f"{what} {key}: {e}"
+            continue
+        key_max = "max_beyond_half_ulp_over_rms" if key in ("dq", "dk", "dv") else "max_abs_over_rms"
+        assert e[key_max] <= BF16_MAX_ABS_OVER_RMS, f"{what} {key}: {e}"
+        assert e["rms_err_over_rms"] <= BF16_RMS_ERR_OVER_RMS, f"{what} {key}: {e}"
     return res
 
 

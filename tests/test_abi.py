@@ -158,9 +158,12 @@ def test_backward_zero_frames_needs_no_gradient_outputs(lib):
 
 def test_backward_workspace_bytes(lib):
     a = binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 112, 1)
-    # four D x D float32 matrices per frame-head plus one float per 32-token tile
-    assert a >= 4 * 20 * 961 * 112 * 112 * 4 + 20 * 961 * 28 * 4
-    assert a == binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 112, 0)
+    f = binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 112, 0)
+    # float32 I/O: four D x D float32 matrices per frame-head plus one float per 32-token tile
+    assert f >= 4 * 20 * 961 * 112 * 112 * 4 + 20 * 961 * 28 * 4
+    # bf16 I/O: the M_t image, the E_t blocks and the S_t and U_t images (bf16 hi + lo)
+    assert a >= 20 * 961 * (2 * 112 * 128 + 112 * 112 * 4 + 2 * 4 * 112 * 128)
+    assert a == binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 112, 1)
     assert binding.gdn_bwd_workspace_bytes(1, 20, 0, 880, 112, 1) == 0
     assert binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 24, 1) == 0
     assert binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 112, 5) == 0

@@ -69,7 +69,8 @@ def test_backward_matches_oracle(case):
     got = _run_bwd(wl, x, gr["dout"], S0, dST)
     ref = oracle.frame_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, gr["dout"], dST)
     res = parity.assert_grad_parity(dt, got, ref, f"bwd {case}")
-    print(f"bwd {case}: " + ", ".join(f"{k} {v['max_abs_over_rms']:.2e}" for k, v in res.items()))
+    print(f"bwd {case}: " + ", ".join(f"{k} max {v['max_abs_over_rms']:.2e} rms {v['rms_err_over_rms']:.2e}"
+                                      for k, v in res.items()))
 
 
 @pytest.mark.parametrize("case", [("bf16", 1, 2, 5, 70, 48), ("f32", 1, 2, 4, 37, 32)],
@@ -148,4 +149,5 @@ def test_backward_minute_sampled_heads():
         ref["dstate_in"] = ref.pop("dS0")
         got = {key: np_(res[key][b, h]) for key in parity.GRAD_KEYS}
         r = parity.assert_grad_parity(wl.dtype, got, ref, f"minute bwd head {(b, h)}")
-        print(f"minute bwd head {(b, h)}: " + ", ".join(f"{k} {v['max_abs_over_rms']:.2e}" for k, v in r.items()))
+        print(f"minute bwd head {(b, h)}: " + ", ".join(
+            f"{k} max {v['max_abs_over_rms']:.2e} rms {v['rms_err_over_rms']:.2e}" for k, v in r.items()))
