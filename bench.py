@@ -9,6 +9,9 @@ the timed region starts and are larger than L2, so no flush is needed.
 
     python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
+``--backward`` times the backward pass instead (one gdn_frame_bwd call over the
+same workload: every gradient, states recomputed), on its own metric line.
+
 Under torchrun (N > 1) every rank runs its own full replica of the workload on
 its own GPU (weak scaling; the path needs no cross-GPU exchange), the ranks
 barrier around the timed region and the slowest rank's time is used.
@@ -34,6 +37,7 @@ sys.path.insert(0, ROOT)
 from linear_attention_video_gated_b300 import synth  # noqa: E402
 
 METRIC = "frame-GDN fwd tokens/s at 961f×880tok×20h×d112; % of roofline"
+METRIC_BWD = "frame-GDN bwd tokens/s at 961f×880tok×20h×d112; % of roofline"
 UNIT = "tokens/s"
 
 
@@ -50,6 +54,21 @@ def alg_flops(wl) -> int:
     return 6 * wl.B * wl.H * wl.T * wl.S * wl.D * wl.D
 
 
+def alg_bytes_bwd(wl) -> int:
+    """Backward: q, k, v and dout read once, dq, dk, dv written once, g and beta
+    read once, dg and dbeta written once, state_in and dstate_out read, dstate_in
+    written."""
+    n = wl.B * wl.H * wl.T * wl.S * wl.D
+    fh = wl.B * wl.H * wl.T
+    return 7 * n * wl.elem_bytes + 2 * 4 * fh * (1 + wl.S) + 3 * 4 * wl.B * wl.H * wl.D * wl.D
+
+
+def alg_flops_bwd(wl) -> int:
+    """Seven S x D x D contractions per frame-head: the states again (prediction,
+    write), Q^T dO, K~ U, the two halves of dK~, dO S^T."""
+    return 14 * wl.B * wl.H * wl.T * wl.S * wl.D * wl.D
+
+
 def kernel_alg_bytes(name: str, wl) -> int | None:
     """Algorithmic bytes each kernel is responsible for, per launch (one call).
 
@@ -60,8 +79,10 @@ def kernel_alg_bytes(name: str, wl) -> int | None:
     e = wl.elem_bytes
     if name.endswith("_gram"):
         return fh * (2 * wl.S * wl.D * e + 4 * wl.S + 4)
-    if name.endswith("_readout"):
-        return fh * 2 * wl.S * wl.D * e
+    if name.endswith("_readout") or name.endswith("_q_grad") or name.endswith("_qdo"):
+        return fh * 2 * wl.S * wl.D * e  # q in, out out / dout in, dq out / q and dout in
+    if name.endswith("_kv_grad"):
+        return fh * (4 * wl.S * wl.D * e + 8 * wl.S + 4)  # k, v, beta, g in; dk, dv, dbeta out
     if "_fused" in name:
         return alg_bytes(wl)
     return None
@@ -169,9 +190,11 @@ def bus_id(dev) -> str | None:
 
 # ----------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample(wl, budget_s: float, max_heads: int | None = None, frames: int | None = None):
-    """Times the fp64 oracle on whole heads of the workload until `budget_s` of CPU
-    work.  Returns (equivalent tokens/s, cores, sample description, seconds)."""
+def oracle_sample(wl, budget_s: float, max_heads: int | None = None, frames: int | None = None,
+                  backward: bool = False):
+    """Times the fp64 oracle (its backward pass with ``backward``) on whole heads of
+    the workload until `budget_s` of CPU work.  Returns (equivalent tokens/s,
+    cores, sample description, seconds)."""
     import contextlib
 
     import oracle
@@ -194,14 +217,19 @@ def oracle_sample(wl, budget_s: float, max_heads: int | None = None, frames: int
             _fill_head(wl, b, h, hq, hk, hv, hg, hb)
             cvt = (lambda a: synth.bf16_to_f32(a[0, 0])) if wl.dtype == "bf16" else (lambda a: a[0, 0])
             q, k, v = cvt(hq), cvt(hk), cvt(hv)
-            t0 = time.perf_counter()
-            oracle.scan_head(q, k, v, hg[0, 0], hb[0, 0])
+            if backward:
+                do = synth.head_dout(wl, b, h, 0, T)
+                t0 = time.perf_counter()
+                oracle.backward_head(q, k, v, hg[0, 0], hb[0, 0], None, do)
+            else:
+                t0 = time.perf_counter()
+                oracle.scan_head(q, k, v, hg[0, 0], hb[0, 0])
             spent += time.perf_counter() - t0
             n += 1
             del one
     tokens = n * T * wl.S / wl.H  # a token of the workload spans all H heads
     desc = (f"{n} of {wl.B * wl.H} heads x {T} of {wl.T} frames x {wl.S} tokens (d{wl.D}) of the {wl.name} "
-            f"workload, numpy fp64; tokens counted as heads/{wl.H}")
+            f"workload, numpy fp64{' backward pass' if backward else ''}; tokens counted as heads/{wl.H}")
     return tokens / spent, cores, desc, spent
 
 
@@ -222,15 +250,18 @@ def _fill_head(wl, b, h, hq, hk, hv, hg, hb):
 
 # ----------------------------------------------------------------- arms
 
-def config_of(wl, mode, gate_logits=False, relu_linear=False) -> dict:
+def config_of(wl, mode, gate_logits=False, relu_linear=False, backward=False) -> dict:
     gates = ", gates from logits (fused gate prologue)" if gate_logits else ""
     if relu_linear:
         gates = ", cumulative ReLU linear attention baseline (no decay, no delta rule)"
+    if backward:
+        gates += ", BACKWARD pass (gdn_frame_bwd: every gradient, states recomputed)"
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} T={wl.T} S={wl.S} D={wl.D} {wl.dtype} I/O, fp32 state, "
                         f"single call over all frames{gates}",
             "B": wl.B, "H": wl.H, "T": wl.T, "S": wl.S, "D": wl.D,
-            "mode": {0: "sequential", 1: "prefix", 2: "split", 3: "cluster"}[mode],
-            "l2": f"no flush: inputs larger than L2 ({alg_bytes(wl) / 1e9:.1f} GB moved per step vs 126 MB L2)"}
+            "mode": "backward" if backward else {0: "sequential", 1: "prefix", 2: "split", 3: "cluster"}[mode],
+            "l2": f"no flush: inputs larger than L2 "
+                  f"({(alg_bytes_bwd(wl) if backward else alg_bytes(wl)) / 1e9:.1f} GB moved per step vs 126 MB L2)"}
 
 
 def reference_arm(args, rank, world):
@@ -241,15 +272,15 @@ def reference_arm(args, rank, world):
     times = []
     cores = len(os.sched_getaffinity(0))
     for i in range(args.warmup + args.steps):
-        v, cores, desc, spent = oracle_sample(wl, 0.0, max_heads=1, frames=frames)
+        v, cores, desc, spent = oracle_sample(wl, 0.0, max_heads=1, frames=frames, backward=args.backward)
         if i >= args.warmup:
             times.append(spent)
     ms = 1e3 * float(np.mean(times))
     value = (frames * wl.S / wl.H) / (ms / 1e3)
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": config_of(wl, args.mode),
+    line = {"impl": "reference", "metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl, args.mode, backward=args.backward),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -288,15 +319,30 @@ def ours_arm(args, rank, world, local_rank):
     sp = stream.cuda_stream
 
     entry = binding.gdn_frame_fwd_from_logits if args.gate_logits else binding.gdn_frame_fwd_ex
+    if args.backward:
+        hdo = torch.empty(shape, dtype=hdt, pin_memory=True)
+        synth.fill_dout(wl, hdo.numpy())
+        dout = (hdo.view(torch.bfloat16) if wl.dtype == "bf16" else hdo).to(dev)
+        grads = [torch.empty(shape, dtype=tdt, device=dev) for _ in range(3)]
+        dg = torch.empty((wl.B, wl.H, wl.T), dtype=torch.float32, device=dev)
+        dbeta = torch.empty((wl.B, wl.H, wl.T, wl.S), dtype=torch.float32, device=dev)
+        need = binding.gdn_bwd_workspace_bytes(wl.B, wl.H, wl.T, wl.S, wl.D, dtype)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        bentry = binding.gdn_frame_bwd_from_logits if args.gate_logits else binding.gdn_frame_bwd
 
-    def step(qq=q, kk=k, vv=v, gg=g, bb=beta, oo=out, so=st_out):
-        if args.relu_linear:
-            rc = binding.gdn_relu_linear_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), None, oo.data_ptr(),
+    def step(qq=q, kk=k, vv=v, gg=g, bb=beta, so=st_out):
+        if args.backward:
+            rc = bentry(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), gg.data_ptr(), bb.data_ptr(), None,
+                        dout.data_ptr(), None, grads[0].data_ptr(), grads[1].data_ptr(), grads[2].data_ptr(),
+                        dg.data_ptr(), dbeta.data_ptr(), so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype,
+                        ws.data_ptr(), need, sp)
+        elif args.relu_linear:
+            rc = binding.gdn_relu_linear_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), None, out.data_ptr(),
                                              so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype, mode,
                                              ws.data_ptr(), need, sp)
         else:
             rc = entry(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), gg.data_ptr(), bb.data_ptr(),
-                       None, oo.data_ptr(), so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype,
+                       None, out.data_ptr(), so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype,
                        mode, ws.data_ptr(), need, sp)
         if rc != 0:
             raise binding.GDNError(rc, "gdn_frame_fwd_ex")
@@ -355,12 +401,12 @@ def ours_arm(args, rank, world, local_rank):
                     "frac": ach / pk["hbm_gbs"], "traffic": traffic, "alg_bytes_per_launch": ab,
                     "avg_launch_ms": avg, "peak_source": f"{pk['source']} (MEASURED_PEAKS.json hbm_gbs)"
                     if pk["source"] == "measured" else "fallback 6.4 TB/s"}
-    call_gbs = alg_bytes(wl) / (ms / 1e3) / 1e9
+    call_gbs = (alg_bytes_bwd(wl) if args.backward else alg_bytes(wl)) / (ms / 1e3) / 1e9
 
     # end to end through the C ABI from pinned host buffers: gdn_frame_fwd_host,
     # which overlaps the copies of one chunk of frames with the kernels of another
     e2e = None
-    if not args.no_e2e and not args.gate_logits and not args.relu_linear:
+    if not args.no_e2e and not args.gate_logits and not args.relu_linear and not args.backward:
         ho = torch.empty(shape, dtype=tdt, pin_memory=True)
         hs = torch.empty((wl.B, wl.H, wl.D, wl.D), dtype=torch.float32, pin_memory=True)
         n_e2e = max(2, min(args.steps, args.e2e_steps))
@@ -396,17 +442,18 @@ def ours_arm(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        v_, cores, desc, spent = oracle_sample(wl, args.cpu_seconds)
+        v_, cores, desc, spent = oracle_sample(wl, args.cpu_seconds, frames=240 if args.backward else None,
+                                               backward=args.backward)
         cpu = {"value": v_, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "seconds": spent}
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-                "config": config_of(wl, mode, args.gate_logits, args.relu_linear),
+        line = {"metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+                "config": config_of(wl, mode, args.gate_logits, args.relu_linear, args.backward),
                 "roofline_pct": 100.0 * call_gbs / pk["hbm_gbs"],
                 "call_achieved_gbs": call_gbs,
-                "tflops": alg_flops(wl) / (ms / 1e3) / 1e12,
+                "tflops": (alg_flops_bwd(wl) if args.backward else alg_flops(wl)) / (ms / 1e3) / 1e12,
                 "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
                 "gpu_launches": int(sum(n for n, _ in kstats.values())),
                 "kernels": {k_: {"launches": n, "avg_ms": t / n} for k_, (n, t) in kstats.items()}}
@@ -427,6 +474,8 @@ def main():
                     help="pass g and beta as logits (gdn_frame_fwd_from_logits)")
     ap.add_argument("--relu-linear", action="store_true",
                     help="time the cumulative ReLU linear attention baseline (gdn_relu_linear_fwd)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass (gdn_frame_bwd) instead of the forward scan")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-chunk", type=int, default=32, help="frames per chunk of the host-buffer entry point")

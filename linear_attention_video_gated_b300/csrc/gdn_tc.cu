@@ -971,7 +971,7 @@ __global__ void __launch_bounds__(128) tc_state_image_kernel(const float* __rest
 }
 
 constexpr int kKvTok = 128;      // tokens per tile (MMA M)
-constexpr int kKvThreads = 192;  // 4 epilogue, 1 copy, 1 MMA warps
+constexpr int kKvThreads = 448;  // 8 element-wise warps, 4 dK warps, 1 copy warp, 1 MMA warp
 
 struct KvArgs {
   const uint8_t* s_img;   // S_t images (F slots, the scan's block layout)
@@ -979,7 +979,11 @@ struct KvArgs {
   const uint8_t* u_img;   // U_t images (F slots)
   const float* g;
   const float* beta;
+  const __nv_bfloat16* k;  // K and V themselves (L2 prefetches of coming tiles)
+  const __nv_bfloat16* v;
   int gate_logits;
+  __nv_bfloat16* dk;
+  __nv_bfloat16* dv;
   float* dbeta;
   float* dg_part;  // [F][ntiles]
   long long nitems;
@@ -988,52 +992,72 @@ struct KvArgs {
   unsigned int* status;
 };
 
-// Persistent CTAs over frame-heads; per frame-head the S_{t-1} and U_t images are
-// gathered once, then the tiles run one after another through a single K / V
-// slot: K tile -> (after the first MMAs) dP -> (after the second) dK staging;
-// V tile -> R in place; a third slot stages dV.
+// Persistent CTAs over frame-heads.  Per frame-head the S_{t-1} and U_t images
+// (bf16 hi + lo) are gathered once; then its 128-token tiles run through a
+// software pipeline:
+//   tensor core : P_b = K S_{t-1}, dR_b = K U_t for tile n (TMEM buffer b = n % 2,
+//                 hi and lo parts accumulated) issued before tile n - 1's
+//                 dK~ = R U_t^T + dP S_{t-1}^T (into tile n - 1's P buffer), so
+//                 the first MMAs of a tile overlap the element-wise stage of the
+//                 one before;
+//   warps 0-7   : the element-wise stage (two warps per TMEM lane quadrant,
+//                 alternate 16-column chunks): R over V in place, dP, dV, dbeta,
+//                 the dg partial sums;
+//   warps 8-11  : dK~ out of TMEM, scaled, to global memory;
+//   warp 12     : copies in, one slot each for K, V (then R) and dP.
+// dK and dV go to global memory straight from registers (one token row per thread).
 __global__ void __launch_bounds__(kKvThreads, 1)
-    tc_kv_grad_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV,
-                      const __grid_constant__ CUtensorMap mapdK, const __grid_constant__ CUtensorMap mapdV, KvArgs a) {
+    tc_kv_grad_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV, KvArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int NA = a.NA, D = a.D, S = a.S, T = a.T, KS = D / 16;
-  const int img_bytes = 2 * NA * D * 128;
-  const int img_stride = (img_bytes + 1023) & ~1023;
+  const int img_bytes = 2 * NA * D * 128;  // one image: hi, then lo (a multiple of 1024)
+  const int lo = NA * D * 128;             // offset of the lo part
   const int tile_bytes = NA * kKvTok * 128;
   uint8_t* imgS = smem;
-  uint8_t* imgU = imgS + img_stride;
-  uint8_t* tK = imgU + img_stride;
+  uint8_t* imgU = imgS + img_bytes;
+  uint8_t* tK = imgU + img_bytes;
   uint8_t* tV = tK + tile_bytes;
-  uint8_t* tdV = tV + tile_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tdV + tile_bytes);
+  uint8_t* tP = tV + tile_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tP + tile_bytes);
   uint64_t* ifull = bars;
   uint64_t* iempty = bars + 1;
   uint64_t* kfull = bars + 2;
   uint64_t* kempty = bars + 3;
-  uint64_t* mma1 = bars + 4;
-  uint64_t* epi1 = bars + 5;
-  uint64_t* mma2 = bars + 6;
-  uint64_t* mma_done = bars + 7;
-  float* red = reinterpret_cast<float*>(bars + 8);  // 4 per-warp partial sums
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(red + 4);
+  uint64_t* vfull = bars + 4;
+  uint64_t* vempty = bars + 5;   // V slot free: the tile's MMA2 has read R (and dP)
+  uint64_t* mma1 = bars + 8;     // [2] per TMEM buffer
+  uint64_t* mma2 = bars + 10;    // [2] per TMEM buffer
+  uint64_t* dkfree = bars + 12;  // [2] the dK warps have read that buffer's dK~
+  uint64_t* epi1 = bars + 14;
+  uint64_t* mma_done = bars + 15;
+  // per tile parity (a warp can start tile n + 1 while others still read tile n's):
+  float* red = reinterpret_cast<float*>(bars + 16);  // [2][8] per-warp partial sums of dg
+  float* dbh = red + 2 * 8;                          // [2][128] dbeta halves of the odd-chunk warps
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dbh + 2 * kKvTok);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
+  constexpr int wcopy = 12, wmma = 13;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(ifull), 1);
     mbar_init(smem_u32(iempty), 1);
     mbar_init(smem_u32(kfull), 1);
-    mbar_init(smem_u32(kempty), 4);
-    mbar_init(smem_u32(mma1), 1);
-    mbar_init(smem_u32(epi1), 4);
-    mbar_init(smem_u32(mma2), 1);
+    mbar_init(smem_u32(kempty), 1);
+    mbar_init(smem_u32(vfull), 1);
+    mbar_init(smem_u32(vempty), 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&mma1[b]), 1);
+      mbar_init(smem_u32(&mma2[b]), 1);
+      mbar_init(smem_u32(&dkfree[b]), 4);
+    }
+    mbar_init(smem_u32(epi1), 8);
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
-    tmem_alloc(smem_u32(tmem_slot), 256);  // P, later dK~ (columns 0-127); dR (128-255)
+  if (warp == wmma) {
+    tmem_alloc(smem_u32(tmem_slot), 512);  // buffer b: P (256b + 0..127, later dK~), dR (256b + 128..255)
     tmem_relinquish();
   }
   tc_fence_before();
@@ -1042,121 +1066,186 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const int ntiles = (S + kKvTok - 1) / kKvTok;
 
-  if (warp == 4) {
-    // ---------------- copies in: the two images per frame-head, K and V per tile
+  if (warp == wcopy) {
+    // ---------------- copies in
     if (lane == 0) {
       prefetch_tmap(&mapK);
       prefetch_tmap(&mapV);
-      Ring<1> ri, rk;
+      Ring<1> ri, rk, rv;
       bool ok = true;
       for (long long f = blockIdx.x; ok && f < a.nitems; f += gridDim.x) {
-        if (!wait_or_abort(smem_u32(iempty), ri.phase ^ 1, abort_flag, a.status)) break;
-        const int t = (int)(f % T);
-        const uint8_t* srcS = t > 0 ? a.s_img + (size_t)(f - 1) * img_bytes : a.s0_img + (size_t)(f / T) * img_bytes;
-        const uint8_t* srcU = a.u_img + (size_t)f * img_bytes;
-        const uint32_t ib = smem_u32(ifull);
-        mbar_arrive_expect_tx(ib, 2 * img_bytes);
-        // block cb of the scan = [atom][hi 16 rows | lo 16 rows][128 B]
-        for (int cb = 0; cb < D / 16; ++cb)
-          for (int at = 0; at < NA; ++at)
-            for (int hl = 0; hl < 2; ++hl) {
-              const size_t so = ((size_t)cb * NA + at) * (32 * 128) + hl * 16 * 128;
-              const uint32_t dof = (hl * NA + at) * D * 128 + cb * 16 * 128;
-              bulk_g2s(smem_u32(imgS + dof), srcS + so, 16 * 128, ib);
-              bulk_g2s(smem_u32(imgU + dof), srcU + so, 16 * 128, ib);
-            }
-        ri.mark_issued();
-        ri.advance();
-        for (int tile = 0; tile < ntiles; ++tile) {
+        for (int tile = 0; ok && tile < ntiles; ++tile) {
           if (!wait_or_abort(smem_u32(kempty), rk.phase ^ 1, abort_flag, a.status)) {
             ok = false;
             break;
           }
           const uint32_t kb = smem_u32(kfull);
-          mbar_arrive_expect_tx(kb, 2 * tile_bytes);
-          for (int at = 0; at < NA; ++at) {
+          mbar_arrive_expect_tx(kb, tile_bytes);
+          for (int at = 0; at < NA; ++at)
             tma_load_3d(smem_u32(tK + at * kKvTok * 128), &mapK, kb, 64 * at, tile * kKvTok, (int)f);
-            tma_load_3d(smem_u32(tV + at * kKvTok * 128), &mapV, kb, 64 * at, tile * kKvTok, (int)f);
-          }
           rk.mark_issued();
           rk.advance();
+          {  // into L2: this tile's V rows and the next tile's K rows (contiguous in memory)
+            const int rows = min(kKvTok, S - tile * kKvTok);
+            prefetch_l2(a.v + ((size_t)f * S + (size_t)tile * kKvTok) * D, (uint32_t)rows * D * 2);
+            const bool last = tile + 1 == ntiles;
+            const long long fn = last ? f + gridDim.x : f;
+            const int tn = last ? 0 : tile + 1;
+            if (fn < a.nitems)
+              prefetch_l2(a.k + ((size_t)fn * S + (size_t)tn * kKvTok) * D,
+                          (uint32_t)min(kKvTok, S - tn * kKvTok) * D * 2);
+          }
+          if (tile == 0) {  // the frame-head's images, once the previous one's last MMAs are done
+            if (!wait_or_abort(smem_u32(iempty), ri.phase ^ 1, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            const int t = (int)(f % T);
+            const uint8_t* srcS =
+                t > 0 ? a.s_img + (size_t)(f - 1) * img_bytes : a.s0_img + (size_t)(f / T) * img_bytes;
+            const uint8_t* srcU = a.u_img + (size_t)f * img_bytes;
+            const uint32_t ib = smem_u32(ifull);
+            mbar_arrive_expect_tx(ib, 2 * img_bytes);
+            // block cb of the scan = [atom][hi 16 rows | lo 16 rows][128 B]
+            for (int cb = 0; cb < D / 16; ++cb)
+              for (int at = 0; at < NA; ++at)
+                for (int hl = 0; hl < 2; ++hl) {
+                  const size_t so = ((size_t)cb * NA + at) * (32 * 128) + hl * 16 * 128;
+                  const uint32_t dof = hl * lo + at * D * 128 + cb * 16 * 128;
+                  bulk_g2s(smem_u32(imgS + dof), srcS + so, 16 * 128, ib);
+                  bulk_g2s(smem_u32(imgU + dof), srcU + so, 16 * 128, ib);
+                }
+            ri.mark_issued();
+            ri.advance();
+            const long long fn = f + gridDim.x;  // the next frame-head's images, into L2
+            if (fn < a.nitems) {
+              const int tn = (int)(fn % T);
+              prefetch_l2(tn > 0 ? a.s_img + (size_t)(fn - 1) * img_bytes : a.s0_img + (size_t)(fn / T) * img_bytes,
+                          (uint32_t)img_bytes);
+              prefetch_l2(a.u_img + (size_t)fn * img_bytes, (uint32_t)img_bytes);
+            }
+          }
+          if (!wait_or_abort(smem_u32(vempty), rv.phase ^ 1, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          const uint32_t vb = smem_u32(vfull);
+          mbar_arrive_expect_tx(vb, tile_bytes);
+          for (int at = 0; at < NA; ++at)
+            tma_load_3d(smem_u32(tV + at * kKvTok * 128), &mapV, vb, 64 * at, tile * kKvTok, (int)f);
+          rv.mark_issued();
+          rv.advance();
         }
       }
       ri.drain(ifull);
       rk.drain(kfull);
+      rv.drain(vfull);
     }
-  } else if (warp == 5) {
-    // ---------------- MMAs
+  } else if (warp == wmma) {
+    // ---------------- MMAs, software-pipelined: MMA1(n) goes out before MMA2(n - 1)
+    // (except at a frame-head boundary, where MMA2 of the previous head's last tile
+    // must finish before the new images may land)
     if (lane == 0) {
       const uint32_t idK = idesc_bf16(128, D, 0, 0);  // B = image, K-major (K = key dim)
       const uint32_t idT = idesc_bf16(128, D, 0, 1);  // B = image, MN-major (K = value dim)
-      const uint32_t sS = smem_u32(imgS), sU = smem_u32(imgU), lo = NA * D * 128;
-      const uint32_t aK = smem_u32(tK), aV = smem_u32(tV);
-      uint32_t iph = 0, ph = 0;
+      const uint32_t sS = smem_u32(imgS), sU = smem_u32(imgU);
+      const uint32_t aK = smem_u32(tK), aV = smem_u32(tV), aP = smem_u32(tP);
+      long long n = 0;        // tiles of this CTA so far
+      bool pending = false;   // tile n - 1 still needs its MMA2
+      bool pend_last = false;  // ... and it is its frame-head's last tile
+      uint32_t iph = 0;
+      // MMA2 of tile m: dK~ = R U^T + dP S^T into the P columns of buffer m % 2
+      auto mma2_of = [&](long long m, bool last_of_item) -> bool {
+        if (!wait_or_abort(smem_u32(epi1), (uint32_t)(m & 1), abort_flag, a.status)) return false;
+        tc_fence_after();
+        const int bm = (int)(m & 1);
+        const uint32_t acc = tmem + 256 * bm;
+        for (int kk = 0; kk < KS; ++kk) {
+          const uint32_t ko = (kk >> 2) * (kKvTok * 128) + (kk & 3) * 32;
+          const uint32_t mo = kk * 2048;
+          const uint64_t ar = smem_desc(aV + ko, 16, 1024), ap = smem_desc(aP + ko, 16, 1024);
+          mma_bf16(acc, ar, smem_desc(sU + mo, D * 128, 1024), idT, kk > 0 ? 1u : 0u);
+          mma_bf16(acc, ar, smem_desc(sU + lo + mo, D * 128, 1024), idT, 1u);
+          mma_bf16(acc, ap, smem_desc(sS + mo, D * 128, 1024), idT, 1u);
+          mma_bf16(acc, ap, smem_desc(sS + lo + mo, D * 128, 1024), idT, 1u);
+        }
+        mma_commit(smem_u32(&mma2[bm]));
+        mma_commit(smem_u32(vempty));
+        if (last_of_item) mma_commit(smem_u32(iempty));
+        return true;
+      };
       for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
-        if (!wait_or_abort(smem_u32(ifull), iph, abort_flag, a.status)) goto done;
-        for (int tile = 0; tile < ntiles; ++tile) {
-          if (!wait_or_abort(smem_u32(kfull), ph, abort_flag, a.status)) goto done;
+        for (int tile = 0; tile < ntiles; ++tile, ++n) {
+          const int b = (int)(n & 1);
+          const uint32_t bph = (uint32_t)((n >> 1) & 1);
+          if (!wait_or_abort(smem_u32(kfull), (uint32_t)(n & 1), abort_flag, a.status)) goto done;
+          if (tile == 0) {
+            if (pending && !mma2_of(n - 1, pend_last)) goto done;
+            pending = false;
+            if (!wait_or_abort(smem_u32(ifull), iph, abort_flag, a.status)) goto done;
+            iph ^= 1;
+          }
+          // buffer b was last used by tile n - 2: its dK~ must have been read out
+          if (!wait_or_abort(smem_u32(&dkfree[b]), bph ^ 1, abort_flag, a.status)) goto done;
           tc_fence_after();
-          // P = K S_{t-1}, dR = K U_t (the key scale is applied in the epilogue)
+          // P = K S_{t-1}, dR = K U_t (the key scale is applied by the element-wise warps)
           for (int kk = 0; kk < KS; ++kk) {
             const uint32_t ko = (kk >> 2) * (kKvTok * 128) + (kk & 3) * 32;
             const uint32_t so = (kk >> 2) * (D * 128) + (kk & 3) * 32;
             const uint64_t ad = smem_desc(aK + ko, 16, 1024);
-            mma_bf16(tmem, ad, smem_desc(sS + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
-            mma_bf16(tmem, ad, smem_desc(sS + lo + so, 16, 1024), idK, 1u);
-            mma_bf16(tmem + 128, ad, smem_desc(sU + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
-            mma_bf16(tmem + 128, ad, smem_desc(sU + lo + so, 16, 1024), idK, 1u);
+            mma_bf16(tmem + 256 * b, ad, smem_desc(sS + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + 256 * b, ad, smem_desc(sS + lo + so, 16, 1024), idK, 1u);
+            mma_bf16(tmem + 256 * b + 128, ad, smem_desc(sU + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + 256 * b + 128, ad, smem_desc(sU + lo + so, 16, 1024), idK, 1u);
           }
-          mma_commit(smem_u32(mma1));
-          if (!wait_or_abort(smem_u32(epi1), ph, abort_flag, a.status)) goto done;
-          tc_fence_after();
-          // dK~ (unscaled) = R U_t^T + dP S_{t-1}^T, into columns 0-127
-          for (int kk = 0; kk < KS; ++kk) {
-            const uint32_t ko = (kk >> 2) * (kKvTok * 128) + (kk & 3) * 32;
-            const uint32_t mo = kk * 2048;
-            const uint64_t ar = smem_desc(aV + ko, 16, 1024), ap = smem_desc(aK + ko, 16, 1024);
-            mma_bf16(tmem, ar, smem_desc(sU + mo, D * 128, 1024), idT, kk > 0 ? 1u : 0u);
-            mma_bf16(tmem, ar, smem_desc(sU + lo + mo, D * 128, 1024), idT, 1u);
-            mma_bf16(tmem, ap, smem_desc(sS + mo, D * 128, 1024), idT, 1u);
-            mma_bf16(tmem, ap, smem_desc(sS + lo + mo, D * 128, 1024), idT, 1u);
-          }
-          mma_commit(smem_u32(mma2));
-          if (tile == ntiles - 1) mma_commit(smem_u32(iempty));
-          ph ^= 1;
+          mma_commit(smem_u32(&mma1[b]));
+          mma_commit(smem_u32(kempty));
+          if (pending && !mma2_of(n - 1, pend_last)) goto done;
+          pending = true;
+          pend_last = tile == ntiles - 1;
         }
-        iph ^= 1;
       }
+      if (pending && !mma2_of(n - 1, pend_last)) goto done;
     }
-  } else if (warp < 4) {
-    // ---------------- epilogue: thread = token row of the tile
-    const int row = warp * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    uint32_t iph = 0, ph = 0;
+  } else if (warp < 8) {
+    // ---------------- element-wise stage: warp w owns token rows 32 (w % 4) .. + 31
+    // (its TMEM lane quadrant) and the 16-column chunks c with c % 2 == w / 4
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = quad * 32 + lane;
+    const int et = threadIdx.x;  // 0 .. 255
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    long long n = 0;
+    uint32_t iph = 0;
     for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
       const float gt = decay_of(__ldg(a.g + f), a.gate_logits);
-      for (int tile = 0; tile < ntiles; ++tile) {
+      for (int tile = 0; tile < ntiles; ++tile, ++n) {
+        const int b = (int)(n & 1);
+        const uint32_t bph = (uint32_t)((n >> 1) & 1);
         const int s = tile * kKvTok + row;
         const bool valid = s < S;
-        const float b = valid ? beta_of(__ldg(a.beta + f * S + s), a.gate_logits) : 0.f;
-        // the V tile (read here) has landed, and the first MMAs are done
-        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(kfull), ph, abort_flag, a.status) &&
-                                         wait_or_abort(smem_u32(mma1), ph, abort_flag, a.status)))
+        const float bt = valid ? beta_of(__ldg(a.beta + f * S + s), a.gate_logits) : 0.f;
+        __nv_bfloat16* dvrow = a.dv + (f * S + s) * D;
+        // this tile's V (loaded once the previous tile's MMA2 had read the V and
+        // dP slots) and its first MMAs
+        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(vfull), (uint32_t)(n & 1), abort_flag, a.status) &&
+                                         wait_or_abort(smem_u32(&mma1[b]), bph, abort_flag, a.status)))
           goto done;
         tc_fence_after();
+        uint8_t* vslot = tV;
+        uint8_t* pslot = tP;
         float part = 0.f;
         if (tile == 0) {
           // <U_t, S_{t-1}> over the images (positions past D excluded: never written)
           if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(ifull), iph, abort_flag, a.status))) goto done;
-          const int nch = NA * D * 8;  // 16-byte chunks of one hi (or lo) image
-          for (int c = row; c < nch; c += 128) {
+          const int nch = NA * D * 8;  // 16-byte chunks of one hi (or lo) part
+          for (int c = et; c < nch; c += 256) {
             const int at = c / (D * 8), r = (c / 8) % D, pc = c % 8;
             if (64 * at + 8 * (pc ^ (r & 7)) >= D) continue;
             const uint32_t off = (uint32_t)c * 16;
             const uint4 sh = *reinterpret_cast<const uint4*>(imgS + off);
-            const uint4 sl = *reinterpret_cast<const uint4*>(imgS + NA * D * 128 + off);
+            const uint4 sl = *reinterpret_cast<const uint4*>(imgS + lo + off);
             const uint4 uh = *reinterpret_cast<const uint4*>(imgU + off);
-            const uint4 ul = *reinterpret_cast<const uint4*>(imgU + NA * D * 128 + off);
+            const uint4 ul = *reinterpret_cast<const uint4*>(imgU + lo + off);
             const uint32_t w[4][4] = {{sh.x, sh.y, sh.z, sh.w}, {sl.x, sl.y, sl.z, sl.w},
                                       {uh.x, uh.y, uh.z, uh.w}, {ul.x, ul.y, ul.z, ul.w}};
 #pragma unroll
@@ -1169,19 +1258,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               part = fmaf(a0.y + a1.y, b0.y + b1.y, part);
             }
           }
+          iph ^= 1;
         }
-        // element-wise stage, 16 value columns at a time
         float db = 0.f, dgp = 0.f;
-        for (int c0 = 0; c0 < D; c0 += 16) {
+        for (int c0 = 16 * half; c0 < D; c0 += 32) {
           float pv[16], rv[16];
-          tmem_ld16(tmem + lane_base + c0, pv);
-          tmem_ld16(tmem + lane_base + 128 + c0, rv);
+          tmem_ld16(tmem + lane_base + 256 * b + c0, pv);
+          tmem_ld16(tmem + lane_base + 256 * b + 128 + c0, rv);
           tmem_ld_wait();
           const uint32_t ab = (c0 >> 6) * (kKvTok * 128);
+          uint4 dvo[2];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             const uint32_t off = ab + sw128_off(row, (c0 & 63) + 8 * h);
-            const uint4 vv = *reinterpret_cast<const uint4*>(tV + off);
+            const uint4 vv = *reinterpret_cast<const uint4*>(vslot + off);
             const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
             uint32_t ro[4], po[4], vo[4];
 #pragma unroll
@@ -1192,77 +1282,101 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               const float r0 = v2.x - gt * p0, r1 = v2.y - gt * p1;
               db = fmaf(d0, r0, fmaf(d1, r1, db));
               dgp = fmaf(d0, p0, fmaf(d1, p1, dgp));
-              ro[e] = pack_bf16(b * r0, b * r1);
-              po[e] = pack_bf16(-gt * b * d0, -gt * b * d1);
-              vo[e] = pack_bf16(b * d0, b * d1);
+              ro[e] = pack_bf16(bt * r0, bt * r1);
+              po[e] = pack_bf16(-gt * bt * d0, -gt * bt * d1);
+              vo[e] = pack_bf16(bt * d0, bt * d1);
             }
-            *reinterpret_cast<uint4*>(tV + off) = make_uint4(ro[0], ro[1], ro[2], ro[3]);
-            *reinterpret_cast<uint4*>(tK + off) = make_uint4(po[0], po[1], po[2], po[3]);
-            *reinterpret_cast<uint4*>(tdV + off) = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+            *reinterpret_cast<uint4*>(vslot + off) = make_uint4(ro[0], ro[1], ro[2], ro[3]);
+            *reinterpret_cast<uint4*>(pslot + off) = make_uint4(po[0], po[1], po[2], po[3]);
+            dvo[h] = make_uint4(vo[0], vo[1], vo[2], vo[3]);
+          }
+          if (valid) {
+            reinterpret_cast<uint4*>(dvrow + c0)[0] = dvo[0];
+            reinterpret_cast<uint4*>(dvrow + c0)[1] = dvo[1];
           }
         }
-        if (valid) a.dbeta[f * S + s] = a.gate_logits ? db * b * (1.f - b) : db;
-        part -= b * dgp;
+        float* redb = red + 8 * b;
+        float* dbhb = dbh + kKvTok * b;
+        if (half == 1) dbhb[row] = db;
+        part -= bt * dgp;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (lane == 0) red[warp] = part;
+        if (lane == 0) redb[warp] = part;
         tc_fence_before();
         fence_proxy_async_smem();
-        named_barrier(1, 128);  // every row's R, dP, dV written; partial sums in `red`
-        if (threadIdx.x == 0) a.dg_part[f * ntiles + tile] = (red[0] + red[1]) + (red[2] + red[3]);
-        if (lane == 0) {
-          mbar_arrive(smem_u32(epi1));
-          for (int at = 0; at < NA; ++at)
-            tma_store_3d(&mapdV, smem_u32(tdV + at * (kKvTok * 128) + warp * 32 * 128), 64 * at,
-                         tile * kKvTok + warp * 32, (int)f);
-          bulk_commit();
+        named_barrier(1, 256);  // R, dP written; dbeta halves and partial sums in place
+        if (half == 0 && valid) {
+          const float dbt = db + dbhb[row];
+          a.dbeta[f * S + s] = a.gate_logits ? dbt * bt * (1.f - bt) : dbt;
         }
-        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(mma2), ph, abort_flag, a.status))) goto done;
+        if (et == 0) {
+          float tot = 0.f;
+          for (int w = 0; w < 8; ++w) tot += redb[w];
+          a.dg_part[f * ntiles + tile] = tot;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(epi1));
+      }
+    }
+  } else if (warp < 12) {
+    // ---------------- dK: warp 8 + q drains rows 32q .. 32q + 31 of dK~
+    const int quad = warp - 8;
+    const int row = quad * 32 + lane;
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    long long n = 0;
+    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+      for (int tile = 0; tile < ntiles; ++tile, ++n) {
+        const int b = (int)(n & 1);
+        const int s = tile * kKvTok + row;
+        const bool valid = s < S;
+        __nv_bfloat16* dkrow = a.dk + (f * S + s) * D;
+        if (!__all_sync(0xffffffffu,
+                        wait_or_abort(smem_u32(&mma2[b]), (uint32_t)((n >> 1) & 1), abort_flag, a.status)))
+          goto done;
         tc_fence_after();
-        // dK = dK~ / sqrt(D*S) -> bf16 into the K slot (dP has been consumed)
-        for (int c0 = 0; c0 < D; c0 += 16) {
-          float kv[16];
-          tmem_ld16(tmem + lane_base + c0, kv);
-          tmem_ld_wait();
-          const uint32_t ab = (c0 >> 6) * (kKvTok * 128);
+        // two rounds of up to four 16-column chunks: all of a round's loads go out
+        // before its first wait
 #pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            uint4 o;
-            o.x = pack_bf16(a.ck * kv[8 * h + 0], a.ck * kv[8 * h + 1]);
-            o.y = pack_bf16(a.ck * kv[8 * h + 2], a.ck * kv[8 * h + 3]);
-            o.z = pack_bf16(a.ck * kv[8 * h + 4], a.ck * kv[8 * h + 5]);
-            o.w = pack_bf16(a.ck * kv[8 * h + 6], a.ck * kv[8 * h + 7]);
-            *reinterpret_cast<uint4*>(tK + ab + sw128_off(row, (c0 & 63) + 8 * h)) = o;
+        for (int r = 0; r < 2; ++r) {
+          float kv[4][16];
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (16 * (4 * r + c) < D) tmem_ld16(tmem + lane_base + 256 * b + 16 * (4 * r + c), kv[c]);
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+            if (16 * (4 * r + c) < D) tmem_ld_wait_regs(kv[c]);
+          if (r == 1) {  // every TMEM read of this buffer is done
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&dkfree[b]));
+          }
+          if (valid) {
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+              const int col = 16 * (4 * r + c);
+              if (col < D) {
+                uint32_t o[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] = pack_bf16(a.ck * kv[c][2 * e], a.ck * kv[c][2 * e + 1]);
+                reinterpret_cast<uint4*>(dkrow + col)[0] = make_uint4(o[0], o[1], o[2], o[3]);
+                reinterpret_cast<uint4*>(dkrow + col)[1] = make_uint4(o[4], o[5], o[6], o[7]);
+              }
+            }
           }
         }
-        tc_fence_before();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          for (int at = 0; at < NA; ++at)
-            tma_store_3d(&mapdK, smem_u32(tK + at * (kKvTok * 128) + warp * 32 * 128), 64 * at,
-                         tile * kKvTok + warp * 32, (int)f);
-          bulk_commit();
-          bulk_wait_read0();  // this warp's dV and dK rows have left the K and dV slots
-          mbar_arrive(smem_u32(kempty));
-        }
-        __syncwarp();
-        ph ^= 1;
       }
-      iph ^= 1;
     }
   }
 done:
-  if (warp < 4 && lane == 0) bulk_wait0();  // this warp's stores are complete
-  if (warp == 5 && lane == 0) {
+  if (warp == wmma && lane == 0) {
     mma_commit(smem_u32(mma_done));
     wait_bounded(smem_u32(mma_done), 0, 500000000ull);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == wmma) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -1279,13 +1393,14 @@ int num_sms() {
 }
 
 constexpr int kBarBytes = 256;
+constexpr int kKvBarBytes = 1536;  // barriers, partial sums and dbeta halves of tc_kv_grad_kernel
 
 // Every kernel here asks for more than half of the SM's shared memory, so two of
 // them never share an SM (the gram and read-out kernels allocate all of TMEM).
 int gram_smem(int NA, int D) {
   return kGramRaw * kRawStage + kGramConv * kConvStage + NA * D * 128 + kBarBytes + 1024;
 }
-int kv_smem(int NA, int D) { return 2 * ((2 * NA * D * 128 + 1023) & ~1023) + 3 * NA * kKvTok * 128 + kBarBytes + 1024; }
+int kv_smem(int NA, int D) { return 4 * NA * D * 128 + 3 * NA * kKvTok * 128 + kKvBarBytes + 1024; }
 int scan_smem() { return kScanStages * (kScanMStage + kScanBStage) + 2 * kScanImg + kBarBytes + 1024; }
 int out_smem(int NA, int D) {
   return 2 * ((2 * NA * D * 128 + 1023) & ~1023) + (kOutQStages + 1) * NA * kOutTok * 128 + kBarBytes + 1024;
@@ -1396,11 +1511,10 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st)
   const int nsm = num_sms();
   const unsigned pgrid = (unsigned)(F < nsm ? F : nsm);
 
-  CUtensorMap mapK, mapV, mapQ, mapDO, mapDO128, mapDQ, mapDK, mapDV;
+  CUtensorMap mapK, mapV, mapQ, mapDO, mapDO128, mapDQ;
   if (!make_map(&mapK, p.k, D, p.S, F, kGramTok) || !make_map(&mapV, p.v, D, p.S, F, kGramTok) ||
       !make_map(&mapQ, p.q, D, p.S, F, kGramTok) || !make_map(&mapDO, gr.dout, D, p.S, F, kGramTok) ||
-      !make_map(&mapDO128, gr.dout, D, p.S, F, kOutTok) || !make_map(&mapDQ, gr.dq, D, p.S, F, 32) ||
-      !make_map(&mapDK, gr.dk, D, p.S, F, 32) || !make_map(&mapDV, gr.dv, D, p.S, F, 32))
+      !make_map(&mapDO128, gr.dout, D, p.S, F, kOutTok) || !make_map(&mapDQ, gr.dq, D, p.S, F, 32))
     return kCuda;
   CUtensorMap mapK128, mapV128;
   if (!make_map(&mapK128, p.k, D, p.S, F, kKvTok) || !make_map(&mapV128, p.v, D, p.S, F, kKvTok)) return kCuda;
@@ -1450,10 +1564,12 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st)
     const int smem = kv_smem(NA, D);
     if (cudaFuncSetAttribute(tc_kv_grad_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
-    KvArgs ka{s_img, s0_img, u_img, p.g, p.beta, p.gate_logits, gr.dbeta, dg_part, F, p.T, p.S, D, NA,
-              p.key_scale, p.status};
+    KvArgs ka{s_img, s0_img, u_img, p.g, p.beta, static_cast<const __nv_bfloat16*>(p.k),
+              static_cast<const __nv_bfloat16*>(p.v), p.gate_logits,
+              static_cast<__nv_bfloat16*>(gr.dk),
+              static_cast<__nv_bfloat16*>(gr.dv), gr.dbeta, dg_part, F, p.T, p.S, D, NA, p.key_scale, p.status};
     ProfScope ps(st, "tc_bwd_kv_grad");
-    tc_kv_grad_kernel<<<pgrid, kKvThreads, smem, st>>>(mapK128, mapV128, mapDK, mapDV, ka);
+    tc_kv_grad_kernel<<<pgrid, kKvThreads, smem, st>>>(mapK128, mapV128, ka);
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   // dQ = dO S_t^T / sqrt(D)

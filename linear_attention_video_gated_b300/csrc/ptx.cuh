@@ -171,6 +171,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+// tmem_ld_wait that also ties the registers of `v` (the destination of an earlier
+// tmem_ld16) to the wait, so the compiler cannot move their uses above it: for
+// loads issued ahead of the arithmetic that consumes an earlier load.
+__device__ __forceinline__ void tmem_ld_wait_regs(float (&v)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+f"(v[0]), "+f"(v[1]), "+f"(v[2]), "+f"(v[3]), "+f"(v[4]), "+f"(v[5]), "+f"(v[6]), "+f"(v[7]),
+                 "+f"(v[8]), "+f"(v[9]), "+f"(v[10]), "+f"(v[11]), "+f"(v[12]), "+f"(v[13]), "+f"(v[14]),
+                 "+f"(v[15])
+               :
+               : "memory");
+}
 
 // ---- clusters ------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_rank() {
