@@ -88,6 +88,26 @@ def kernel_alg_bytes(name: str, wl) -> int | None:
     return None
 
 
+# ----------------------------------------------------------------- multi-rank timing
+
+def rank_max(value: float, world: int, device=None) -> float:
+    """The maximum of `value` over all ranks (the slowest rank's time); the value
+    itself when world == 1.  `device` is where the reduction tensor lives: the
+    rank's GPU under NCCL, the CPU under gloo."""
+    if world <= 1:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(units_per_rank: float, world: int, ms: float) -> float:
+    """Whole-job throughput: the units every rank processed (each rank a full
+    replica of the workload) divided by the slowest rank's time."""
+    return units_per_rank * world / (ms / 1e3)
+
+
 # ----------------------------------------------------------------- environment
 
 def peaks() -> dict:
@@ -379,12 +399,8 @@ def ours_arm(args, rank, world, local_rank):
     rc = binding.gdn_last_error(sp)
     if rc != 0:
         raise binding.GDNError(rc, "timed region")
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
-    value = wl.tokens * world / (ms / 1e3)
+    ms = rank_max(ev0.elapsed_time(ev1) / args.steps, world, dev)
+    value = job_value(wl.tokens, world, ms)
     pk = peaks()
 
     # roofline of the dominant kernel, from its own CUDA-event durations
@@ -429,14 +445,10 @@ def ours_arm(args, rank, world, local_rank):
             e2e_step()
         e1.record(stream)
         torch.cuda.synchronize()
-        ems = e0.elapsed_time(e1) / n_e2e
-        if world > 1:
-            t = torch.tensor([ems], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            ems = float(t.item())
+        ems = rank_max(e0.elapsed_time(e1) / n_e2e, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
         d2h = ho.numel() * ho.element_size() + hs.numel() * hs.element_size()
-        e2e = {"value": wl.tokens * world / (ems / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_value(wl.tokens, world, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": n_e2e,
                "api": f"gdn_frame_fwd_host, {args.e2e_chunk}-frame chunks, pinned host buffers"}
 
