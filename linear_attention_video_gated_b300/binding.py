@@ -313,3 +313,42 @@ def frame_bwd(q, k, v, g, beta, dout, state_in=None, dstate_out=None, gate_logit
     if rc != 0:
         raise GDNError(rc, "gdn_frame_bwd")
     return out
+
+
+_FRAME_GDN = None
+
+
+def _frame_gdn_function():
+    """torch.autograd.Function over the forward and backward entry points (built
+    on first use so that importing the binding does not import torch)."""
+    global _FRAME_GDN
+    if _FRAME_GDN is None:
+        import torch
+
+        class FrameGDN(torch.autograd.Function):
+            @staticmethod
+            def forward(ctx, q, k, v, g, beta, state_in, gate_logits):
+                out, st = frame_fwd(q, k, v, g, beta, state_in=state_in, mode=GDN_MODE_SEQUENTIAL,
+                                    gate_logits=gate_logits)
+                ctx.save_for_backward(q, k, v, g, beta, state_in)
+                ctx.gate_logits = gate_logits
+                return out, st
+
+            @staticmethod
+            def backward(ctx, dout, dstate):
+                q, k, v, g, beta, state_in = ctx.saved_tensors
+                res = frame_bwd(q, k, v, g, beta, dout.contiguous(), state_in=state_in,
+                                dstate_out=dstate.contiguous(), gate_logits=ctx.gate_logits,
+                                want_dstate_in=state_in is not None)
+                return res["dq"], res["dk"], res["dv"], res["dg"], res["dbeta"], res["dstate_in"], None
+
+        _FRAME_GDN = FrameGDN
+    return _FRAME_GDN
+
+
+def gdn(q, k, v, g, beta, state_in=None, gate_logits=False):
+    """The scan as a differentiable torch op: (out, state_out) = gdn_frame_fwd(...),
+    with gradients from gdn_frame_bwd (gdn_frame_*_from_logits when gate_logits).
+    Layouts as frame_fwd; every input may require grad."""
+    return _frame_gdn_function().apply(q, k, v, g, beta, state_in, gate_logits)
+

@@ -151,3 +151,27 @@ def test_backward_minute_sampled_heads():
         r = parity.assert_grad_parity(wl.dtype, got, ref, f"minute bwd head {(b, h)}")
         print(f"minute bwd head {(b, h)}: " + ", ".join(
             f"{k} max {v['max_abs_over_rms']:.2e} rms {v['rms_err_over_rms']:.2e}" for k, v in r.items()))
+
+
+@pytest.mark.parametrize("gate_logits", [False, True])
+def test_autograd_op_matches_the_backward_entry(gate_logits):
+    """binding.gdn under torch.autograd: a loss over both outputs gives exactly the
+    gradients gdn_frame_bwd returns for that loss's output gradients."""
+    wl, x, gr, S0 = _case_inputs("bf16", 1, 2, 4, 70, 48, True, 6600)
+    q, k, v, g, beta = parity.upload(wl, x)
+    if gate_logits:
+        lg = synth.logits_full(wl)
+        g, beta = torch.from_numpy(lg["g_logit"]).cuda(), torch.from_numpy(lg["beta_logit"]).cuda()
+    s0 = torch.from_numpy(S0).cuda()
+    leaves = [t.clone().requires_grad_(True) for t in (q, k, v, g, beta, s0)]
+    out, st = binding.gdn(*leaves, gate_logits=gate_logits)
+    w_out = torch.from_numpy(gr["dout"]).cuda().to(q.dtype)
+    w_st = torch.from_numpy(gr["dstate"]).cuda()
+    ((out.float() * w_out.float()).sum() + (st * w_st).sum()).backward()
+    ref = binding.frame_bwd(q, k, v, g, beta, w_out.contiguous(), state_in=s0, dstate_out=w_st,
+                            gate_logits=gate_logits)
+    torch.cuda.synchronize()
+    parity.check_status()
+    for leaf, key in zip(leaves, ("dq", "dk", "dv", "dg", "dbeta", "dstate_in")):
+        assert torch.equal(leaf.grad, ref[key]), key
+
