@@ -270,14 +270,16 @@ def _fill_head(wl, b, h, hq, hk, hv, hg, hb):
 
 # ----------------------------------------------------------------- arms
 
-def config_of(wl, mode, gate_logits=False, relu_linear=False, backward=False) -> dict:
+def config_of(wl, mode, gate_logits=False, relu_linear=False, backward=False, rollout=False) -> dict:
     gates = ", gates from logits (fused gate prologue)" if gate_logits else ""
     if relu_linear:
         gates = ", cumulative ReLU linear attention baseline (no decay, no delta rule)"
     if backward:
         gates += ", BACKWARD pass (gdn_frame_bwd: every gradient, states recomputed)"
+    calls = (f"{len(wl.chunks)} chunk-causal calls of <= {max(wl.chunks)} frames carrying the state" if rollout
+             else "single call over all frames")
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} T={wl.T} S={wl.S} D={wl.D} {wl.dtype} I/O, fp32 state, "
-                        f"single call over all frames{gates}",
+                        f"{calls}{gates}",
             "B": wl.B, "H": wl.H, "T": wl.T, "S": wl.S, "D": wl.D,
             "mode": "backward" if backward else {0: "sequential", 1: "prefix", 2: "split", 3: "cluster"}[mode],
             "l2": f"no flush: inputs larger than L2 "
@@ -339,6 +341,20 @@ def ours_arm(args, rank, world, local_rank):
     sp = stream.cuda_stream
 
     entry = binding.gdn_frame_fwd_from_logits if args.gate_logits else binding.gdn_frame_fwd_ex
+    # chunk-causal rollout (a workload with chunks): one step = every chunk's call in
+    # order, each chunk's tensors contiguous as a generator would produce them, the
+    # state carried from call to call
+    rollout = bool(wl.chunks) and not args.frames and not args.backward and not args.relu_linear
+    if rollout:
+        spans, t0 = [], 0
+        for n in wl.chunks:
+            spans.append((t0, n))
+            t0 += n
+        cut = lambda t, a, n: t[:, :, a:a + n].contiguous()  # noqa: E731
+        chunk_in = [tuple(cut(t, a, n) for t in (q, k, v, g, beta)) + (cut(out, a, n),) for a, n in spans]
+        need = max(binding.gdn_workspace_bytes(wl.B, wl.H, n, wl.S, wl.D, dtype, mode) for n in wl.chunks)
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
+        states = [torch.empty((wl.B, wl.H, wl.D, wl.D), dtype=torch.float32, device=dev) for _ in range(2)]
     if args.backward:
         hdo = torch.empty(shape, dtype=hdt, pin_memory=True)
         synth.fill_dout(wl, hdo.numpy())
@@ -351,6 +367,17 @@ def ours_arm(args, rank, world, local_rank):
         bentry = binding.gdn_frame_bwd_from_logits if args.gate_logits else binding.gdn_frame_bwd
 
     def step(qq=q, kk=k, vv=v, gg=g, bb=beta, so=st_out):
+        if rollout:
+            sin = None
+            for i, ((_, n), (cq, ck, cv, cg, cb, co)) in enumerate(zip(spans, chunk_in)):
+                sout = states[i & 1]
+                rc = entry(cq.data_ptr(), ck.data_ptr(), cv.data_ptr(), cg.data_ptr(), cb.data_ptr(),
+                           None if sin is None else sin.data_ptr(), co.data_ptr(), sout.data_ptr(), wl.B, wl.H, n,
+                           wl.S, wl.D, dtype, mode, ws.data_ptr(), need, sp)
+                if rc != 0:
+                    raise binding.GDNError(rc, "gdn_frame_fwd_ex (rollout)")
+                sin = sout
+            return
         if args.backward:
             rc = bentry(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), gg.data_ptr(), bb.data_ptr(), None,
                         dout.data_ptr(), None, grads[0].data_ptr(), grads[1].data_ptr(), grads[2].data_ptr(),
@@ -409,12 +436,14 @@ def ours_arm(args, rank, world, local_rank):
     if dom is not None:
         name, (launches, tot) = dom
         avg = tot / launches
-        ab = kernel_alg_bytes(name, wl)
+        ab = kernel_alg_bytes(name, wl)  # per call over the whole workload
         if ab is not None:
-            ach = ab / (avg / 1e3) / 1e9
-            traffic = ncu_traffic(name, wl)
+            # a rollout splits each call's work over one launch per chunk
+            ab_launch = ab * args.steps / launches
+            ach = ab_launch / (avg / 1e3) / 1e9
+            traffic = ncu_traffic(name, wl) if launches == args.steps else None
             roof = {"bound": "hbm", "kernel": name, "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                    "frac": ach / pk["hbm_gbs"], "traffic": traffic, "alg_bytes_per_launch": ab,
+                    "frac": ach / pk["hbm_gbs"], "traffic": traffic, "alg_bytes_per_launch": ab_launch,
                     "avg_launch_ms": avg, "peak_source": f"{pk['source']} (MEASURED_PEAKS.json hbm_gbs)"
                     if pk["source"] == "measured" else "fallback 6.4 TB/s"}
     call_gbs = (alg_bytes_bwd(wl) if args.backward else alg_bytes(wl)) / (ms / 1e3) / 1e9
@@ -426,13 +455,14 @@ def ours_arm(args, rank, world, local_rank):
         ho = torch.empty(shape, dtype=tdt, pin_memory=True)
         hs = torch.empty((wl.B, wl.H, wl.D, wl.D), dtype=torch.float32, pin_memory=True)
         n_e2e = max(2, min(args.steps, args.e2e_steps))
-        hneed = binding.gdn_host_workspace_bytes(wl.B, wl.H, wl.T, wl.S, wl.D, dtype, args.e2e_chunk)
+        echunk = max(wl.chunks) if rollout else args.e2e_chunk
+        hneed = binding.gdn_host_workspace_bytes(wl.B, wl.H, wl.T, wl.S, wl.D, dtype, echunk)
         hws = torch.empty(max(hneed, 1), dtype=torch.uint8, device=dev)
 
         def e2e_step():
             rc = binding.gdn_frame_fwd_host(hq.data_ptr(), hk.data_ptr(), hv.data_ptr(), hg.data_ptr(),
                                             hb.data_ptr(), None, ho.data_ptr(), hs.data_ptr(), wl.B, wl.H, wl.T,
-                                            wl.S, wl.D, dtype, args.e2e_chunk, hws.data_ptr(), hneed, sp)
+                                            wl.S, wl.D, dtype, echunk, hws.data_ptr(), hneed, sp)
             if rc != 0:
                 raise binding.GDNError(rc, "gdn_frame_fwd_host")
 
@@ -450,7 +480,7 @@ def ours_arm(args, rank, world, local_rank):
         d2h = ho.numel() * ho.element_size() + hs.numel() * hs.element_size()
         e2e = {"value": job_value(wl.tokens, world, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": n_e2e,
-               "api": f"gdn_frame_fwd_host, {args.e2e_chunk}-frame chunks, pinned host buffers"}
+               "api": f"gdn_frame_fwd_host, {echunk}-frame chunks, pinned host buffers"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -462,7 +492,7 @@ def ours_arm(args, rank, world, local_rank):
         line = {"metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-                "config": config_of(wl, mode, args.gate_logits, args.relu_linear, args.backward),
+                "config": config_of(wl, mode, args.gate_logits, args.relu_linear, args.backward, rollout),
                 "roofline_pct": 100.0 * call_gbs / pk["hbm_gbs"],
                 "call_achieved_gbs": call_gbs,
                 "tflops": (alg_flops_bwd(wl) if args.backward else alg_flops(wl)) / (ms / 1e3) / 1e12,
