@@ -10,7 +10,9 @@ the timed region starts and are larger than L2, so no flush is needed.
     python bench.py [--gpus N --steps K --warmup W] [--impl reference]
 
 ``--backward`` times the backward pass instead (one gdn_frame_bwd call over the
-same workload: every gradient, states recomputed), on its own metric line.
+same workload: every gradient, states recomputed), on its own metric line;
+``--backward --reuse-forward`` the backward that reads the per-frame states a
+forward call left in the shared workspace (gdn_frame_bwd_ex).
 
 Under torchrun (N > 1) every rank runs its own full replica of the workload on
 its own GPU (weak scaling; the path needs no cross-GPU exchange), the ranks
@@ -270,12 +272,14 @@ def _fill_head(wl, b, h, hq, hk, hv, hg, hb):
 
 # ----------------------------------------------------------------- arms
 
-def config_of(wl, mode, gate_logits=False, relu_linear=False, backward=False, rollout=False) -> dict:
+def config_of(wl, mode, gate_logits=False, relu_linear=False, backward=False, rollout=False, reuse=False) -> dict:
     gates = ", gates from logits (fused gate prologue)" if gate_logits else ""
     if relu_linear:
         gates = ", cumulative ReLU linear attention baseline (no decay, no delta rule)"
     if backward:
-        gates += ", BACKWARD pass (gdn_frame_bwd: every gradient, states recomputed)"
+        gates += (", BACKWARD pass (gdn_frame_bwd_ex: every gradient, the per-frame states read from the "
+                  "forward call's workspace)" if reuse else
+                  ", BACKWARD pass (gdn_frame_bwd: every gradient, states recomputed)")
     calls = (f"{len(wl.chunks)} chunk-causal calls of <= {max(wl.chunks)} frames carrying the state" if rollout
              else "single call over all frames")
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} T={wl.T} S={wl.S} D={wl.D} {wl.dtype} I/O, fp32 state, "
@@ -364,7 +368,14 @@ def ours_arm(args, rank, world, local_rank):
         dbeta = torch.empty((wl.B, wl.H, wl.T, wl.S), dtype=torch.float32, device=dev)
         need = binding.gdn_bwd_workspace_bytes(wl.B, wl.H, wl.T, wl.S, wl.D, dtype)
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=dev)
-        bentry = binding.gdn_frame_bwd_from_logits if args.gate_logits else binding.gdn_frame_bwd
+        bflags = ((binding.GDN_BWD_GATE_LOGITS if args.gate_logits else 0)
+                  | (binding.GDN_BWD_STATES_IN_WORKSPACE if args.reuse_forward else 0))
+        if args.reuse_forward:  # one forward call leaves the per-frame states in the workspace
+            rc = entry(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(), None,
+                       out.data_ptr(), st_out.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype, 0, ws.data_ptr(),
+                       need, sp)
+            if rc != 0:
+                raise binding.GDNError(rc, "gdn_frame_fwd_ex")
 
     def step(qq=q, kk=k, vv=v, gg=g, bb=beta, so=st_out):
         if rollout:
@@ -379,10 +390,11 @@ def ours_arm(args, rank, world, local_rank):
                 sin = sout
             return
         if args.backward:
-            rc = bentry(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), gg.data_ptr(), bb.data_ptr(), None,
-                        dout.data_ptr(), None, grads[0].data_ptr(), grads[1].data_ptr(), grads[2].data_ptr(),
-                        dg.data_ptr(), dbeta.data_ptr(), so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype,
-                        ws.data_ptr(), need, sp)
+            rc = binding.gdn_frame_bwd_ex(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), gg.data_ptr(),
+                                          bb.data_ptr(), None, dout.data_ptr(), None, grads[0].data_ptr(),
+                                          grads[1].data_ptr(), grads[2].data_ptr(), dg.data_ptr(),
+                                          dbeta.data_ptr(), so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype,
+                                          bflags, ws.data_ptr(), need, sp)
         elif args.relu_linear:
             rc = binding.gdn_relu_linear_fwd(qq.data_ptr(), kk.data_ptr(), vv.data_ptr(), None, out.data_ptr(),
                                              so.data_ptr(), wl.B, wl.H, wl.T, wl.S, wl.D, dtype, mode,
@@ -492,7 +504,8 @@ def ours_arm(args, rank, world, local_rank):
         line = {"metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": UNIT, "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
-                "config": config_of(wl, mode, args.gate_logits, args.relu_linear, args.backward, rollout),
+                "config": config_of(wl, mode, args.gate_logits, args.relu_linear, args.backward, rollout,
+                                    args.reuse_forward),
                 "roofline_pct": 100.0 * call_gbs / pk["hbm_gbs"],
                 "call_achieved_gbs": call_gbs,
                 "tflops": (alg_flops_bwd(wl) if args.backward else alg_flops(wl)) / (ms / 1e3) / 1e12,
@@ -518,6 +531,8 @@ def main():
                     help="time the cumulative ReLU linear attention baseline (gdn_relu_linear_fwd)")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass (gdn_frame_bwd) instead of the forward scan")
+    ap.add_argument("--reuse-forward", action="store_true",
+                    help="with --backward: the backward reads the states a forward call left in its workspace")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--e2e-chunk", type=int, default=32, help="frames per chunk of the host-buffer entry point")
@@ -526,6 +541,8 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.reuse_forward and not args.backward:
+        ap.error("--reuse-forward goes with --backward")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

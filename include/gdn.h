@@ -121,9 +121,11 @@ size_t gdn_workspace_bytes(int B, int H, int T, int S, int D, int dtype, int mod
 /*
  * gdn_frame_fwd_ex -- gdn_frame_fwd with an explicit algorithm form and a
  * caller-owned device workspace of at least gdn_workspace_bytes() bytes,
- * 256-byte aligned.  The workspace is not read before it is written; its
- * contents after the call are unspecified.  Two calls in flight at the same time
- * must not share a workspace.
+ * 256-byte aligned.  The workspace is not read before it is written.  After a
+ * call with GDN_MODE_SEQUENTIAL or GDN_MODE_SPLIT (and, for GDN_F32 only, with
+ * GDN_MODE_PREFIX) it holds the per-frame states that gdn_frame_bwd_ex reads with
+ * GDN_BWD_STATES_IN_WORKSPACE; otherwise its contents after the call are
+ * unspecified.  Two calls in flight at the same time must not share a workspace.
  *   mode : gdn_mode_t.
  */
 int gdn_frame_fwd_ex(const void* q, const void* k, const void* v,
@@ -226,8 +228,37 @@ int gdn_frame_bwd_from_logits(const void* q, const void* k, const void* v,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* gdn_bwd_workspace_bytes -- workspace gdn_frame_bwd needs (0 for T = 0 and for
- * arguments it rejects). */
+ * arguments it rejects).  It is never smaller than gdn_workspace_bytes() of the
+ * forward's sequential form for the same shape and dtype. */
 size_t gdn_bwd_workspace_bytes(int B, int H, int T, int S, int D, int dtype);
+
+/* Flags of gdn_frame_bwd_ex. */
+#define GDN_BWD_STATES_IN_WORKSPACE 1 /* reuse the states a forward call left in the workspace */
+#define GDN_BWD_GATE_LOGITS 2         /* g and beta are logits (as gdn_frame_bwd_from_logits) */
+
+/*
+ * gdn_frame_bwd_ex -- gdn_frame_bwd / gdn_frame_bwd_from_logits with flags.
+ * (No counterpart on the pages: it saves recomputing the forward states in a
+ * training step that has just run the forward.)
+ *   GDN_BWD_STATES_IN_WORKSPACE : `workspace` (at least gdn_bwd_workspace_bytes())
+ *       already holds what a gdn_frame_fwd_ex call left in it -- GDN_MODE_SEQUENTIAL
+ *       or GDN_MODE_SPLIT (for GDN_F32 also GDN_MODE_PREFIX) -- over the same q, k,
+ *       v, g, beta, state_in, shape and dtype, with gates given the same way (a
+ *       logit forward for GDN_BWD_GATE_LOGITS), and nothing has written to the
+ *       workspace since.  The backward then skips recomputing the per-frame
+ *       states; its results are bit for bit those of the call without the flag.
+ *       The library cannot check that the workspace holds such states: a
+ *       workspace that does not gives wrong gradients, not an error.
+ *   GDN_BWD_GATE_LOGITS : g and beta are logits; dg and dbeta are the logits'
+ *       gradients (as gdn_frame_bwd_from_logits).
+ * Other flag bits give GDN_ERR_INVALID_ARG.  Everything else as gdn_frame_bwd.
+ */
+int gdn_frame_bwd_ex(const void* q, const void* k, const void* v,
+                     const float* g, const float* beta, const float* state_in,
+                     const void* dout, const float* dstate_out,
+                     void* dq, void* dk, void* dv, float* dg, float* dbeta, float* dstate_in,
+                     int B, int H, int T, int S, int D, int dtype, int flags,
+                     void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * gdn_frame_fwd_host -- the forward scan over inputs and outputs in HOST memory.

@@ -15,6 +15,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libgdn.so")
 
 GDN_F32, GDN_BF16 = 0, 1
+GDN_BWD_STATES_IN_WORKSPACE, GDN_BWD_GATE_LOGITS = 1, 2
 GDN_MODE_SEQUENTIAL, GDN_MODE_PREFIX, GDN_MODE_SPLIT, GDN_MODE_CLUSTER = 0, 1, 2, 3
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_MISALIGNED",
           4: "GDN_ERR_CUDA", 5: "GDN_ERR_TIMEOUT", 6: "GDN_ERR_WORKSPACE"}
@@ -39,6 +40,7 @@ _SIGS = {
     "gdn_frame_bwd": (_I, [_P] * 14 + [_I] * 6 + [_P, ctypes.c_size_t, _P]),
     "gdn_frame_bwd_from_logits": (_I, [_P] * 14 + [_I] * 6 + [_P, ctypes.c_size_t, _P]),
     "gdn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "gdn_frame_bwd_ex": (_I, [_P] * 14 + [_I] * 7 + [_P, ctypes.c_size_t, _P]),
     "gdn_last_error": (_I, [_P]),
     "gdn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "gdn_status_string": (ctypes.c_char_p, [_I]),
@@ -127,6 +129,12 @@ def gdn_frame_bwd_from_logits(q, k, v, g_logit, beta_logit, state_in, dout, dsta
     return lib().gdn_frame_bwd_from_logits(q, k, v, g_logit, beta_logit, state_in, dout, dstate_out, dq, dk, dv,
                                            dg_logit, dbeta_logit, dstate_in, B, H, T, S, D, dtype, workspace,
                                            workspace_bytes, stream)
+
+
+def gdn_frame_bwd_ex(q, k, v, g, beta, state_in, dout, dstate_out, dq, dk, dv, dg, dbeta, dstate_in, B, H, T, S, D,
+                     dtype, flags, workspace, workspace_bytes, stream) -> int:
+    return lib().gdn_frame_bwd_ex(q, k, v, g, beta, state_in, dout, dstate_out, dq, dk, dv, dg, dbeta, dstate_in, B,
+                                  H, T, S, D, dtype, flags, workspace, workspace_bytes, stream)
 
 
 def gdn_bwd_workspace_bytes(B, H, T, S, D, dtype) -> int:
@@ -282,12 +290,13 @@ def relu_linear_fwd(q, k, v, state_in=None, mode=GDN_MODE_SEQUENTIAL, workspace=
 
 
 def frame_bwd(q, k, v, g, beta, dout, state_in=None, dstate_out=None, gate_logits=False, workspace=None,
-              stream=None, want_dstate_in=True):
-    """gdn_frame_bwd (or gdn_frame_bwd_from_logits with gate_logits=True) on torch
-    CUDA tensors: the forward's inputs (layouts as frame_fwd), dout like q, and
-    dstate_out [B,H,D,D] float32 or None.  Returns a dict of dq, dk, dv (dtype of q),
-    dg [B,H,T], dbeta [B,H,T,S] and dstate_in [B,H,D,D] (None unless want_dstate_in);
-    with gate_logits the dg and dbeta entries are the logits' gradients."""
+              stream=None, want_dstate_in=True, states_in_workspace=False):
+    """gdn_frame_bwd_ex on torch CUDA tensors: the forward's inputs (layouts as
+    frame_fwd), dout like q, and dstate_out [B,H,D,D] float32 or None.  Returns a
+    dict of dq, dk, dv (dtype of q), dg [B,H,T], dbeta [B,H,T,S] and dstate_in
+    [B,H,D,D] (None unless want_dstate_in); with gate_logits the dg and dbeta
+    entries are the logits' gradients.  states_in_workspace: ``workspace`` holds
+    what a frame_fwd call (mode 0 or 2) over the same inputs left in it."""
     import torch
 
     B, H, T, S, D = q.shape
@@ -304,12 +313,14 @@ def frame_bwd(q, k, v, g, beta, dout, state_in=None, dstate_out=None, gate_logit
     need = gdn_bwd_workspace_bytes(B, H, T, S, D, dtype)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if states_in_workspace and workspace is None:
+        raise ValueError("states_in_workspace needs the forward call's workspace")
     strm = stream if stream is not None else torch.cuda.current_stream(q.device)
-    fn = gdn_frame_bwd_from_logits if gate_logits else gdn_frame_bwd
-    rc = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(dout), _ptr(dstate_out),
-            _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]), _ptr(out["dbeta"]),
-            _ptr(out["dstate_in"]), B, H, T, S, D, dtype, _ptr(workspace),
-            0 if workspace is None else workspace.numel(), strm.cuda_stream)
+    flags = (GDN_BWD_GATE_LOGITS if gate_logits else 0) | (GDN_BWD_STATES_IN_WORKSPACE if states_in_workspace else 0)
+    rc = gdn_frame_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(dout),
+                          _ptr(dstate_out), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]), _ptr(out["dg"]),
+                          _ptr(out["dbeta"]), _ptr(out["dstate_in"]), B, H, T, S, D, dtype, flags, _ptr(workspace),
+                          0 if workspace is None else workspace.numel(), strm.cuda_stream)
     if rc != 0:
         raise GDNError(rc, "gdn_frame_bwd")
     return out
@@ -328,10 +339,17 @@ def _frame_gdn_function():
         class FrameGDN(torch.autograd.Function):
             @staticmethod
             def forward(ctx, q, k, v, g, beta, state_in, gate_logits):
+                # the forward runs in a workspace sized for the backward, which then
+                # reuses the per-frame states the forward left there
+                B, H, T, S, D = q.shape
+                dtype = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}[q.dtype]
+                need = gdn_bwd_workspace_bytes(B, H, T, S, D, dtype)
+                ws = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
                 out, st = frame_fwd(q, k, v, g, beta, state_in=state_in, mode=GDN_MODE_SEQUENTIAL,
-                                    gate_logits=gate_logits)
+                                    gate_logits=gate_logits, workspace=ws)
                 ctx.save_for_backward(q, k, v, g, beta, state_in)
                 ctx.gate_logits = gate_logits
+                ctx.ws = ws if need > 0 else None
                 return out, st
 
             @staticmethod
@@ -339,7 +357,9 @@ def _frame_gdn_function():
                 q, k, v, g, beta, state_in = ctx.saved_tensors
                 res = frame_bwd(q, k, v, g, beta, dout.contiguous(), state_in=state_in,
                                 dstate_out=dstate.contiguous(), gate_logits=ctx.gate_logits,
-                                want_dstate_in=state_in is not None)
+                                want_dstate_in=state_in is not None, workspace=ctx.ws,
+                                states_in_workspace=ctx.ws is not None)
+                ctx.ws = None
                 return res["dq"], res["dk"], res["dv"], res["dg"], res["dbeta"], res["dstate_in"], None
 
         _FRAME_GDN = FrameGDN

@@ -393,7 +393,7 @@ BwdLayout bwd_layout(const Problem& p) {
 using Grads = BwdGrads;
 
 template <typename TIn>
-int run_bwd(const Problem& p, const Grads& gr, void* ws, cudaStream_t st) {
+int run_bwd(const Problem& p, const Grads& gr, void* ws, cudaStream_t st, bool states_ready) {
   const BwdLayout L = bwd_layout(p);
   char* w = static_cast<char*>(ws);
   float* Mws = reinterpret_cast<float*>(w + L.m_off);
@@ -404,12 +404,16 @@ int run_bwd(const Problem& p, const Grads& gr, void* ws, cudaStream_t st) {
   const int D = p.D;
   const size_t mat = (size_t)D * D * sizeof(float);
 
-  // forward states (b_t lands in the E buffer and is overwritten below)
-  Problem pf = p;
-  pf.out = nullptr;
-  pf.state_out = nullptr;
-  int rc = simt_states(pf, Mws, Ews, Sws, st);
-  if (rc != kOk) return rc;
+  // forward states (b_t lands in the E buffer and is overwritten below), unless a
+  // forward call left them in the workspace: the float32 forward's scratch (M_t,
+  // b_t, S_t, each BHT x D x D, 256-byte aligned) is this layout's first three regions
+  if (!states_ready) {
+    Problem pf = p;
+    pf.out = nullptr;
+    pf.state_out = nullptr;
+    const int rc = simt_states(pf, Mws, Ews, Sws, st);
+    if (rc != kOk) return rc;
+  }
 
   {
     ProfScope ps(st, "bwd_qdo");
@@ -493,13 +497,15 @@ int check_bwd(const void* q, const void* k, const void* v, const float* g, const
 int frame_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, const float* state_in,
               const void* dout, const float* dstate_out, void* dq, void* dk, void* dv, float* dg, float* dbeta,
               float* dstate_in, int B, int H, int T, int S, int D, int dtype, void* workspace,
-              size_t workspace_bytes, void* stream, int gate_logits) {
+              size_t workspace_bytes, void* stream, int flags) {
+  if (flags & ~(GDN_BWD_STATES_IN_WORKSPACE | GDN_BWD_GATE_LOGITS)) return kInvalidArg;
   Problem p{};
   Grads gr{};
   int rc = check_bwd(q, k, v, g, beta, state_in, dout, dstate_out, dq, dk, dv, dg, dbeta, dstate_in, B, H, T, S, D,
                      dtype, &p, &gr);
   if (rc != kOk) return rc;
-  p.gate_logits = gate_logits;
+  p.gate_logits = (flags & GDN_BWD_GATE_LOGITS) ? 1 : 0;
+  const bool states_ready = (flags & GDN_BWD_STATES_IN_WORKSPACE) != 0;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (T == 0) {  // the initial state's gradient is the final state's
     if (!dstate_in) return kOk;
@@ -512,7 +518,8 @@ int frame_bwd(const void* q, const void* k, const void* v, const float* g, const
   if (!aligned(workspace, 256)) return kMisaligned;
   p.status = device_status_word();
   if (!p.status) return kCuda;
-  return dtype == GDN_F32 ? run_bwd<float>(p, gr, workspace, st) : tc_backward(p, gr, workspace, st);
+  return dtype == GDN_F32 ? run_bwd<float>(p, gr, workspace, st, states_ready)
+                          : tc_backward(p, gr, workspace, st, states_ready);
 }
 
 }  // namespace
@@ -550,11 +557,19 @@ extern "C" int gdn_frame_bwd(const void* q, const void* k, const void* v, const 
                    dtype, workspace, workspace_bytes, stream, 0);
 }
 
+extern "C" int gdn_frame_bwd_ex(const void* q, const void* k, const void* v, const float* g, const float* beta,
+                                const float* state_in, const void* dout, const float* dstate_out, void* dq, void* dk,
+                                void* dv, float* dg, float* dbeta, float* dstate_in, int B, int H, int T, int S,
+                                int D, int dtype, int flags, void* workspace, size_t workspace_bytes, void* stream) {
+  return frame_bwd(q, k, v, g, beta, state_in, dout, dstate_out, dq, dk, dv, dg, dbeta, dstate_in, B, H, T, S, D,
+                   dtype, workspace, workspace_bytes, stream, flags);
+}
+
 extern "C" int gdn_frame_bwd_from_logits(const void* q, const void* k, const void* v, const float* g_logit,
                                          const float* beta_logit, const float* state_in, const void* dout,
                                          const float* dstate_out, void* dq, void* dk, void* dv, float* dg_logit,
                                          float* dbeta_logit, float* dstate_in, int B, int H, int T, int S, int D,
                                          int dtype, void* workspace, size_t workspace_bytes, void* stream) {
   return frame_bwd(q, k, v, g_logit, beta_logit, state_in, dout, dstate_out, dq, dk, dv, dg_logit, dbeta_logit,
-                   dstate_in, B, H, T, S, D, dtype, workspace, workspace_bytes, stream, 1);
+                   dstate_in, B, H, T, S, D, dtype, workspace, workspace_bytes, stream, GDN_BWD_GATE_LOGITS);
 }

@@ -106,8 +106,11 @@ struct BwdGrads {
 // Tensor-core backward (bf16 I/O): workspace bytes, and the call.  Writes dq, dk,
 // dv, dbeta and dstate_in, and per (frame-head, 128-token tile) partial sums of dg
 // into `dg_part` (*ntiles tiles per frame-head), which launch_dg_sum reduces.
+// With states_ready the workspace already holds the M_t image, b_t blocks and S_t
+// images of a forward split-form call over the same inputs (the first three regions
+// of the backward layout are the forward's), and their recomputation is skipped.
 size_t tc_bwd_workspace_bytes(const Problem& p);
-int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st);
+int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st, bool states_ready);
 // dg[f] = sum of dg_part[f * ntiles .. + ntiles) (times dg/dlogit for logits).
 int launch_dg_sum(const float* dg_part, const float* g, float* dg, long long nframes, int ntiles, int logits,
                   cudaStream_t st);

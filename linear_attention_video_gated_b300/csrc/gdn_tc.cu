@@ -1497,8 +1497,17 @@ TcBwdLayout tc_bwd_layout(const Problem& p) {
 
 size_t tc_bwd_workspace_bytes(const Problem& p) { return tc_bwd_layout(p).total; }
 
-int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st) {
+// The forward split form's scratch (tc_layout) is the backward layout's first
+// three regions, so a forward call's states can be reused in place.
+bool tc_bwd_layout_extends_forward(const Problem& p) {
+  const TcLayout f = tc_layout(p);
+  const TcBwdLayout b = tc_bwd_layout(p);
+  return f.m_off == b.m_off && f.b_off == b.e_off && f.s_off == b.s_off && f.total <= b.total;
+}
+
+int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st, bool states_ready) {
   const TcBwdLayout L = tc_bwd_layout(p);
+  if (states_ready && !tc_bwd_layout_extends_forward(p)) return kInvalidArg;
   const int NA = num_atoms(p.D), D = p.D;
   uint8_t* w = static_cast<uint8_t*>(ws);
   uint8_t* m_img = w + L.m_off;
@@ -1527,20 +1536,23 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st)
     return kCuda;
   const unsigned sgrid = (unsigned)(p.BH() * (D / 16));
 
-  // forward states: M_t (image), b_t (into the E blocks), S_t (images)
-  {
-    GramArgs ga{p.beta, p.gate_logits, kGdn, m_img, e_blk, F, p.S, D, NA, p.key_scale * p.key_scale, p.key_scale,
-                p.status, 0};
-    ProfScope ps(st, "tc_gram");
-    tc_gram_kernel<<<pgrid, kGramThreads, gsmem, st>>>(mapK, mapV, ga);
+  // forward states: M_t (image), b_t (into the E blocks), S_t (images), unless a
+  // forward call left them in the workspace (tc_layout's regions are this layout's first three)
+  if (!states_ready) {
+    {
+      GramArgs ga{p.beta, p.gate_logits, kGdn, m_img, e_blk, F, p.S, D, NA, p.key_scale * p.key_scale, p.key_scale,
+                  p.status, 0};
+      ProfScope ps(st, "tc_gram");
+      tc_gram_kernel<<<pgrid, kGramThreads, gsmem, st>>>(mapK, mapV, ga);
+    }
+    if (cudaGetLastError() != cudaSuccess) return kCuda;
+    {
+      ScanArgs sa{m_img, e_blk, p.g, p.gate_logits, kGdn, p.state_in, s_img, nullptr, p.T, D, NA, p.status, 0};
+      ProfScope ps(st, "tc_scan");
+      tc_scan_kernel<<<sgrid, kScanThreads, ssmem, st>>>(sa);
+    }
+    if (cudaGetLastError() != cudaSuccess) return kCuda;
   }
-  if (cudaGetLastError() != cudaSuccess) return kCuda;
-  {
-    ScanArgs sa{m_img, e_blk, p.g, p.gate_logits, kGdn, p.state_in, s_img, nullptr, p.T, D, NA, p.status, 0};
-    ProfScope ps(st, "tc_scan");
-    tc_scan_kernel<<<sgrid, kScanThreads, ssmem, st>>>(sa);
-  }
-  if (cudaGetLastError() != cudaSuccess) return kCuda;
   // E_t = Q_t^T dO_t / sqrt(D) (overwrites b_t, which the scan has consumed)
   {
     GramArgs ga{nullptr, 0, kGdn, nullptr, e_blk, F, p.S, D, NA, 0.f, p.out_scale, p.status, 1};

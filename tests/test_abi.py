@@ -168,3 +168,19 @@ def test_backward_workspace_bytes(lib):
     assert binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 24, 1) == 0
     assert binding.gdn_bwd_workspace_bytes(1, 20, 961, 880, 112, 5) == 0
     assert binding.gdn_bwd_workspace_bytes(2, 20, 961, 880, 112, 1) > a
+
+
+@pytest.mark.parametrize("flags", [4, 8, -1, 1 << 30])
+def test_backward_ex_rejects_unknown_flags(lib, flags):
+    assert binding.gdn_frame_bwd_ex(A16, A16, A16, A16, A16, None, A16, None, A16, A16, A16, A16, A16, None,
+                                    1, 2, 3, 17, 32, 1, flags, A16, 1 << 40, None) == 1
+
+
+def test_backward_workspace_holds_the_forward_scratch(lib):
+    """The backward's workspace is never smaller than the forward's (sequential form),
+    so one buffer serves a training step's forward and backward."""
+    for dtype in (0, 1):
+        for shape in ((1, 20, 961, 880, 112), (2, 3, 7, 129, 16), (4, 16, 241, 3600, 128)):
+            assert binding.gdn_bwd_workspace_bytes(*shape, dtype) >= binding.gdn_workspace_bytes(*shape, dtype, 0)
+            if dtype == 1:
+                assert binding.gdn_bwd_workspace_bytes(*shape, dtype) >= binding.gdn_workspace_bytes(*shape, 1, 2)

@@ -175,3 +175,38 @@ def test_autograd_op_matches_the_backward_entry(gate_logits):
     for leaf, key in zip(leaves, ("dq", "dk", "dv", "dg", "dbeta", "dstate_in")):
         assert torch.equal(leaf.grad, ref[key]), key
 
+
+
+# (dtype, forward mode, gate logits)
+REUSE = [("bf16", 0, False), ("bf16", 2, False), ("bf16", 0, True), ("f32", 0, False), ("f32", 1, False)]
+
+
+@pytest.mark.parametrize("case", REUSE, ids=lambda c: "-".join(map(str, c)))
+def test_backward_reuses_the_forward_states(case):
+    """GDN_BWD_STATES_IN_WORKSPACE: a backward that reads the states a forward call
+    left in the workspace gives the recomputing backward's gradients bit for bit (the
+    same kernels made the states), or, after the fp32 prefix form (whose states come
+    from its own composition), gradients within the oracle bound."""
+    dt, mode, logits = case
+    wl, x, gr, S0 = _case_inputs(dt, 1, 2, 6, 150, 48, True, 6700 + mode)
+    q, k, v, g, beta = parity.upload(wl, x)
+    if logits:
+        lg = synth.logits_full(wl)
+        g, beta = torch.from_numpy(lg["g_logit"]).cuda(), torch.from_numpy(lg["beta_logit"]).cuda()
+    s0 = torch.from_numpy(S0).cuda()
+    dout = torch.from_numpy(gr["dout"]).cuda().to(q.dtype).contiguous()
+    dst = torch.from_numpy(gr["dstate"]).cuda()
+    need = binding.gdn_bwd_workspace_bytes(1, 2, 6, 150, 48, binding.GDN_BF16 if dt == "bf16" else binding.GDN_F32)
+    ws = torch.full((need,), 0xFF, dtype=torch.uint8, device="cuda")
+    binding.frame_fwd(q, k, v, g, beta, state_in=s0, mode=mode, workspace=ws, gate_logits=logits)
+    a = binding.frame_bwd(q, k, v, g, beta, dout, state_in=s0, dstate_out=dst, gate_logits=logits, workspace=ws,
+                          states_in_workspace=True)
+    b = binding.frame_bwd(q, k, v, g, beta, dout, state_in=s0, dstate_out=dst, gate_logits=logits)
+    torch.cuda.synchronize()
+    parity.check_status()
+    if (dt, mode) == ("f32", 1):
+        ref = oracle.frame_bwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0, gr["dout"], gr["dstate"])
+        parity.assert_grad_parity(dt, {key: np_(val) for key, val in a.items()}, ref, f"reuse {case}")
+    else:
+        for key in parity.GRAD_KEYS:
+            assert torch.equal(a[key], b[key]), key
