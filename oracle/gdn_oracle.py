@@ -163,9 +163,9 @@ def frame_fwd_from_logits(q, k, v, g_logit, beta_logit, state_in=None):
 # ----------------------------------------------------------------------------
 # Baseline: SANA-Video's cumulative ReLU-based linear attention.
 #
-# The pages contrast GDN with its predecessor's "cumulative ReLU-based linear
-# attention": a recurrent state that only accumulates, with no decay and no
-# delta-rule correction (zhichai.net summary, section 1, the paragraph on
+# The pages contrast GDN with the linear attention of its predecessor, which
+# applies a ReLU feature map and keeps a recurrent state that only accumulates,
+# with no decay and no delta-rule correction (zhichai.net summary, section 1, the paragraph on
 # SANA-Video; bilibili article, third key point).  They give no formula; the
 # plainest reading with the GDN scan's own scalings (so the two differ only in
 # the decay, the delta rule and the feature map) is
