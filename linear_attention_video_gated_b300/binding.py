@@ -299,6 +299,8 @@ def frame_bwd(q, k, v, g, beta, dout, state_in=None, dstate_out=None, gate_logit
     what a frame_fwd call (mode 0 or 2) over the same inputs left in it."""
     import torch
 
+    if states_in_workspace and workspace is None:
+        raise ValueError("states_in_workspace needs the forward call's workspace")
     B, H, T, S, D = q.shape
     dtype = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}[q.dtype]
     for name, t in (("k", k), ("v", v), ("dout", dout)):
@@ -313,8 +315,6 @@ def frame_bwd(q, k, v, g, beta, dout, state_in=None, dstate_out=None, gate_logit
     need = gdn_bwd_workspace_bytes(B, H, T, S, D, dtype)
     if workspace is None and need > 0:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
-    if states_in_workspace and workspace is None:
-        raise ValueError("states_in_workspace needs the forward call's workspace")
     strm = stream if stream is not None else torch.cuda.current_stream(q.device)
     flags = (GDN_BWD_GATE_LOGITS if gate_logits else 0) | (GDN_BWD_STATES_IN_WORKSPACE if states_in_workspace else 0)
     rc = gdn_frame_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in), _ptr(dout),
