@@ -75,7 +75,7 @@ def kernel_alg_bytes(name: str, wl) -> int | None:
     """Algorithmic bytes each kernel is responsible for, per launch (one call).
 
     gram-type kernels read k, v, beta (and g); read-out kernels read q and write
-    out; the fused kernel moves everything.  Scratch traffic is not algorithmic.
+    out.  Scratch traffic is not algorithmic.
     """
     fh = wl.B * wl.H * wl.T
     e = wl.elem_bytes
@@ -85,8 +85,6 @@ def kernel_alg_bytes(name: str, wl) -> int | None:
         return fh * 2 * wl.S * wl.D * e  # q in, out out / dout in, dq out / q and dout in
     if name.endswith("_kv_grad"):
         return fh * (4 * wl.S * wl.D * e + 8 * wl.S + 4)  # k, v, beta, g in; dk, dv, dbeta out
-    if "_fused" in name:
-        return alg_bytes(wl)
     return None
 
 
@@ -285,7 +283,7 @@ def config_of(wl, mode, gate_logits=False, relu_linear=False, backward=False, ro
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} T={wl.T} S={wl.S} D={wl.D} {wl.dtype} I/O, fp32 state, "
                         f"{calls}{gates}",
             "B": wl.B, "H": wl.H, "T": wl.T, "S": wl.S, "D": wl.D,
-            "mode": "backward" if backward else {0: "sequential", 1: "prefix", 2: "split", 3: "cluster"}[mode],
+            "mode": "backward" if backward else {0: "sequential", 1: "prefix", 2: "split"}[mode],
             "l2": f"no flush: inputs larger than L2 "
                   f"({(alg_bytes_bwd(wl) if backward else alg_bytes(wl)) / 1e9:.1f} GB moved per step vs 126 MB L2)"}
 
@@ -522,7 +520,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="minute", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3])
+    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--frames", type=int, default=None,
                     help="run the workload's first N frames only (small cases for profiling)")
     ap.add_argument("--gate-logits", action="store_true",

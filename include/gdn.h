@@ -84,13 +84,8 @@ typedef enum {
    * (M_t = K~^T diag(beta) K~, b_t = K~^T diag(beta) V_t) for all frames in
    * parallel, the serial D x D recurrence, then the read-out for all frames in
    * parallel. */
-  GDN_MODE_SPLIT = 2,
-  /* bf16 I/O only: one fused kernel, one thread-block cluster per head split
-   * over its value columns (columns of the state evolve independently), K and
-   * Q tiles multicast to the cluster, every stage of a frame on chip; no
-   * workspace.  Slower than the split form on B300 (its tile rings are shared
-   * by the whole cluster, so too few bytes are in flight per head). */
-  GDN_MODE_CLUSTER = 3
+  GDN_MODE_SPLIT = 2
+  /* Any other value gives GDN_ERR_INVALID_ARG. */
 } gdn_mode_t;
 
 /*
@@ -160,8 +155,7 @@ int gdn_frame_fwd_from_logits(const void* q, const void* k, const void* v,
  * (The pages give no formula; this is the plainest reading with the GDN scan's
  * own scalings, so the two differ only in the decay, the delta rule and the
  * feature map.)  Arguments, layouts, workspace (gdn_workspace_bytes with the same
- * mode) and errors as gdn_frame_fwd_ex without g and beta; GDN_MODE_CLUSTER is not
- * offered (GDN_ERR_UNSUPPORTED).
+ * mode) and errors as gdn_frame_fwd_ex without g and beta.
  */
 int gdn_relu_linear_fwd(const void* q, const void* k, const void* v, const float* state_in,
                         void* out, float* state_out,

@@ -36,8 +36,7 @@ int validate(const void* q, const void* k, const void* v, const float* g, const 
              int mode, Problem* p, bool need_gates = true) {
   if (B < 1 || H < 1 || T < 0 || S < 1 || D < 1) return kInvalidArg;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return kInvalidArg;
-  if (mode < GDN_MODE_SEQUENTIAL || mode > GDN_MODE_CLUSTER) return kInvalidArg;
-  if (mode == GDN_MODE_CLUSTER && dtype != GDN_BF16) return kUnsupported;
+  if (mode < GDN_MODE_SEQUENTIAL || mode > GDN_MODE_SPLIT) return kInvalidArg;
   if (D % 16 != 0 || D > 128) return kUnsupported;
   // Counts must stay inside what the kernels index with 64-bit offsets and
   // 32-bit grid dimensions / tensor-map extents.
@@ -178,7 +177,6 @@ int gdn_frame_fwd_ex(const void* q, const void* k, const void* v, const float* g
 int gdn_relu_linear_fwd(const void* q, const void* k, const void* v, const float* state_in, void* out,
                         float* state_out, int B, int H, int T, int S, int D, int dtype, int mode, void* workspace,
                         size_t workspace_bytes, void* stream) {
-  if (mode == GDN_MODE_CLUSTER) return GDN_ERR_UNSUPPORTED;
   Problem p{};
   int rc = validate(q, k, v, nullptr, nullptr, state_in, out, state_out, B, H, T, S, D, dtype, mode, &p, false);
   if (rc != kOk) return rc;

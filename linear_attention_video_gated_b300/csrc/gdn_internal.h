@@ -115,10 +115,6 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st,
 int launch_dg_sum(const float* dg_part, const float* g, float* dg, long long nframes, int ntiles, int logits,
                   cudaStream_t st);
 
-// ---- fused tensor-core path (bf16 I/O, one cluster per head, no scratch) ---------
-bool fused_supported(const Problem& p);
-int fused_forward(const Problem& p, cudaStream_t st);
-
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Brackets one kernel launch with CUDA events while gdn_profile_begin() is in

@@ -1409,17 +1409,14 @@ int out_smem(int NA, int D) {
 }  // namespace
 
 // Sequential and split forms: the three kernels above, through a workspace.
-// Cluster form: the fused cluster kernel (no scratch).  Prefix form: the SIMT
-// kernels for now.
+// Prefix form: the SIMT kernels for now.
 size_t tc_workspace_bytes(const Problem& p, int mode) {
   if (mode == 1) return simt_workspace_bytes(p, mode);
-  if (mode == 3) return 0;
   return tc_layout(p).total;
 }
 
 int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
   if (p.mode == 1) return simt_forward(p, ws, st);
-  if (p.mode == 3) return fused_supported(p) ? fused_forward(p, st) : kUnsupported;
   const TcLayout L = tc_layout(p);
   const int NA = num_atoms(p.D);
   uint8_t* w = static_cast<uint8_t*>(ws);

@@ -24,16 +24,6 @@ __device__ __forceinline__ uint64_t globaltimer() {
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31; }
 __device__ __forceinline__ uint32_t warp_id() { return threadIdx.x >> 5; }
 
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred = 0;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "elect.sync _|p, 0xffffffff;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(pred));
-  return pred != 0;
-}
-
 // ---- mbarrier -------------------------------------------------------------------
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -183,61 +173,16 @@ __device__ __forceinline__ void tmem_ld_wait_regs(float (&v)[16]) {
                : "memory");
 }
 
-// ---- clusters ------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Whole-cluster barrier (every thread of every CTA of the cluster executes it;
-// the non-.aligned form, so a warp need not be converged).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-// The shared::cluster address of the same byte in CTA `rank` of the cluster.
-__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
-  return r;
-}
-// TMA tile load written to the same offset of every CTA in `mask`, each CTA's
-// mbarrier at `bar`'s offset receiving complete_tx for its copy.
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const CUtensorMap* m, uint32_t bar, int c0, int c1, int c2,
-                                               uint16_t mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
-      "[%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(m)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "h"(mask)
-      : "memory");
-}
-// Bulk copy from this CTA's shared memory into another CTA's (dst and bar are
-// shared::cluster addresses in the destination CTA).
-__device__ __forceinline__ void bulk_s2dsmem(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t bar) {
-  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-                   dst),
-               "r"(src), "r"(bytes), "r"(bar)
-               : "memory");
-}
 // Asks L2 to fetch [src, src + bytes) (16-byte aligned, size a multiple of 16).
 __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(src)), "r"(bytes)
                : "memory");
 }
-// Arrives once on the mbarrier at `bar`'s offset in every CTA of `mask` when every
-// tcgen05 op this thread issued so far completes.
-__device__ __forceinline__ void mma_commit_mc(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
-
 // ---- descriptors --------------------------------------------------------------------
 // Shared-memory matrix descriptor (tcgen05): start address, leading / stride byte
 // offsets, the fixed version bits, and the layout (swizzle) mode: 2 = 128-byte
-// swizzle (the default), 6 = 32-byte swizzle.
+// swizzle.
 constexpr uint32_t kLayoutSw128 = 2;
-constexpr uint32_t kLayoutSw32 = 6;
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
                                               uint32_t layout = kLayoutSw128) {
   uint64_t d = 0;
@@ -261,13 +206,6 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int a_mn, int b_
 // must be 1024-byte aligned; col < 64.
 __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t row, uint32_t col) {
   return row * 128u + ((((col >> 3) ^ (row & 7u)) & 7u) << 4) + ((col & 7u) << 1);
-}
-
-// Byte offset of element (row, col) of a 16-bit tile stored as 32-byte rows with
-// the 32-byte swizzle (16-byte chunk index XOR bit 2 of the row).  The tile base
-// must be 256-byte aligned; col < 16.
-__host__ __device__ __forceinline__ uint32_t sw32_off(uint32_t row, uint32_t col) {
-  return row * 32u + ((((col >> 3) ^ (row >> 2)) & 1u) << 4) + ((col & 7u) << 1);
 }
 
 }  // namespace ptx

@@ -39,7 +39,7 @@ def test_tiny_f32(mode):
     parity.assert_parity("f32", np_(out), ro, np_(st), rs, f"tiny mode={mode}")
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_short_bf16(mode):
     wl = synth.WORKLOADS["short"]
     x = synth.full(wl)
@@ -66,12 +66,10 @@ EDGE = [
 ]
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("case", EDGE, ids=lambda c: "-".join(map(str, c)))
 def test_edge_shapes(case, mode):
     dt, B, H, T, S, D, nz = case
-    if mode == 3 and dt != "bf16":
-        pytest.skip("the cluster form is bf16 only")
     base = synth.WORKLOADS["short" if dt == "bf16" else "tiny"]
     wl = base.with_(B=B, H=H, T=T, S=S, D=D, seed=base.seed + 17 * S + D)
     x = synth.full(wl)
@@ -93,14 +91,12 @@ LOGIT_CASES = [
 ]
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 @pytest.mark.parametrize("case", LOGIT_CASES, ids=lambda c: "-".join(map(str, c)))
 def test_gate_logits(case, mode):
     """gdn_frame_fwd_from_logits: g and beta computed from raw logits inside the
     kernels, against the oracle's gate prologue followed by its scan."""
     dt, B, H, T, S, D = case
-    if mode == 3 and dt != "bf16":
-        pytest.skip("the cluster form is bf16 only")
     wl = synth.WORKLOADS["short"].with_(B=B, H=H, T=T, S=S, D=D, dtype=dt, seed=4000 + 7 * S + D)
     x = synth.full(wl)
     lg = synth.logits_full(wl)
@@ -142,19 +138,12 @@ def test_relu_linear_baseline(case, mode):
     parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"relu-linear {case} mode={mode}", strict=False)
 
 
-def test_relu_linear_rejects_the_cluster_form():
-    wl = synth.WORKLOADS["short"].with_(H=1, T=2, S=16, D=16)
-    q, k, v, _, _ = parity.upload(wl, synth.full(wl))
-    with pytest.raises(binding.GDNError):
-        binding.relu_linear_fwd(q, k, v, mode=3)
-
-
 def _small_bf16(T=21, H=3, S=300, D=112):
     wl = synth.WORKLOADS["short"].with_(H=H, T=T, S=S, D=D)
     return wl, synth.full(wl)
 
 
-@pytest.mark.parametrize("mode", [0, 2, 3])
+@pytest.mark.parametrize("mode", [0, 2])
 def test_state_aliasing_is_bitwise_identical(mode):
     wl, x = _small_bf16()
     ins = parity.upload(wl, x)
@@ -177,7 +166,7 @@ def test_zero_frames_copies_state():
     assert torch.count_nonzero(st2) == 0
 
 
-@pytest.mark.parametrize("mode", [0, 1, 2, 3])
+@pytest.mark.parametrize("mode", [0, 1, 2])
 def test_chunked_calls_equal_single_call(mode):
     """Chunk-causal rollout: consecutive calls passing state_out -> state_in give the
     single call's outputs.  In the sequential and split forms the per-frame
@@ -192,14 +181,14 @@ def test_chunked_calls_equal_single_call(mode):
         o, st = run(sl(q), sl(k), sl(v), sl(g), sl(beta), state_in=st, mode=mode)
         outs.append(o)
     out2 = torch.cat(outs, dim=2)
-    if mode in (0, 2, 3):
+    if mode in (0, 2):
         assert torch.equal(out1, out2) and torch.equal(st1, st)
     else:
         ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"])
         parity.assert_parity("bf16", np_(out2), ro, np_(st), rs, "chunked prefix", strict=False)
 
 
-@pytest.mark.parametrize("mode", [0, 2, 3])
+@pytest.mark.parametrize("mode", [0, 2])
 def test_repeat_calls_are_deterministic(mode):
     wl, x = _small_bf16(T=9)
     ins = parity.upload(wl, x)
@@ -256,7 +245,7 @@ def _check_heads(wl, out, st, ref, what):
         print(f"{what} head {(b, h)}: out {eo} state {es}")
 
 
-@pytest.mark.parametrize("mode", [0, 3])
+@pytest.mark.parametrize("mode", [0])
 def test_minute_single_call(minute_inputs, minute_oracle, mode):
     """961 frames x 880 tokens x 20 heads x d112, one call (mode 0 is the bench's
     launch configuration); sampled heads checked over every frame against the oracle."""
