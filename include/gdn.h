@@ -117,10 +117,8 @@ size_t gdn_workspace_bytes(int B, int H, int T, int S, int D, int dtype, int mod
  * gdn_frame_fwd_ex -- gdn_frame_fwd with an explicit algorithm form and a
  * caller-owned device workspace of at least gdn_workspace_bytes() bytes,
  * 256-byte aligned.  The workspace is not read before it is written.  After a
- * call with GDN_MODE_SEQUENTIAL or GDN_MODE_SPLIT (and, for GDN_F32 only, with
- * GDN_MODE_PREFIX) it holds the per-frame states that gdn_frame_bwd_ex reads with
- * GDN_BWD_STATES_IN_WORKSPACE; otherwise its contents after the call are
- * unspecified.  Two calls in flight at the same time must not share a workspace.
+ * call it holds the per-frame states that gdn_frame_bwd_ex reads with
+ * GDN_BWD_STATES_IN_WORKSPACE.  Two calls in flight at the same time must not share a workspace.
  *   mode : gdn_mode_t.
  */
 int gdn_frame_fwd_ex(const void* q, const void* k, const void* v,
@@ -222,8 +220,8 @@ int gdn_frame_bwd_from_logits(const void* q, const void* k, const void* v,
                               void* workspace, size_t workspace_bytes, void* stream);
 
 /* gdn_bwd_workspace_bytes -- workspace gdn_frame_bwd needs (0 for T = 0 and for
- * arguments it rejects).  It is never smaller than gdn_workspace_bytes() of the
- * forward's sequential form for the same shape and dtype. */
+ * arguments it rejects).  It is never smaller than gdn_workspace_bytes() of any
+ * forward form for the same shape and dtype. */
 size_t gdn_bwd_workspace_bytes(int B, int H, int T, int S, int D, int dtype);
 
 /* Flags of gdn_frame_bwd_ex. */
@@ -246,6 +244,8 @@ size_t gdn_bwd_workspace_bytes(int B, int H, int T, int S, int D, int dtype);
  *   GDN_BWD_GATE_LOGITS : g and beta are logits; dg and dbeta are the logits'
  *       gradients (as gdn_frame_bwd_from_logits).
  * Other flag bits give GDN_ERR_INVALID_ARG.  Everything else as gdn_frame_bwd.
+ * For the GDN_MODE_PREFIX forward the states are the prefix composition's, so
+ * the gradients agree with the recomputing call's up to rounding, not bit for bit.
  */
 int gdn_frame_bwd_ex(const void* q, const void* k, const void* v,
                      const float* g, const float* beta, const float* state_in,
@@ -288,6 +288,65 @@ int gdn_frame_fwd_host(const void* q, const void* k, const void* v,
 size_t gdn_host_workspace_bytes(int B, int H, int T, int S, int D, int dtype, int chunk_frames);
 
 /*
+ * Context parallelism over frames (zhichai.net SANA-WM summary, training pipeline
+ * Stage 3: the latent sequence is split across GPUs and the GDN transition maps
+ * are composed by prefix sums, exactly).  Per head, a range of frames maps any
+ * state S entering it to
+ *     A S + b,   A = A_{T-1} ... A_1 A_0,   A_t = g_t (I - K~_t^T diag(beta_t) K~_t),
+ * with b the state the range produces from a zero initial state.  A rank holding
+ * frames [t0, t1) of a sequence computes its range's (A, b) with
+ * gdn_frame_summary, the ranks exchange them (2 D^2 floats per head), each rank
+ * folds the maps of the ranges before its own onto the sequence's initial state
+ * with gdn_summary_apply, and then runs gdn_frame_fwd_ex on its frames from that
+ * state: its outputs are those of one call over the whole sequence up to
+ * rounding (the replayed frames take the same arithmetic; only the entering
+ * state is reached through composed maps).
+ */
+
+/* Flags of gdn_frame_summary. */
+#define GDN_SUMMARY_GATE_LOGITS 1 /* g and beta are logits (as gdn_frame_fwd_from_logits) */
+
+/*
+ * gdn_frame_summary -- the affine map (A, b) the T frames of every head apply to
+ * the state.
+ *   k, v, g, beta : as gdn_frame_fwd (q takes no part); with
+ *                   GDN_SUMMARY_GATE_LOGITS, g and beta are logits.
+ *   A_out, b_out  : [B, H, D, D] float32 each, written: A_out[i][j] maps key
+ *                   dim j of the entering state to key dim i of the leaving one;
+ *                   b_out is laid out as a state.  T = 0 gives A = I, b = 0.
+ *   workspace     : device memory of gdn_summary_workspace_bytes() bytes,
+ *                   256-byte aligned, owned by the caller (not read before it is
+ *                   written).
+ * The frames are cut into chunks of 16 whose maps are formed in parallel (for
+ * GDN_BF16 on the tensor cores, as the prefix form's summaries; for GDN_F32 on
+ * CUDA cores) and then composed in float32.  Returns GDN_OK, GDN_ERR_INVALID_ARG
+ * (bad counts, NULL pointers, unknown flags), GDN_ERR_UNSUPPORTED (D),
+ * GDN_ERR_MISALIGNED, GDN_ERR_WORKSPACE or GDN_ERR_CUDA; device-side timeouts
+ * through gdn_last_error.
+ */
+int gdn_frame_summary(const void* k, const void* v, const float* g, const float* beta,
+                      float* A_out, float* b_out,
+                      int B, int H, int T, int S, int D, int dtype, int flags,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* gdn_summary_workspace_bytes -- workspace gdn_frame_summary needs (0 for T = 0
+ * and for arguments it rejects). */
+size_t gdn_summary_workspace_bytes(int B, int H, int T, int S, int D, int dtype);
+
+/*
+ * gdn_summary_apply -- state_out = A state_in + b for every head, in float32:
+ * the state after a range of frames whose map gdn_frame_summary returned.
+ *   A, b      : [B, H, D, D] float32 (device).
+ *   state_in  : [B, H, D, D] float32, or NULL (zeros: state_out = b).
+ *   state_out : [B, H, D, D] float32, written; may alias state_in (each
+ *               head's block is read before it is written), not A or b.
+ * All pointers 16-byte aligned.  Returns GDN_OK, GDN_ERR_INVALID_ARG,
+ * GDN_ERR_UNSUPPORTED (D), GDN_ERR_MISALIGNED or GDN_ERR_CUDA.
+ */
+int gdn_summary_apply(const float* A, const float* b, const float* state_in, float* state_out,
+                      int B, int H, int D, void* stream);
+
+/*
  * gdn_last_error -- synchronises `stream`, then returns and clears the
  * device-side status word: GDN_OK, GDN_ERR_TIMEOUT (a kernel's bounded wait on
  * an mbarrier or a flag gave up; its results are invalid), or GDN_ERR_CUDA
@@ -325,16 +384,21 @@ int gdn_version(void);
  * point takes the same arguments as gdn_frame_fwd and runs the split form
  * (GDN_MODE_SPLIT, the form whose kernels use scratch memory), but it calls no
  * cudaMalloc, cudaFree or other allocating routine: its scratch is one fixed
- * array of
- * gdn_noalloc_scratch_bytes() bytes (64 MiB) in the library's own device
- * memory, which every GPU that loads the library holds until the process exits.
+ * array of gdn_noalloc_scratch_bytes() bytes (64 MiB) in the library's own
+ * device memory.  The array sits in a module of its own: with CUDA's lazy
+ * module loading (the default) a device reserves it when this entry point is
+ * first called there, and holds it until the process exits; with eager loading
+ * (CUDA_MODULE_LOADING=EAGER) every device the process uses reserves it when its
+ * context is created.  So make the first call before a caching allocator has
+ * taken the rest of the memory, or load eagerly.
  *   - Shapes whose scratch (gdn_workspace_bytes(..., GDN_MODE_SPLIT)) is
  *     larger than that are rejected with GDN_ERR_WORKSPACE before any CUDA call.
  *     At D = 112 that is about 490 frame-heads per call, e.g. 20 heads
  *     x 24 frames: chunk-causal rollouts of a few frames per call fit.
- *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *   - The first call on a device (and after a device reset, the first call in
+ *     the new context) loads the array's module and looks up its device
+ *     address with that device current, then caches it; make that first call
+ *     before any stream capture.
  *   - Every call, on every stream, shares the one array, and it keeps the last
  *     call's contents (each call writes its scratch before reading it, so nothing
  *     needs clearing).  Calls that overlap on the GPU race on it: serialise them

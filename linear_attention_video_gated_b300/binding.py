@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(PKG, "libgdn.so")
 
 GDN_F32, GDN_BF16 = 0, 1
 GDN_BWD_STATES_IN_WORKSPACE, GDN_BWD_GATE_LOGITS = 1, 2
+GDN_SUMMARY_GATE_LOGITS = 1
 GDN_MODE_SEQUENTIAL, GDN_MODE_PREFIX, GDN_MODE_SPLIT = 0, 1, 2
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_MISALIGNED",
           4: "GDN_ERR_CUDA", 5: "GDN_ERR_TIMEOUT", 6: "GDN_ERR_WORKSPACE"}
@@ -41,6 +42,9 @@ _SIGS = {
     "gdn_frame_bwd_from_logits": (_I, [_P] * 14 + [_I] * 6 + [_P, ctypes.c_size_t, _P]),
     "gdn_bwd_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
     "gdn_frame_bwd_ex": (_I, [_P] * 14 + [_I] * 7 + [_P, ctypes.c_size_t, _P]),
+    "gdn_frame_summary": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P, ctypes.c_size_t, _P]),
+    "gdn_summary_workspace_bytes": (ctypes.c_size_t, [_I, _I, _I, _I, _I, _I]),
+    "gdn_summary_apply": (_I, [_P, _P, _P, _P, _I, _I, _I, _P]),
     "gdn_last_error": (_I, [_P]),
     "gdn_selftest_wait_timeout": (_I, [ctypes.c_uint, _P]),
     "gdn_status_string": (ctypes.c_char_p, [_I]),
@@ -143,6 +147,20 @@ def gdn_bwd_workspace_bytes(B, H, T, S, D, dtype) -> int:
 
 def gdn_workspace_bytes(B, H, T, S, D, dtype, mode) -> int:
     return lib().gdn_workspace_bytes(B, H, T, S, D, dtype, mode)
+
+
+def gdn_frame_summary(k, v, g, beta, A_out, b_out, B, H, T, S, D, dtype, flags, workspace, workspace_bytes,
+                      stream) -> int:
+    return lib().gdn_frame_summary(k, v, g, beta, A_out, b_out, B, H, T, S, D, dtype, flags, workspace,
+                                   workspace_bytes, stream)
+
+
+def gdn_summary_workspace_bytes(B, H, T, S, D, dtype) -> int:
+    return lib().gdn_summary_workspace_bytes(B, H, T, S, D, dtype)
+
+
+def gdn_summary_apply(A, b, state_in, state_out, B, H, D, stream) -> int:
+    return lib().gdn_summary_apply(A, b, state_in, state_out, B, H, D, stream)
 
 
 def gdn_last_error(stream) -> int:
@@ -287,6 +305,43 @@ def relu_linear_fwd(q, k, v, state_in=None, mode=GDN_MODE_SEQUENTIAL, workspace=
     if rc != 0:
         raise GDNError(rc, "gdn_relu_linear_fwd")
     return out, state_out
+
+
+def frame_summary(k, v, g, beta, gate_logits=False, workspace=None, stream=None):
+    """gdn_frame_summary on torch CUDA tensors (k, v [B,H,T,S,D], g [B,H,T], beta
+    [B,H,T,S]): returns (A, b), each [B,H,D,D] float32, the map the frames apply
+    to the state, S -> A S + b."""
+    import torch
+
+    B, H, T, S, D = k.shape
+    dtype = {torch.float32: GDN_F32, torch.bfloat16: GDN_BF16}[k.dtype]
+    A = torch.empty((B, H, D, D), dtype=torch.float32, device=k.device)
+    b = torch.empty_like(A)
+    need = gdn_summary_workspace_bytes(B, H, T, S, D, dtype)
+    if workspace is None and need > 0:
+        workspace = torch.empty(need, dtype=torch.uint8, device=k.device)
+    strm = stream if stream is not None else torch.cuda.current_stream(k.device)
+    rc = gdn_frame_summary(_ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(A), _ptr(b), B, H, T, S, D, dtype,
+                           GDN_SUMMARY_GATE_LOGITS if gate_logits else 0, _ptr(workspace),
+                           0 if workspace is None else workspace.numel(), strm.cuda_stream)
+    if rc != 0:
+        raise GDNError(rc, "gdn_frame_summary")
+    return A, b
+
+
+def summary_apply(A, b, state_in=None, state_out=None, stream=None):
+    """gdn_summary_apply on torch CUDA tensors: state_out = A state_in + b per head
+    ([B,H,D,D] float32; state_in None means zeros).  Returns state_out."""
+    import torch
+
+    B, H, D, _ = A.shape
+    if state_out is None:
+        state_out = torch.empty_like(b)
+    strm = stream if stream is not None else torch.cuda.current_stream(A.device)
+    rc = gdn_summary_apply(_ptr(A), _ptr(b), _ptr(state_in), _ptr(state_out), B, H, D, strm.cuda_stream)
+    if rc != 0:
+        raise GDNError(rc, "gdn_summary_apply")
+    return state_out
 
 
 def frame_bwd(q, k, v, g, beta, dout, state_in=None, dstate_out=None, gate_logits=False, workspace=None,

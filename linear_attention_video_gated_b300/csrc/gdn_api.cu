@@ -1,5 +1,7 @@
 // C ABI of libgdn (declared in include/gdn.h): argument validation, workspace
 // management and dispatch to the float32 SIMT path or the bf16 tensor-core path.
+#include <cuda.h>
+
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -13,22 +15,53 @@ namespace gdn {
 
 __device__ unsigned int g_device_status = 0;
 
-namespace {
-
-// Device address of the status word on the current device (cached per device).
-unsigned int* status_word() {
-  static unsigned int* cache[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!cache[dev]) {
+// The driver context current on this thread (nullptr if none or on failure).
+// A symbol's device address belongs to the context the module was loaded in: a
+// cudaDeviceReset or a primary-context teardown unloads the module, and the next
+// context loads it again, possibly elsewhere.
+void* current_context() {
+  using Fn = CUresult (*)(CUcontext*);
+  static Fn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
     void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_device_status) != cudaSuccess) return nullptr;
-    cache[dev] = static_cast<unsigned int*>(ptr);
-  }
-  return cache[dev];
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<Fn>(ptr);
+  });
+  CUcontext ctx = nullptr;
+  if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
 }
 
-bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+void* SymbolAddressCache::get(const void* symbol) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  void* ctx = current_context();
+  if (!ctx) {  // no context current yet: the runtime makes the device's primary one current
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, symbol) != cudaSuccess) return nullptr;
+    ctx = current_context();
+    if (!ctx) return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(mu_);
+  if (ctx_[dev] != ctx || !ptr_[dev]) {
+    void* ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, symbol) != cudaSuccess) return nullptr;
+    ctx_[dev] = ctx;
+    ptr_[dev] = ptr;
+  }
+  return ptr_[dev];
+}
+
+namespace {
+
+// Device address of the status word in the current device's current context.
+unsigned int* status_word() {
+  static SymbolAddressCache cache;
+  return static_cast<unsigned int*>(cache.get(reinterpret_cast<const void*>(&g_device_status)));
+}
 
 // Validates everything that can be checked on the host.  Fills `p`.
 int validate(const void* q, const void* k, const void* v, const float* g, const float* beta,
@@ -284,59 +317,3 @@ int gdn_profile_end(gdn_kernel_stat_t* stats, int max_stats, int* n_stats) {
 }
 
 }  // extern "C"
-
-// ---- entry point that allocates nothing ------------------------------------------
-//
-// gdn_frame_fwd_noalloc runs the split form (the kernels that use scratch), but
-// its scratch is a fixed array in the library's own device memory instead of
-// memory taken from an allocator.  It exists for callers that cannot call cudaMalloc: code
-// plugged into another runtime that owns the device memory (its caching
-// allocator has reserved the HBM, so a raw cudaMalloc fails or fragments the
-// pool), and latency-critical loops in which an allocation or free that
-// synchronises the device would stall unrelated streams.
-namespace gdn {
-namespace {
-
-// Every GPU that loads libgdn.so holds this array until the process exits.
-constexpr size_t kStaticScratchBytes = size_t(64) << 20;  // 64 MiB
-__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
-
-// Device address of g_static_scratch on the current device.  In host code the
-// array's name is only a host-side stand-in, so the address is looked up once
-// per device (with that device current) and cached.
-void* static_scratch_address() {
-  static std::mutex mu;
-  static void* cache[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!cache[dev]) {
-    void* ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess) return nullptr;
-    cache[dev] = ptr;
-  }
-  return cache[dev];
-}
-
-}  // namespace
-}  // namespace gdn
-
-extern "C" int gdn_frame_fwd_noalloc(const void* q, const void* k, const void* v, const float* g,
-                                     const float* beta, const float* state_in, void* out, float* state_out, int B,
-                                     int H, int T, int S, int D, int dtype, void* stream) {
-  gdn::Problem p{};
-  int rc = gdn::validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, GDN_MODE_SPLIT, &p);
-  if (rc != gdn::kOk) return rc;
-  // Every stage writes its scratch before reading it, so the previous call's
-  // contents never need clearing.
-  const size_t need = gdn::workspace_for(p);
-  if (need > gdn::kStaticScratchBytes) return GDN_ERR_WORKSPACE;
-  void* ws = nullptr;
-  if (need > 0) {
-    ws = gdn::static_scratch_address();
-    if (!ws) return GDN_ERR_CUDA;
-  }
-  return gdn::forward(p, ws, static_cast<cudaStream_t>(stream));
-}
-
-extern "C" size_t gdn_noalloc_scratch_bytes(void) { return gdn::kStaticScratchBytes; }

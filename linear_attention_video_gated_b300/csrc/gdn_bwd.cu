@@ -459,11 +459,17 @@ int run_bwd(const Problem& p, const Grads& gr, void* ws, cudaStream_t st, bool s
   return launch_dg_sum(dg_part, p.g, gr.dg, p.BHT(), L.ntiles, p.gate_logits, st);
 }
 
+// The backward's own layout, and never less than any forward form needs for the
+// shape, so one workspace serves a forward call and the backward that reuses its
+// states.
 size_t workspace_of(const Problem& p) {
-  return p.dtype == GDN_BF16 ? tc_bwd_workspace_bytes(p) : bwd_layout(p).total;
+  const size_t own = p.dtype == GDN_BF16 ? tc_bwd_workspace_bytes(p) : bwd_layout(p).total;
+  Problem pf = p;
+  pf.mode = GDN_MODE_PREFIX;  // the largest forward form
+  const size_t fwd = scratch_bytes(pf);
+  return own > fwd ? own : fwd;
 }
 
-bool aligned(const void* ptr, uintptr_t a) { return (reinterpret_cast<uintptr_t>(ptr) & (a - 1)) == 0; }
 
 // Validation shared by gdn_frame_bwd and gdn_bwd_workspace_bytes; fills p and gr.
 int check_bwd(const void* q, const void* k, const void* v, const float* g, const float* beta, const float* state_in,

@@ -19,6 +19,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace gdn {
 
 struct Problem {
@@ -78,12 +80,28 @@ __device__ __forceinline__ void report_device_error(unsigned int* status, unsign
 int check_args(const void* q, const void* k, const void* v, const float* g, const float* beta,
                const float* state_in, void* out, float* state_out, int B, int H, int T, int S, int D, int dtype,
                int mode, Problem* p, bool need_gates = true);
-// Scratch bytes the call `p` needs.
-size_t scratch_bytes(const Problem& p);
 // Enqueues the call on `st` (scratch `ws` of scratch_bytes(p) bytes).
 int run_forward(const Problem& p, void* ws, cudaStream_t st);
 // Device address of the status word on the current device (nullptr on failure).
 unsigned int* device_status_word();
+// Scratch bytes the call `p` needs.
+size_t scratch_bytes(const Problem& p);
+
+// Device addresses of a __device__ variable, looked up (cudaGetSymbolAddress)
+// once per device and context and cached: a symbol's name in host code is only
+// a host-side stand-in, and its address changes if the context is torn down
+// and re-created.  Thread-safe.
+class SymbolAddressCache {
+ public:
+  // The address of `symbol` (the address of the __device__ variable as host
+  // code names it) in the current device's current context; nullptr on failure.
+  void* get(const void* symbol);
+ private:
+  static constexpr int kMaxDevices = 64;
+  std::mutex mu_;
+  void* ctx_[kMaxDevices] = {nullptr};
+  void* ptr_[kMaxDevices] = {nullptr};
+};
 
 // ---- SIMT path (float32 arithmetic; used for float32 I/O) --------------------
 size_t simt_workspace_bytes(const Problem& p, int mode);
@@ -92,9 +110,28 @@ int simt_forward(const Problem& p, void* ws, cudaStream_t st);
 // major), by the sequential scan; writes p.state_out when it is not null.
 int simt_states(const Problem& p, float* Mws, float* bws, float* Sws, cudaStream_t st);
 
+// Per-chunk composed maps [A_c | b_c] (BH x nchunks x D x 2D float32, in `ws`,
+// which holds at least simt_workspace_bytes(p, GDN_MODE_PREFIX) bytes) of
+// 16-frame chunks: the float32 gram and composition.
+int simt_chunk_maps(const Problem& p, void* ws, float** maps, int* nchunks, cudaStream_t st);
+
+// Fold of affine maps over chunks in float32 (gdn_simt.cu): per head,
+// x_{c+1} = A_c x_c + b_c for c = 0 .. nchunks - 1, with A_c at A + (head *
+// nchunks + c) * chunk_stride (rows `ld` floats apart) and b_c likewise from b.
+// Boundary form (A_out null): x_0 = state_in (zeros if null); x_c -> starts (if
+// set), the last x -> x_out (if set; may alias state_in).  Summary form: the
+// composed map of all chunks -> A_out, b_out ([BH][D][D] each).
+int launch_chunk_fold(const float* A, const float* b, long long chunk_stride, int ld, int nchunks,
+                      const float* state_in, float* starts, float* x_out, float* A_out, float* b_out, long long BH,
+                      int D, cudaStream_t st);
+
 // ---- tensor-core path (bf16 I/O) ------------------------------------------------
 size_t tc_workspace_bytes(const Problem& p, int mode);
 int tc_forward(const Problem& p, void* ws, cudaStream_t st);
+// Per-chunk composed maps [A_c | b_c] of kTcChunkFrames-frame chunks on the tensor
+// cores (the gram, then the chunked scan's summary form), in `ws` of at least
+// tc_workspace_bytes(p, GDN_MODE_PREFIX) bytes.
+int tc_chunk_maps(const Problem& p, void* ws, float** maps, int* nchunks, cudaStream_t st);
 
 // ---- backward pass (gdn_bwd.cu; the bf16 kernels in gdn_tc.cu) -------------------
 struct BwdGrads {
@@ -116,6 +153,7 @@ int launch_dg_sum(const float* dg_part, const float* g, float* dg, long long nfr
                   cudaStream_t st);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
 // Brackets one kernel launch with CUDA events while gdn_profile_begin() is in
 // effect (no-op otherwise).  Construct immediately before the launch.

@@ -16,6 +16,7 @@
 // head, over chunks) -> replay (per head and chunk, parallel) -> readout.
 #include <cuda_bf16.h>
 
+#include "../../include/gdn.h"
 #include "gdn_internal.h"
 
 namespace gdn {
@@ -324,6 +325,99 @@ __global__ void __launch_bounds__(kThreads) readout_kernel(const TIn* __restrict
   }
 }
 
+// Fold of affine maps over chunks, float32 (used by both I/O dtypes): per head,
+// x_{c+1} = A_c x_c + b_c for c = 0 .. nchunks - 1.  One CTA per (head, 16-column
+// block of x): columns of x evolve independently, so a CTA holds its D x 16 block
+// in registers (thread i = row i) and stages each A_c in shared memory.
+//   boundary form (A_out null): x_0 = state_in (or zeros); writes x_c into
+//     `starts` (the initial state of every chunk) and the last x into `x_out`.
+//   summary form (A_out set): the composed map of all chunks, [A | b]: 2 D/16
+//     column blocks per head, the first D columns starting as the identity and
+//     taking no b term (A = A_{n-1} ... A_0), the last D starting at zero (b).
+struct FoldArgs {
+  const float* A;
+  const float* b;
+  long long chunk_stride;  // floats between consecutive chunk maps (and heads: nchunks of them)
+  int ld;                  // floats between rows of A_c and of b_c
+  int nchunks, D;
+  const float* state_in;
+  float* starts;
+  float* x_out;
+  float* A_out;
+  float* b_out;
+};
+
+constexpr int kFoldThreads = 128;
+
+__global__ void __launch_bounds__(kFoldThreads) chunk_fold_kernel(FoldArgs a) {
+  extern __shared__ float fsm[];
+  const int D = a.D, ncb = D / 16;
+  float* sA = fsm;                // [D][D + 1]: the padding keeps row reads conflict-free
+  float* sx = sA + D * (D + 1);   // [D][16]
+  const bool summary = a.A_out != nullptr;
+  const int ncbx = summary ? 2 * ncb : ncb;
+  const long long bh = blockIdx.x / ncbx;
+  const int cbx = (int)(blockIdx.x % ncbx);
+  const bool ident = summary && cbx < ncb;
+  const int cb = cbx < ncb ? cbx : cbx - ncb;
+  const int i = threadIdx.x;
+  const bool row = i < D;
+  float x[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) x[j] = (ident && i == 16 * cb + j) ? 1.f : 0.f;
+  if (!summary && a.state_in && row) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) x[j] = a.state_in[((size_t)bh * D + i) * D + 16 * cb + j];
+  }
+  for (int c = 0; c < a.nchunks; ++c) {
+    const size_t mo = (size_t)(bh * a.nchunks + c) * a.chunk_stride;
+    if (row) {
+      if (a.starts) {
+        float* dst = a.starts + ((size_t)(bh * a.nchunks + c) * D + i) * D + 16 * cb;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) dst[j] = x[j];
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) sx[i * 16 + j] = x[j];
+      const float4* ar = reinterpret_cast<const float4*>(a.A + mo + (size_t)i * a.ld);
+      for (int k4 = 0; k4 < D / 4; ++k4) {
+        const float4 w = ar[k4];
+        sA[i * (D + 1) + 4 * k4] = w.x;
+        sA[i * (D + 1) + 4 * k4 + 1] = w.y;
+        sA[i * (D + 1) + 4 * k4 + 2] = w.z;
+        sA[i * (D + 1) + 4 * k4 + 3] = w.w;
+      }
+    }
+    __syncthreads();
+    if (row) {
+      float y[16];
+      const float* br = a.b + mo + (size_t)i * a.ld + 16 * cb;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) y[j] = ident ? 0.f : br[j];
+      for (int k = 0; k < D; ++k) {
+        const float aik = sA[i * (D + 1) + k];
+        const float4* xr = reinterpret_cast<const float4*>(sx + k * 16);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 w = xr[q];
+          y[4 * q] = fmaf(aik, w.x, y[4 * q]);
+          y[4 * q + 1] = fmaf(aik, w.y, y[4 * q + 1]);
+          y[4 * q + 2] = fmaf(aik, w.z, y[4 * q + 2]);
+          y[4 * q + 3] = fmaf(aik, w.w, y[4 * q + 3]);
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) x[j] = y[j];
+    }
+    __syncthreads();
+  }
+  float* dst = summary ? (ident ? a.A_out : a.b_out) : a.x_out;
+  if (row && dst) {
+#pragma unroll
+    for (int j = 0; j < 16; ++j) dst[((size_t)bh * D + i) * D + 16 * cb + j] = x[j];
+  }
+}
+
 struct SimtLayout {
   size_t m_off, b_off, s_off, maps_off, starts_off, total;
   int nchunks;
@@ -435,7 +529,54 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
 
 }  // namespace
 
+int launch_chunk_fold(const float* A, const float* b, long long chunk_stride, int ld, int nchunks,
+                      const float* state_in, float* starts, float* x_out, float* A_out, float* b_out, long long BH,
+                      int D, cudaStream_t st) {
+  const int smem = (D * (D + 1) + D * 16) * (int)sizeof(float);
+  if (cudaFuncSetAttribute(chunk_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return kCuda;
+  FoldArgs fa{A, b, chunk_stride, ld, nchunks, D, state_in, starts, x_out, A_out, b_out};
+  const long long ctas = BH * (D / 16) * (A_out ? 2 : 1);
+  ProfScope ps(st, A_out ? "chunk_fold_summary" : "chunk_fold");
+  chunk_fold_kernel<<<(unsigned)ctas, kFoldThreads, smem, st>>>(fa);
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
+
 size_t simt_workspace_bytes(const Problem& p, int mode) { return simt_layout(p, mode).total; }
+
+int simt_chunk_maps(const Problem& p, void* ws, float** maps, int* nchunks, cudaStream_t st) {
+  const SimtLayout L = simt_layout(p, GDN_MODE_PREFIX);
+  char* w = static_cast<char*>(ws);
+  float* Mws = reinterpret_cast<float*>(w + L.m_off);
+  float* bws = reinterpret_cast<float*>(w + L.b_off);
+  const int D = p.D;
+  const size_t mat = (size_t)D * D * sizeof(float);
+  {
+    ProfScope pg(st, "simt_gram");
+    if (p.dtype == GDN_F32)
+      gram_kernel<float><<<dim3((unsigned)p.BHT(), 2), kThreads, 2 * kTok * D * sizeof(float), st>>>(
+          static_cast<const float*>(p.k), static_cast<const float*>(p.v), p.beta, Mws, bws, p.S, D, p.key_scale,
+          p.gate_logits, p.variant);
+    else
+      gram_kernel<__nv_bfloat16><<<dim3((unsigned)p.BHT(), 2), kThreads, 2 * kTok * D * sizeof(float), st>>>(
+          static_cast<const __nv_bfloat16*>(p.k), static_cast<const __nv_bfloat16*>(p.v), p.beta, Mws, bws, p.S, D,
+          p.key_scale, p.gate_logits, p.variant);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  float* mp = reinterpret_cast<float*>(w + L.maps_off);
+  const size_t csmem = 3 * mat;
+  if (cudaFuncSetAttribute(compose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)csmem) != cudaSuccess)
+    return kCuda;
+  {
+    ProfScope pc(st, "simt_compose");
+    compose_kernel<<<(unsigned)(p.BH() * L.nchunks), kThreads, csmem, st>>>(Mws, bws, p.g, mp, p.T, D, L.nchunks,
+                                                                             p.gate_logits, p.variant);
+  }
+  if (cudaGetLastError() != cudaSuccess) return kCuda;
+  *maps = mp;
+  *nchunks = L.nchunks;
+  return kOk;
+}
 
 int simt_forward(const Problem& p, void* ws, cudaStream_t st) {
   if (p.dtype == 0) return run<float>(p, ws, st);

@@ -25,6 +25,7 @@
 
 #include <mutex>
 
+#include "../../include/gdn.h"
 #include "gdn_internal.h"
 #include "ptx.cuh"
 
@@ -47,9 +48,12 @@ __host__ __device__ inline int num_atoms(int D) { return (D + 63) / 64; }
 struct TcLayout {
   size_t m_off, b_off, s_off, total;
   size_t m_bytes, b_bytes, s_bytes;  // per frame-head
+  size_t maps_off, starts_off;       // prefix form: chunk maps [A|b] and chunk starts
 };
 
-TcLayout tc_layout(const Problem& p) {
+constexpr int kTcChunkFrames = 16;  // frames per chunk of the prefix form
+
+TcLayout tc_layout(const Problem& p, int mode = GDN_MODE_SPLIT) {
   TcLayout L{};
   const int NA = num_atoms(p.D);
   L.m_bytes = (size_t)NA * p.D * 128;      // M_t image: NA regions of D rows x 128 B
@@ -60,6 +64,13 @@ TcLayout tc_layout(const Problem& p) {
   L.b_off = align_up(L.m_off + F * L.m_bytes, 1024);
   L.s_off = align_up(L.b_off + F * L.b_bytes, 1024);
   L.total = align_up(L.s_off + F * L.s_bytes, 1024);
+  if (mode == GDN_MODE_PREFIX) {
+    const size_t nch = (size_t)((p.T + kTcChunkFrames - 1) / kTcChunkFrames);
+    const size_t mat = (size_t)p.D * p.D * 4;
+    L.maps_off = L.total;
+    L.starts_off = align_up(L.maps_off + (size_t)p.BH() * nch * 2 * mat, 1024);
+    L.total = align_up(L.starts_off + (size_t)p.BH() * nch * mat, 1024);
+  }
   return L;
 }
 
@@ -177,6 +188,8 @@ constexpr int kGramRaw = 4;
 constexpr int kGramConv = 2;
 constexpr int kRawStage = 4 * kGramRegion;   // K atoms (NA) then V atoms (NA): 32 KB
 constexpr int kConvStage = 4 * kGramRegion;  // AH atoms (2) then AL atoms (2): 32 KB
+constexpr int kBetaAhead = 3;                // beta fetched this many 64-token chunks ahead
+constexpr int kBetaRing = (kBetaAhead + 1) * kGramTok * 4;  // its shared-memory ring, bytes
 
 struct GramArgs {
   const float* beta;
@@ -202,7 +215,8 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   uint8_t* raw = smem;
   uint8_t* conv = raw + kGramRaw * kRawStage;
   uint8_t* mstage = conv + kGramConv * kConvStage;  // NA x D rows x 128 B
-  uint64_t* bars = reinterpret_cast<uint64_t*>(mstage + NA * D * 128);
+  float* bring = reinterpret_cast<float*>(mstage + NA * D * 128);  // beta: (kBetaAhead + 1) x 64 tokens
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(bring) + kBetaRing);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + kGramRaw;
   uint64_t* conv_full = raw_empty + kGramRaw;
@@ -320,29 +334,44 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     int rs = 0, cs = 0;
     uint32_t rph = 0, cph = 0;
     const int units = NA * kGramTok * 8;  // 16-byte chunks of K per tile
-    // This thread's chunks lie in tile rows r0 and r0 + 32; their beta values are
-    // loaded one tile ahead so the load latency stays off the critical path.
+    // This thread's chunks lie in tile rows r0 and r0 + 32.  Their beta values
+    // reach shared memory by asynchronous copies kBetaAhead chunks ahead (one
+    // lane of each group of 8 fetches its rows for the warp), so no register
+    // waits on a global load.  Rows past S (or past the last frame-head) read
+    // as -inf, which maps to 0.
     const int r0 = ct >> 3;
-    auto beta_at = [&](long long f, int c, int rw) {
-      const int s = c * kGramTok + rw;
-      // raw value, mapped when used: mapping here would wait for the load
-      if (!(f < a.nitems && s < S)) return -INFINITY;
-      return (a.variant == kReluLinear || a.b_only) ? 1.f : __ldg(a.beta + f * S + s);
+    const bool unit_beta = a.variant == kReluLinear || a.b_only;
+    const bool copier = (lane & 7) == 0 && !unit_beta;
+    long long fl = blockIdx.x;  // the chunk whose beta is fetched next
+    int cl = 0;
+    auto fetch = [&](int slot) {
+      if (copier) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int rw = r0 + 32 * h;
+          const int s = cl * kGramTok + rw;
+          float* dst = bring + slot * kGramTok + rw;
+          if (fl < a.nitems && s < S)
+            cp_async4(smem_u32(dst), a.beta + fl * S + s);
+          else
+            *dst = -INFINITY;
+        }
+      }
+      cp_async_commit();
+      if (++cl == nchunks) { cl = 0; fl += gridDim.x; }
     };
-    long long fn = blockIdx.x;
-    int cn = 0;
-    // beta of token rows r0 and r0 + 32: raw values loaded one tile ahead, mapped
-    // (rows past S, loaded as -inf, give 0) after the current tile is converted.
-    auto mapped = [&](float x) {
-      return x == -INFINITY ? 0.f : ((a.variant == kReluLinear || a.b_only) ? x : beta_of(x, a.gate_logits));
-    };
-    float bn0 = beta_at(fn, 0, r0), bn1 = beta_at(fn, 0, r0 + 32);
-    float b0 = mapped(bn0), b1 = mapped(bn1);
+    auto mapped = [&](float x) { return x == -INFINITY ? 0.f : beta_of(x, a.gate_logits); };
+    for (int d = 0; d < kBetaAhead; ++d) fetch(d);
+    int n = 0;  // chunks converted so far
     for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
-      for (int c = 0; c < nchunks; ++c) {
-        if (++cn == nchunks) { cn = 0; fn += gridDim.x; }
-        bn0 = beta_at(fn, cn, r0);
-        bn1 = beta_at(fn, cn, r0 + 32);
+      for (int c = 0; c < nchunks; ++c, ++n) {
+        __syncwarp();  // every lane has read the slot the next fetch overwrites
+        fetch((n + kBetaAhead) % (kBetaAhead + 1));
+        cp_async_wait<kBetaAhead>();  // this chunk's copies have landed
+        __syncwarp();
+        const float* bsl = bring + (n % (kBetaAhead + 1)) * kGramTok;
+        const float b0 = unit_beta ? (c * kGramTok + r0 < S ? 1.f : 0.f) : mapped(bsl[r0]);
+        const float b1 = unit_beta ? (c * kGramTok + r0 + 32 < S ? 1.f : 0.f) : mapped(bsl[r0 + 32]);
         const bool ok = wait_or_abort(smem_u32(&raw_full[rs]), rph, abort_flag, a.status) &&
                         wait_or_abort(smem_u32(&conv_empty[cs]), cph ^ 1, abort_flag, a.status);
         if (!__all_sync(0xffffffffu, ok)) goto done;
@@ -366,8 +395,6 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&conv_full[cs]));
         if (++rs == kGramRaw) { rs = 0; rph ^= 1; }
         if (++cs == kGramConv) { cs = 0; cph ^= 1; }
-        b0 = mapped(bn0);
-        b1 = mapped(bn1);
       }
     }
   } else {
@@ -424,6 +451,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     }
   }
 done:
+  cp_async_wait_all();  // the beta copies still in flight (converter lanes) have landed
   if (threadIdx.x == 0) bulk_wait0();  // M image stores complete
   if (warp == 13 && lane == 0) {  // every MMA this CTA issued has completed
     mma_commit(smem_u32(mma_done));
@@ -444,11 +472,20 @@ done:
 // CTAs, CTA c owning the value columns J = [16c, 16c + 16): no communication.
 // Per frame: P = M_t S_{t-1}[:, J] on the tensor core (A = the M_t image, B =
 // the state block as bf16 hi and lo side by side, N = 32, the two halves summed
-// in the epilogue), then the update in fp32 registers (thread i = state row i).  M_t and the b_t block stream in through a 4-deep ring of
-// bulk copies; the new state block goes back to the read-out's S_t image with
-// bulk stores (hi / lo, NA atoms, rows 16c .. 16c + 15 of each).
+// in the epilogue), then the update in fp32 registers (thread i = state row i).
+// M_t and the b_t block stream in through a ring of bulk copies; the new state
+// block goes back to the read-out's S_t image with bulk stores (hi / lo, NA
+// atoms, rows 16c .. 16c + 15 of each).
+//
+// Chunked forms (the prefix composition of the affine maps; zhichai.net SANA-WM
+// summary, training pipeline Stage 3): the frames of a head are cut into chunks
+// of `chunk` frames, one CTA per (head, chunk, column block), all in parallel.
+//   summary : each chunk's composed map [A_c | b_c] (S_end = A_c S_start + b_c):
+//             the A columns start as the identity's columns and take no b_t
+//             term, the b columns start at zero; written to `maps`.
+//   replay  : each chunk from its true initial state (`starts`), writing the
+//             S_t images as the single pass does.
 // =============================================================================
-constexpr int kScanStages = 4;
 constexpr int kScanThreads = 192;         // 4 epilogue, 1 copy, 1 MMA warps
 constexpr int kScanMStage = 2 * 128 * 128;  // M image: 2 atoms x 128 rows x 128 B
 constexpr int kScanBStage = 128 * 64;       // b block: up to 128 rows x 16 floats
@@ -468,32 +505,52 @@ struct ScanArgs {
   // 1: the backward pass's state-gradient scan, U_{t-1} = g_t (U_t - M_t U_t) + E_{t-1}
   // over t = T-1 .. 0.  b_blk holds E; state_in is dS_T and the scan starts from
   // U_{T-1} = dS_T + E_{T-1}; image slot t receives U_t (t = T-1 .. 0); state_out
-  // receives dS_0 = g_0 (U_0 - M_0 U_0).
+  // receives dS_0 = g_0 (U_0 - M_0 U_0).  Not chunked.
   int reverse;
+  // Chunking: frames per chunk and the number of chunks (T and 1 for one pass).
+  int chunk, nchunks;
+  // replay: the initial state of every chunk, [BH][nchunks][D][D] float32
+  // (null: state_in, for one pass).  state_out is written by the last chunk.
+  const float* starts;
+  // summary: [BH][nchunks][D][2D] float32, row i = [A_c row i | b_c row i]; the
+  // grid then has 2 D/16 column blocks per chunk (A's, then b's) and no image or
+  // state_out is written.
+  float* maps;
 };
 
-__global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
+template <int STAGES>
+__global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_kernel(ScanArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int NA = a.NA, D = a.D, T = a.T;
   const int ncb = D / 16, KS = D / 16;
   uint8_t* mring = smem;
-  uint8_t* bring = mring + kScanStages * kScanMStage;
-  uint8_t* img = bring + kScanStages * kScanBStage;  // 2 buffers
+  uint8_t* bring = mring + STAGES * kScanMStage;
+  uint8_t* img = bring + STAGES * kScanBStage;  // 2 buffers
   uint64_t* bars = reinterpret_cast<uint64_t*>(img + 2 * kScanImg);
   uint64_t* full = bars;
-  uint64_t* empty = full + kScanStages;
-  uint64_t* pfull = empty + kScanStages;
+  uint64_t* empty = full + STAGES;
+  uint64_t* pfull = empty + STAGES;
   uint64_t* sready = pfull + 1;
   uint64_t* mma_done = sready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  const long long bh = blockIdx.x / ncb;
-  const int cb = blockIdx.x % ncb;
+  // block -> (head, chunk, column block); in summary form column blocks 0 .. ncb-1
+  // are A's (identity start, no b term), ncb .. 2 ncb - 1 are b's
+  const int ncbx = a.maps ? 2 * ncb : ncb;
+  const int cbx = (int)(blockIdx.x % ncbx);
+  const long long hc = blockIdx.x / ncbx;
+  const int chunk_id = (int)(hc % a.nchunks);
+  const long long bh = hc / a.nchunks;
+  const bool ident = a.maps != nullptr && cbx < ncb;
+  const int cb = cbx < ncb ? cbx : cbx - ncb;
+  const int t0 = chunk_id * a.chunk;
+  const int nsteps = min(T, t0 + a.chunk) - t0;
+  const bool use_b = !ident;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kScanStages; ++s) {
+    for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
       mbar_init(smem_u32(&empty[s]), 5);  // the MMA's commit + the 4 epilogue warps (b read)
     }
@@ -504,7 +561,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     fence_mbar_init();
   }
   // M image rows D..127 (never copied in) must be finite: zero them once.
-  for (int idx = threadIdx.x; idx < kScanStages * kScanMStage / 16; idx += blockDim.x)
+  for (int idx = threadIdx.x; idx < STAGES * kScanMStage / 16; idx += blockDim.x)
     reinterpret_cast<uint4*>(mring)[idx] = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   if (warp == 5) {
@@ -519,20 +576,21 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
   if (warp == 4) {
     // ---------------- copies in: M_t image (NA atoms of D rows) and the b_t block
     if (lane == 0) {
-      Ring<kScanStages> r;
-      for (int j = 0; j < T; ++j) {
+      Ring<STAGES> r;
+      for (int j = 0; j < nsteps; ++j) {
         if (!wait_or_abort(smem_u32(&empty[r.stage]), r.phase ^ 1, abort_flag, a.status)) break;
-        const int t = a.reverse ? T - 1 - j : j;
+        const int t = a.reverse ? T - 1 - j : t0 + j;
         const long long f = bh * T + t;
         // the b term of step j: b_t forward, E_{t-1} in reverse (frame 0's block,
         // unused, stands in for E_{-1})
         const long long fbk = a.reverse ? bh * T + (t > 0 ? t - 1 : 0) : f;
         const uint32_t fb = smem_u32(&full[r.stage]);
-        mbar_arrive_expect_tx(fb, NA * D * 128 + D * 64);
+        mbar_arrive_expect_tx(fb, NA * D * 128 + (use_b ? D * 64 : 0));
         const uint8_t* src = a.m_img + (size_t)f * NA * D * 128;
         for (int at = 0; at < NA; ++at)
           bulk_g2s(smem_u32(mring + r.stage * kScanMStage + at * 128 * 128), src + at * D * 128, D * 128, fb);
-        bulk_g2s(smem_u32(bring + r.stage * kScanBStage), a.b_blk + ((size_t)fbk * ncb + cb) * D * 16, D * 64, fb);
+        if (use_b)
+          bulk_g2s(smem_u32(bring + r.stage * kScanBStage), a.b_blk + ((size_t)fbk * ncb + cb) * D * 16, D * 64, fb);
         r.mark_issued();
         r.advance();
       }
@@ -542,11 +600,13 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     // ---------------- MMA: P = M_t S_{t-1}[:, J]
     if (lane == 0) {
       const uint32_t id = idesc_bf16(128, 32, 0, 0);
+      const bool store = a.s_img != nullptr;
       // the state block after step u (image buffer (u + 1) & 1; u = -1 is the
-      // initial state) to global memory, laid out as in shared memory: slot u, or
-      // in reverse slot T - 2 - u (the frame index of the gradient U it holds)
+      // initial state) to global memory, laid out as in shared memory: the slot
+      // of frame t0 + u, or in reverse slot T - 2 - u (the frame index of the
+      // gradient U it holds)
       auto store_block = [&](int u) {
-        const long long f = bh * T + (a.reverse ? T - 2 - u : u);
+        const long long f = bh * T + (a.reverse ? T - 2 - u : t0 + u);
         bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(img + ((u + 1) & 1) * kScanImg),
                  NA * 32 * 128);
         bulk_commit();
@@ -561,25 +621,25 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
       }
       int stage = 0;
       uint32_t phase = 0;
-      for (int t = 0; t < T; ++t) {
+      for (int j = 0; j < nsteps; ++j) {
         if (!wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status)) goto done;
-        if (!wait_or_abort(smem_u32(sready), t & 1, abort_flag, a.status)) goto done;
+        if (!wait_or_abort(smem_u32(sready), j & 1, abort_flag, a.status)) goto done;
         tc_fence_after();
         const uint64_t ao = (uint64_t)((stage * kScanMStage) >> 4);
-        const uint64_t bo = (uint64_t)(((t & 1) * kScanImg) >> 4);
+        const uint64_t bo = (uint64_t)(((j & 1) * kScanImg) >> 4);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           if (kk < KS) mma_bf16(tmem, ad0[kk] + ao, bd0[kk] + bo, id, kk > 0 ? 1u : 0u);
-        if (t >= 1 || a.reverse) store_block(t - 1);
-        // The store of S_{t-2} has read its buffer, which S_t may now overwrite.
+        if (store && (j >= 1 || a.reverse)) store_block(j - 1);
+        // The store of S_{j-2} has read its buffer, which S_j may now overwrite.
         asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         mma_commit(smem_u32(pfull));
         mma_commit(smem_u32(&empty[stage]));
-        if (++stage == kScanStages) { stage = 0; phase ^= 1; }
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
       }
-      if (T > 0 && !a.reverse) {  // the reverse scan's last result is dS_0 (state_out only)
-        if (!wait_or_abort(smem_u32(sready), T & 1, abort_flag, a.status)) goto done;
-        store_block(T - 1);
+      if (store && nsteps > 0 && !a.reverse) {  // the reverse scan's last result is dS_0 (state_out only)
+        if (!wait_or_abort(smem_u32(sready), nsteps & 1, abort_flag, a.status)) goto done;
+        store_block(nsteps - 1);
       }
     }
   } else {
@@ -588,9 +648,11 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     const bool row = i < D;
     float x[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) x[j] = 0.f;
-    if (row && a.state_in) {
-      const float4* si = reinterpret_cast<const float4*>(a.state_in + ((size_t)bh * D + i) * D + 16 * cb);
+    for (int j = 0; j < 16; ++j) x[j] = (ident && i == 16 * cb + j) ? 1.f : 0.f;
+    const float* s_init = a.starts ? a.starts + (size_t)(bh * a.nchunks + chunk_id) * D * D
+                                   : (a.maps ? nullptr : (a.state_in ? a.state_in + (size_t)bh * D * D : nullptr));
+    if (row && s_init) {
+      const float4* si = reinterpret_cast<const float4*>(s_init + (size_t)i * D + 16 * cb);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const float4 w = si[q];
@@ -626,7 +688,7 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
         *reinterpret_cast<uint16_t*>(at + sw128_off(17 + n, i & 63)) = (uint16_t)(lv >> 16);
       }
     };
-    write_img(img);  // S_{-1} into buffer 0
+    write_img(img);  // the initial state into buffer 0
     fence_proxy_async_smem();
     __syncwarp();
     if (lane == 0) mbar_arrive(smem_u32(sready));
@@ -634,14 +696,14 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
     uint32_t phase = 0;
     const bool relu_lin = a.variant == kReluLinear;  // g = 1, no delta-rule term
     // raw decay of the next step's frame; mapped when used
-    float gnext = (T > 0 && !relu_lin) ? __ldg(a.g + bh * T + (a.reverse ? T - 1 : 0)) : 0.f;
-    for (int t = 0; t < T; ++t) {  // t counts steps; the step's frame is fr
-      const int fr = a.reverse ? T - 1 - t : t;
+    float gnext = (nsteps > 0 && !relu_lin) ? __ldg(a.g + bh * T + (a.reverse ? T - 1 : t0)) : 0.f;
+    for (int j = 0; j < nsteps; ++j) {  // j counts steps; the step's frame is fr
+      const int fr = a.reverse ? T - 1 - j : t0 + j;
       const long long f = bh * T + fr;
       const float gt = relu_lin ? 1.f : decay_of(gnext, a.gate_logits);
-      if (t + 1 < T && !relu_lin) gnext = __ldg(a.g + (a.reverse ? f - 1 : f + 1));
-      const bool add_b = !(a.reverse && fr == 0);  // E_{-1} = 0
-      const bool ok = wait_or_abort(smem_u32(pfull), t & 1, abort_flag, a.status) &&
+      if (j + 1 < nsteps && !relu_lin) gnext = __ldg(a.g + (a.reverse ? f - 1 : f + 1));
+      const bool add_b = use_b && !(a.reverse && fr == 0);  // E_{-1} = 0
+      const bool ok = wait_or_abort(smem_u32(pfull), j & 1, abort_flag, a.status) &&
                       wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
@@ -649,7 +711,9 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
         tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), p);
         tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16, pl);
         float bv[16];
-        if (row) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) bv[q] = 0.f;
+        if (row && use_b) {
           const float4* bp = reinterpret_cast<const float4*>(bring + stage * kScanBStage + i * 64);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -666,20 +730,25 @@ __global__ void __launch_bounds__(kScanThreads, 1) tc_scan_kernel(ScanArgs a) {
         if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
         if (row) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j)
-            x[j] = relu_lin ? x[j] + bv[j] : fmaf(gt, x[j] - (p[j] + pl[j]), add_b ? bv[j] : 0.f);
+          for (int jj = 0; jj < 16; ++jj)
+            x[jj] = relu_lin ? x[jj] + bv[jj] : fmaf(gt, x[jj] - (p[jj] + pl[jj]), add_b ? bv[jj] : 0.f);
         }
-        // S_t goes into the buffer of S_{t-2}, whose store has read it (the MMA
-        // thread waited for that before committing pfull(t)).
-        write_img(img + ((t + 1) & 1) * kScanImg);
+        // S_j goes into the buffer of S_{j-2}, whose store has read it (the MMA
+        // thread waited for that before committing pfull(j)).
+        write_img(img + ((j + 1) & 1) * kScanImg);
         fence_proxy_async_smem();
       }
-      if (++stage == kScanStages) { stage = 0; phase ^= 1; }
+      if (++stage == STAGES) { stage = 0; phase ^= 1; }
       if (!__all_sync(0xffffffffu, ok)) goto done;
       __syncwarp();
       if (lane == 0) mbar_arrive(smem_u32(sready));
     }
-    if (row && a.state_out) {
+    if (row && a.maps) {
+      float4* mo = reinterpret_cast<float4*>(a.maps + ((size_t)(bh * a.nchunks + chunk_id) * D + i) * 2 * D +
+                                             (ident ? 0 : D) + 16 * cb);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) mo[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+    } else if (row && a.state_out && chunk_id == a.nchunks - 1) {
       float4* so = reinterpret_cast<float4*>(a.state_out + ((size_t)bh * D + i) * D + 16 * cb);
 #pragma unroll
       for (int q = 0; q < 4; ++q) so[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
@@ -1398,26 +1467,96 @@ constexpr int kKvBarBytes = 1536;  // barriers, partial sums and dbeta halves of
 // Every kernel here asks for more than half of the SM's shared memory, so two of
 // them never share an SM (the gram and read-out kernels allocate all of TMEM).
 int gram_smem(int NA, int D) {
-  return kGramRaw * kRawStage + kGramConv * kConvStage + NA * D * 128 + kBarBytes + 1024;
+  return kGramRaw * kRawStage + kGramConv * kConvStage + NA * D * 128 + kBetaRing + kBarBytes + 1024;
 }
 int kv_smem(int NA, int D) { return 4 * NA * D * 128 + 3 * NA * kKvTok * 128 + kKvBarBytes + 1024; }
-int scan_smem() { return kScanStages * (kScanMStage + kScanBStage) + 2 * kScanImg + kBarBytes + 1024; }
+template <int STAGES>
+int scan_smem() { return STAGES * (kScanMStage + kScanBStage) + 2 * kScanImg + kBarBytes + 1024; }
+
+constexpr int kTcChunk = kTcChunkFrames;
+
+// A one-pass scan's arguments (not chunked).
+ScanArgs one_pass(const uint8_t* m_img, const float* b_blk, const float* g, int gate_logits, int variant,
+                  const float* state_in, uint8_t* s_img, float* state_out, int T, int D, unsigned int* status,
+                  int reverse) {
+  ScanArgs sa{m_img, b_blk, g, gate_logits, variant, state_in, s_img, state_out, T, D, num_atoms(D), status, reverse};
+  sa.chunk = T;
+  sa.nchunks = 1;
+  sa.starts = nullptr;
+  sa.maps = nullptr;
+  return sa;
+}
+
+template <int STAGES>
+int launch_scan(const ScanArgs& sa, long long ctas, cudaStream_t st, const char* name) {
+  const int smem = scan_smem<STAGES>();
+  if (cudaFuncSetAttribute(tc_scan_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return kCuda;
+  ProfScope ps(st, name);
+  tc_scan_kernel<STAGES><<<(unsigned)ctas, kScanThreads, smem, st>>>(sa);
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
 int out_smem(int NA, int D) {
   return 2 * ((2 * NA * D * 128 + 1023) & ~1023) + (kOutQStages + 1) * NA * kOutTok * 128 + kBarBytes + 1024;
 }
 
 }  // namespace
 
-// Sequential and split forms: the three kernels above, through a workspace.
-// Prefix form: the SIMT kernels for now.
-size_t tc_workspace_bytes(const Problem& p, int mode) {
-  if (mode == 1) return simt_workspace_bytes(p, mode);
-  return tc_layout(p).total;
+// Sequential and split forms: the gram, the one-pass scan and the read-out,
+// through a workspace.  Prefix form: the gram, the chunked scan's summaries, the
+// fold over chunk boundaries, the chunked replay and the read-out; its workspace
+// is the split form's plus the chunk maps and starts.
+size_t tc_workspace_bytes(const Problem& p, int mode) { return tc_layout(p, mode).total; }
+
+namespace {
+
+// The gram over every frame-head of the call: the M_t images and b_t blocks.
+int launch_gram(const Problem& p, uint8_t* m_img, float* b_mat, cudaStream_t st) {
+  const int NA = num_atoms(p.D);
+  const long long F = p.BHT();
+  CUtensorMap mapK, mapV;
+  if (!make_map(&mapK, p.k, p.D, p.S, F, kGramTok) || !make_map(&mapV, p.v, p.D, p.S, F, kGramTok)) return kCuda;
+  const int smem = gram_smem(NA, p.D);
+  if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return kCuda;
+  GramArgs ga{p.beta, p.gate_logits, p.variant, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale,
+              p.key_scale, p.status};
+  const int nsm = num_sms();
+  const unsigned grid = (unsigned)(F < nsm ? F : nsm);
+  ProfScope ps(st, "tc_gram");
+  tc_gram_kernel<<<grid, kGramThreads, smem, st>>>(mapK, mapV, ga);
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
+
+// The chunked scan's summary form: [A_c | b_c] of every (head, chunk) into `maps`.
+int launch_chunk_summaries(const Problem& p, const uint8_t* m_img, const float* b_mat, float* maps, int nch,
+                           cudaStream_t st) {
+  ScanArgs sa = one_pass(m_img, b_mat, p.g, p.gate_logits, p.variant, nullptr, nullptr, nullptr, p.T, p.D,
+                         p.status, 0);
+  sa.chunk = kTcChunk;
+  sa.nchunks = nch;
+  sa.maps = maps;
+  return launch_scan<2>(sa, p.BH() * nch * 2 * (p.D / 16), st, "tc_chunk_summary");
+}
+
+}  // namespace
+
+int tc_chunk_maps(const Problem& p, void* ws, float** maps, int* nchunks, cudaStream_t st) {
+  const TcLayout L = tc_layout(p, GDN_MODE_PREFIX);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  const int nch = (p.T + kTcChunk - 1) / kTcChunk;
+  float* mp = reinterpret_cast<float*>(w + L.maps_off);
+  int rc = launch_gram(p, w + L.m_off, reinterpret_cast<float*>(w + L.b_off), st);
+  if (rc != kOk) return rc;
+  rc = launch_chunk_summaries(p, w + L.m_off, reinterpret_cast<float*>(w + L.b_off), mp, nch, st);
+  if (rc != kOk) return rc;
+  *maps = mp;
+  *nchunks = nch;
+  return kOk;
 }
 
 int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
-  if (p.mode == 1) return simt_forward(p, ws, st);
-  const TcLayout L = tc_layout(p);
+  const TcLayout L = tc_layout(p, p.mode);
   const int NA = num_atoms(p.D);
   uint8_t* w = static_cast<uint8_t*>(ws);
   uint8_t* m_img = w + L.m_off;
@@ -1426,31 +1565,35 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
   const long long F = p.BHT();
   const int nsm = num_sms();
 
-  CUtensorMap mapK, mapV, mapQ, mapO;
-  if (!make_map(&mapK, p.k, p.D, p.S, F, kGramTok) || !make_map(&mapV, p.v, p.D, p.S, F, kGramTok) ||
-      !make_map(&mapQ, p.q, p.D, p.S, F, kOutTok) || !make_map(&mapO, p.out, p.D, p.S, F, 32))
-    return kCuda;
+  CUtensorMap mapQ, mapO;
+  if (!make_map(&mapQ, p.q, p.D, p.S, F, kOutTok) || !make_map(&mapO, p.out, p.D, p.S, F, 32)) return kCuda;
 
-  {
-    const int smem = gram_smem(NA, p.D);
-    if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return kCuda;
-    GramArgs ga{p.beta, p.gate_logits, p.variant, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale,
-                p.key_scale, p.status};
-    const unsigned grid = (unsigned)(F < nsm ? F : nsm);
-    ProfScope ps(st, "tc_gram");
-    tc_gram_kernel<<<grid, kGramThreads, smem, st>>>(mapK, mapV, ga);
+  int rc = launch_gram(p, m_img, b_mat, st);
+  if (rc != kOk) return rc;
+  if (p.mode == GDN_MODE_PREFIX) {
+    // chunk summaries [A_c | b_c] -> the fold over chunk boundaries (float32) ->
+    // every chunk replayed from its true initial state
+    const int nch = (p.T + kTcChunk - 1) / kTcChunk;
+    float* maps = reinterpret_cast<float*>(w + L.maps_off);
+    float* starts = reinterpret_cast<float*>(w + L.starts_off);
+    rc = launch_chunk_summaries(p, m_img, b_mat, maps, nch, st);
+    if (rc != kOk) return rc;
+    rc = launch_chunk_fold(maps, maps + p.D, 2LL * p.D * p.D, 2 * p.D, nch, p.state_in, starts, nullptr, nullptr,
+                           nullptr, p.BH(), p.D, st);
+    if (rc != kOk) return rc;
+    ScanArgs sa = one_pass(m_img, b_mat, p.g, p.gate_logits, p.variant, nullptr, s_img, p.state_out, p.T, p.D,
+                           p.status, 0);
+    sa.chunk = kTcChunk;
+    sa.nchunks = nch;
+    sa.starts = starts;
+    rc = launch_scan<2>(sa, p.BH() * nch * (p.D / 16), st, "tc_chunk_replay");
+    if (rc != kOk) return rc;
+  } else {
+    ScanArgs sa = one_pass(m_img, b_mat, p.g, p.gate_logits, p.variant, p.state_in, s_img, p.state_out, p.T, p.D,
+                           p.status, 0);
+    rc = launch_scan<4>(sa, p.BH() * (p.D / 16), st, "tc_scan");
+    if (rc != kOk) return rc;
   }
-  if (cudaGetLastError() != cudaSuccess) return kCuda;
-  {
-    const int smem = scan_smem();
-    if (cudaFuncSetAttribute(tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return kCuda;
-    ScanArgs sa{m_img, b_mat, p.g, p.gate_logits, p.variant, p.state_in, s_img, p.state_out, p.T, p.D, NA, p.status};
-    ProfScope ps(st, "tc_scan");
-    tc_scan_kernel<<<(unsigned)(p.BH() * (p.D / 16)), kScanThreads, smem, st>>>(sa);
-  }
-  if (cudaGetLastError() != cudaSuccess) return kCuda;
   {
     const int smem = out_smem(NA, p.D);
     if (cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
@@ -1528,10 +1671,7 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st,
   const int gsmem = gram_smem(NA, D);
   if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, gsmem) != cudaSuccess)
     return kCuda;
-  const int ssmem = scan_smem();
-  if (cudaFuncSetAttribute(tc_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, ssmem) != cudaSuccess)
-    return kCuda;
-  const unsigned sgrid = (unsigned)(p.BH() * (D / 16));
+  const long long sgrid = p.BH() * (D / 16);
 
   // forward states: M_t (image), b_t (into the E blocks), S_t (images), unless a
   // forward call left them in the workspace (tc_layout's regions are this layout's first three)
@@ -1543,12 +1683,10 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st,
       tc_gram_kernel<<<pgrid, kGramThreads, gsmem, st>>>(mapK, mapV, ga);
     }
     if (cudaGetLastError() != cudaSuccess) return kCuda;
-    {
-      ScanArgs sa{m_img, e_blk, p.g, p.gate_logits, kGdn, p.state_in, s_img, nullptr, p.T, D, NA, p.status, 0};
-      ProfScope ps(st, "tc_scan");
-      tc_scan_kernel<<<sgrid, kScanThreads, ssmem, st>>>(sa);
-    }
-    if (cudaGetLastError() != cudaSuccess) return kCuda;
+    const int rc = launch_scan<4>(one_pass(m_img, e_blk, p.g, p.gate_logits, kGdn, p.state_in, s_img, nullptr, p.T,
+                                           D, p.status, 0),
+                                  sgrid, st, "tc_scan");
+    if (rc != kOk) return rc;
   }
   // E_t = Q_t^T dO_t / sqrt(D) (overwrites b_t, which the scan has consumed)
   {
@@ -1559,11 +1697,11 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st,
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   // U_t for every frame and dS_0, by the reverse scan
   {
-    ScanArgs sa{m_img, e_blk, p.g, p.gate_logits, kGdn, gr.dstate_out, u_img, gr.dstate_in, p.T, D, NA, p.status, 1};
-    ProfScope ps(st, "tc_bwd_rscan");
-    tc_scan_kernel<<<sgrid, kScanThreads, ssmem, st>>>(sa);
+    const int rc = launch_scan<4>(one_pass(m_img, e_blk, p.g, p.gate_logits, kGdn, gr.dstate_out, u_img,
+                                           gr.dstate_in, p.T, D, p.status, 1),
+                                  sgrid, st, "tc_bwd_rscan");
+    if (rc != kOk) return rc;
   }
-  if (cudaGetLastError() != cudaSuccess) return kCuda;
   {
     ProfScope ps(st, "tc_bwd_s0_image");
     tc_state_image_kernel<<<dim3((unsigned)p.BH(), D / 16), 128, 0, st>>>(p.state_in, s0_img, D, NA);

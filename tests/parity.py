@@ -173,3 +173,44 @@ def assert_parity(wl_dtype, out_gpu, out_ref, st_gpu, st_ref, what="", strict=Tr
 def check_status():
     rc = binding.gdn_last_error(torch.cuda.current_stream().cuda_stream)
     assert rc == 0, f"device status {binding.STATUS.get(rc, rc)}"
+
+
+def oracle_heads(wl, heads, S0_of=None, workers=None, fn=None):
+    """Yields ((b, h), out_ref, state_ref) for each head in `heads`, in order: the
+    head's inputs regenerated from the seeded streams and run through the fp64
+    oracle, a few heads at a time on a thread pool (numpy releases the GIL in its
+    generators and matrix products), so a full-size workload's every head can be
+    checked without holding more than `workers` heads' fp64 results in host
+    memory.  S0_of(b, h) gives a head's initial state (None: zeros).  With `fn`,
+    yields ((b, h), fn(b, h)) instead (any per-head oracle computation)."""
+    import contextlib
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    try:
+        from threadpoolctl import threadpool_limits
+    except ImportError:
+        threadpool_limits = None
+    cores = len(os.sched_getaffinity(0))
+    workers = workers or max(1, min(4, cores))
+    limits = threadpool_limits(max(1, cores // workers)) if threadpool_limits else contextlib.nullcontext()
+
+    def one(bh):
+        b, h = bh
+        if fn is not None:
+            return bh, fn(b, h)
+        return bh, oracle_head(wl, b, h, None if S0_of is None else S0_of(b, h))
+
+    with limits, ThreadPoolExecutor(workers) as ex:
+        pending = []
+        it = iter(heads)
+        for bh in it:
+            pending.append(ex.submit(one, bh))
+            if len(pending) >= workers:
+                break
+        while pending:
+            bh, res = pending.pop(0).result()
+            nxt = next(it, None)
+            if nxt is not None:
+                pending.append(ex.submit(one, nxt))
+            yield (bh, res) if fn is not None else (bh, res[0], res[1])

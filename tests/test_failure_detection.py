@@ -39,4 +39,4 @@ def test_bounded_wait_reports_timeout_and_context_stays_usable():
     torch.cuda.synchronize()
     parity.check_status()
     ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"])
-    parity.assert_parity("bf16", out.float().cpu().numpy(), ro, st.cpu().numpy(), rs, "after timeout", strict=False)
+    parity.assert_parity("bf16", out.float().cpu().numpy(), ro, st.cpu().numpy(), rs, "after timeout")

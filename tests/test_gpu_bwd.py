@@ -134,23 +134,33 @@ def test_backward_on_nan_filled_workspace():
         np.testing.assert_array_equal(a[key], b[key])
 
 
-def test_backward_minute_sampled_heads():
+def test_backward_minute_every_head():
     """The one-minute workload (961 frames x 880 tokens x 20 heads x d112, bf16) in
-    one backward call; two heads checked over every frame against the oracle."""
+    one backward call; every one of the 20 heads checked over every frame against
+    the oracle."""
     wl = synth.WORKLOADS["minute"]
     q, k, v, g, beta = parity.device_inputs(wl)
     dout = parity.device_dout(wl)
     res = binding.frame_bwd(q, k, v, g, beta, dout)
     torch.cuda.synchronize()
     parity.check_status()
-    for (b, h) in synth.head_sample(wl, 2):
+    del q, k, v, g, beta, dout
+
+    def ref_of(b, h):
         x = synth.head(wl, b, h)
         ref = oracle.backward_head(x["q"], x["k"], x["v"], x["g"], x["beta"], None, synth.head_dout(wl, b, h))
         ref["dstate_in"] = ref.pop("dS0")
+        return ref
+
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    n = 0
+    for (b, h), ref in parity.oracle_heads(wl, heads, fn=ref_of, workers=2):
+        n += 1
         got = {key: np_(res[key][b, h]) for key in parity.GRAD_KEYS}
         r = parity.assert_grad_parity(wl.dtype, got, ref, f"minute bwd head {(b, h)}")
         print(f"minute bwd head {(b, h)}: " + ", ".join(
             f"{k} max {v['max_abs_over_rms']:.2e} rms {v['rms_err_over_rms']:.2e}" for k, v in r.items()))
+    assert n == len(heads)
 
 
 @pytest.mark.parametrize("gate_logits", [False, True])

@@ -77,7 +77,9 @@ def test_edge_shapes(case, mode):
     si = None if S0 is None else torch.from_numpy(S0).cuda()
     out, st = run(*parity.upload(wl, x), state_in=si, mode=mode)
     ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0)
-    parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"edge {case} mode={mode}", strict=False)
+    # the half-ulp allowance only where a non-zero initial state makes the outputs heavy-tailed
+    eo, es = parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"edge {case} mode={mode}", strict=not nz)
+    print(f"edge {case} mode={mode}: out {eo} state {es}")
 
 
 # (dtype, B, H, T, S, D): gates given as logits (the fused gate prologue)
@@ -105,8 +107,8 @@ def test_gate_logits(case, mode):
     bl = torch.from_numpy(lg["beta_logit"]).cuda()
     out, st = run(q, k, v, gl, bl, mode=mode, gate_logits=True)
     ro, rs = oracle.frame_fwd_from_logits(x["q"], x["k"], x["v"], lg["g_logit"], lg["beta_logit"])
-    strict = (B, H, T, S, D) == (1, 20, 21, 880, 112)
-    parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"logits {case} mode={mode}", strict=strict)
+    eo, es = parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"logits {case} mode={mode}")
+    print(f"logits {case} mode={mode}: out {eo} state {es}")
 
 
 # (dtype, B, H, T, S, D, nonzero initial state): the cumulative ReLU linear attention baseline
@@ -135,7 +137,8 @@ def test_relu_linear_baseline(case, mode):
     torch.cuda.synchronize()
     parity.check_status()
     ro, rs = oracle.relu_linear_fwd(x["q"], x["k"], x["v"], S0)
-    parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"relu-linear {case} mode={mode}", strict=False)
+    eo, es = parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"relu-linear {case} mode={mode}", strict=not nz)
+    print(f"relu-linear {case} mode={mode}: out {eo} state {es}")
 
 
 def _small_bf16(T=21, H=3, S=300, D=112):
@@ -185,7 +188,7 @@ def test_chunked_calls_equal_single_call(mode):
         assert torch.equal(out1, out2) and torch.equal(st1, st)
     else:
         ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"])
-        parity.assert_parity("bf16", np_(out2), ro, np_(st), rs, "chunked prefix", strict=False)
+        parity.assert_parity("bf16", np_(out2), ro, np_(st), rs, "chunked prefix")
 
 
 @pytest.mark.parametrize("mode", [0, 2])
@@ -233,46 +236,49 @@ def minute_inputs():
     return wl, parity.device_inputs(wl)
 
 
-@pytest.fixture(scope="module")
-def minute_oracle():
-    wl = synth.WORKLOADS["minute"]
-    return {bh: parity.oracle_head(wl, *bh) for bh in synth.head_sample(wl, 2)}
+def _check_heads(wl, outs, ref_iter, what):
+    """outs: {label: (out, state)} device results; every head ref_iter yields is
+    compared, for every label, against the oracle."""
+    n = 0
+    for (b, h), ro, rs in ref_iter:
+        for label, (out, st) in outs.items():
+            eo, es = parity.assert_parity(wl.dtype, np_(out[b, h]), ro, np_(st[b, h]), rs,
+                                          f"{what} {label} head {(b, h)}")
+            print(f"{what} {label} head {(b, h)}: out {eo} state {es}")
+        n += 1
+    return n
 
 
-def _check_heads(wl, out, st, ref, what):
-    for (b, h), (ro, rs) in ref.items():
-        eo, es = parity.assert_parity(wl.dtype, np_(out[b, h]), ro, np_(st[b, h]), rs, f"{what} head {(b, h)}")
-        print(f"{what} head {(b, h)}: out {eo} state {es}")
-
-
-@pytest.mark.parametrize("mode", [0])
-def test_minute_single_call(minute_inputs, minute_oracle, mode):
-    """961 frames x 880 tokens x 20 heads x d112, one call (mode 0 is the bench's
-    launch configuration); sampled heads checked over every frame against the oracle."""
-    wl, ins = minute_inputs
-    out, st = run(*ins, mode=mode)
-    _check_heads(wl, out, st, minute_oracle, f"minute mode={mode}")
-
-
-def test_minute_chunked_rollout(minute_inputs, minute_oracle):
-    """The same tensors as 97 calls of <= 10 frames carrying the state."""
+def test_minute_every_head_single_call_and_chunked_rollout(minute_inputs):
+    """961 frames x 880 tokens x 20 heads x d112: one call (the bench's launch
+    configuration) and the same tensors as 97 chunk-causal calls of <= 10 frames
+    carrying the state.  The rollout equals the single call bit for bit (the
+    per-frame arithmetic does not depend on where calls split), and every one of
+    the 20 heads of the single call is compared over every frame with the oracle."""
     wl, (q, k, v, g, beta) = minute_inputs
+    out, st = run(q, k, v, g, beta, mode=0)
     cw = synth.WORKLOADS["chunked"]
-    outs, st, t0 = [], None, 0
+    outs, stc, t0 = [], None, 0
     for n in cw.chunks:
         sl = lambda t: t[:, :, t0:t0 + n].contiguous()  # noqa: E731
-        o, st = run(sl(q), sl(k), sl(v), sl(g), sl(beta), state_in=st, mode=0)
+        o, stc = run(sl(q), sl(k), sl(v), sl(g), sl(beta), state_in=stc, mode=0)
         outs.append(o)
         t0 += n
     assert t0 == wl.T
-    out = torch.cat(outs, dim=2)
-    _check_heads(wl, out, st, minute_oracle, "chunked")
+    outc = torch.cat(outs, dim=2)
+    del outs
+    same = torch.equal(out, outc) and torch.equal(st, stc)
+    checked = {"single": (out, st)} if same else {"single": (out, st), "chunked": (outc, stc)}
+    heads = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+    assert _check_heads(wl, checked, parity.oracle_heads(wl, heads), "minute") == len(heads)
+    assert same, "the chunk-causal rollout differs from the single call"
 
 
 def test_large_sequential_and_prefix_agree():
-    """4 x 16 heads, 241 frames of 3600 tokens, d128: sampled heads of both the
-    sequential scan and the chunked prefix composition match the oracle, and the
-    two forms agree everywhere.
+    """4 x 16 heads, 241 frames of 3600 tokens, d128: eight heads spread over all
+    four batch indices, for both the sequential scan and the chunked prefix
+    composition, match the oracle over every frame, and the two forms agree
+    everywhere.
 
     Agreement of two bf16 outputs: each form rounds its own fp32 value, so the two
     may land on adjacent bf16 values even when both are within the bound of the
@@ -284,9 +290,10 @@ def test_large_sequential_and_prefix_agree():
     out0, st0 = run(*ins, mode=0)
     out1, st1 = run(*ins, mode=1)
     del ins
-    ref = {bh: parity.oracle_head(wl, *bh) for bh in synth.head_sample(wl, 2)}
-    _check_heads(wl, out0, st0, ref, "large seq")
-    _check_heads(wl, out1, st1, ref, "large prefix")
+    heads = synth.head_sample(wl, 8)
+    assert {b for b, _ in heads} == set(range(wl.B))
+    n = _check_heads(wl, {"seq": (out0, st0), "prefix": (out1, st1)}, parity.oracle_heads(wl, heads), "large")
+    assert n == len(heads)
     rms_o = torch.sqrt(torch.mean(out0.float() ** 2)).item()
     rms_s = torch.sqrt(torch.mean(st0 ** 2)).item()
     beyond, sq = 0.0, 0.0
