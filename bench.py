@@ -199,6 +199,27 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
+def host_link_gbs(dev, nbytes: int = 1 << 30, reps: int = 3) -> dict:
+    """Measured pinned host <-> device copy bandwidth (GB/s), each direction alone:
+    one cudaMemcpyAsync of `nbytes`, best of `reps`, timed with CUDA events."""
+    import torch
+    h = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    res = {}
+    for name, (dst, src) in (("h2d_gbs", (d, h)), ("d2h_gbs", (h, d))):
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            dst.copy_(src, non_blocking=True)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        res[name] = nbytes / (best / 1e3) / 1e9
+    res["bytes"] = nbytes
+    return res
+
+
 def bus_id(dev) -> str | None:
     import torch
     try:
@@ -211,10 +232,11 @@ def bus_id(dev) -> str | None:
 # ----------------------------------------------------------------- CPU oracle timing
 
 def oracle_sample(wl, budget_s: float, max_heads: int | None = None, frames: int | None = None,
-                  backward: bool = False):
+                  backward: bool = False, threads: int | None = None):
     """Times the fp64 oracle (its backward pass with ``backward``) on whole heads of
-    the workload until `budget_s` of CPU work.  Returns (equivalent tokens/s,
-    cores, sample description, seconds)."""
+    the workload until `budget_s` of CPU work, with `threads` BLAS threads (all of
+    the process's cores by default).  Returns (equivalent tokens/s, threads,
+    sample description, seconds)."""
     import contextlib
 
     import oracle
@@ -222,7 +244,7 @@ def oracle_sample(wl, budget_s: float, max_heads: int | None = None, frames: int
         from threadpoolctl import threadpool_limits
     except ImportError:  # BLAS then runs on its default thread count: every core
         threadpool_limits = lambda n: contextlib.nullcontext()  # noqa: E731
-    cores = len(os.sched_getaffinity(0))
+    cores = threads or len(os.sched_getaffinity(0))
     T = wl.T if frames is None else min(frames, wl.T)
     max_heads = wl.B * wl.H if max_heads is None else max_heads
     spent, n = 0.0, 0
@@ -488,15 +510,24 @@ def ours_arm(args, rank, world, local_rank):
         ems = rank_max(e0.elapsed_time(e1) / n_e2e, world, dev)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hg, hb))
         d2h = ho.numel() * ho.element_size() + hs.numel() * hs.element_size()
+        link = host_link_gbs(dev)
+        # the copies in and out overlap each other and the kernels (full duplex):
+        # the end-to-end bound is the slowest of the three
+        bound_ms = max(h2d / link["h2d_gbs"] / 1e6, d2h / link["d2h_gbs"] / 1e6, ms)
         e2e = {"value": job_value(wl.tokens, world, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems, "steps": n_e2e,
-               "api": f"gdn_frame_fwd_host, {echunk}-frame chunks, pinned host buffers"}
+               "api": f"gdn_frame_fwd_host, {echunk}-frame chunks, pinned host buffers",
+               "link": link, "bound_ms": bound_ms, "frac_of_bound": bound_ms / ems}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         v_, cores, desc, spent = oracle_sample(wl, args.cpu_seconds, frames=240 if args.backward else None,
                                                backward=args.backward)
         cpu = {"value": v_, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc, "seconds": spent}
+        # the oracle on one thread, on the 21-frame short clip (a whole head)
+        v1, c1, d1, s1 = oracle_sample(synth.WORKLOADS["short"], 0.0, max_heads=1, backward=args.backward,
+                                       threads=1)
+        cpu["one_thread_short"] = {"value": v1, "unit": UNIT, "cores": c1, "sample": d1, "seconds": s1}
 
     if rank == 0:
         line = {"metric": METRIC_BWD if args.backward else METRIC, "value": value, "unit": UNIT, "n_gpus": world,

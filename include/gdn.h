@@ -68,7 +68,11 @@ typedef enum {
   GDN_ERR_MISALIGNED = 3,  /* a pointer misses its alignment              */
   GDN_ERR_CUDA = 4,        /* a CUDA runtime/driver call or launch failed */
   GDN_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up          */
-  GDN_ERR_WORKSPACE = 6    /* workspace NULL or smaller than required     */
+  GDN_ERR_WORKSPACE = 6,   /* workspace NULL or smaller than required     */
+  GDN_ERR_BOUNDS = 7       /* debug build only (libgdn_debug.so, compiled
+                            * with -DGDN_DEBUG=1): a kernel's scratch offset
+                            * fell outside its region; the access was
+                            * skipped and the call's results are invalid  */
 } gdn_status_t;
 
 typedef enum {
@@ -349,8 +353,9 @@ int gdn_summary_apply(const float* A, const float* b, const float* state_in, flo
 /*
  * gdn_last_error -- synchronises `stream`, then returns and clears the
  * device-side status word: GDN_OK, GDN_ERR_TIMEOUT (a kernel's bounded wait on
- * an mbarrier or a flag gave up; its results are invalid), or GDN_ERR_CUDA
- * (the stream reported an error).
+ * an mbarrier or a flag gave up; its results are invalid), GDN_ERR_BOUNDS (the
+ * debug build's index check failed), or GDN_ERR_CUDA (the stream reported an
+ * error).  The first error recorded since the last call wins.
  */
 int gdn_last_error(void* stream);
 

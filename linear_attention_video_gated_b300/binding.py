@@ -13,13 +13,14 @@ import os
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libgdn.so")
+DEBUG_LIB_PATH = os.path.join(PKG, "libgdn_debug.so")
 
 GDN_F32, GDN_BF16 = 0, 1
 GDN_BWD_STATES_IN_WORKSPACE, GDN_BWD_GATE_LOGITS = 1, 2
 GDN_SUMMARY_GATE_LOGITS = 1
 GDN_MODE_SEQUENTIAL, GDN_MODE_PREFIX, GDN_MODE_SPLIT = 0, 1, 2
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_MISALIGNED",
-          4: "GDN_ERR_CUDA", 5: "GDN_ERR_TIMEOUT", 6: "GDN_ERR_WORKSPACE"}
+          4: "GDN_ERR_CUDA", 5: "GDN_ERR_TIMEOUT", 6: "GDN_ERR_WORKSPACE", 7: "GDN_ERR_BOUNDS"}
 
 _lib = None
 
@@ -64,19 +65,36 @@ class GDNError(RuntimeError):
         super().__init__(f"{what}: {STATUS.get(status, status)}")
 
 
+def _load(path) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with __graft_entry__.build()")
+    handle = ctypes.CDLL(path)
+    for name, (res, args) in _SIGS.items():
+        fn = getattr(handle, name)
+        fn.restype = res
+        fn.argtypes = args
+    return handle
+
+
 def lib() -> ctypes.CDLL:
     """Loads libgdn.so (once).  Raises if it is not built."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build()")
-        handle = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in _SIGS.items():
-            fn = getattr(handle, name)
-            fn.restype = res
-            fn.argtypes = args
-        _lib = handle
+        _lib = _load(LIB_PATH)
     return _lib
+
+
+_debug_lib = None
+
+
+def debug_lib() -> ctypes.CDLL:
+    """Loads the debug build, libgdn_debug.so (once): the same entry points, with
+    every kernel's scratch offsets checked (GDN_ERR_BOUNDS).  Its status word and
+    module state are its own; call its functions through the returned handle."""
+    global _debug_lib
+    if _debug_lib is None:
+        _debug_lib = _load(DEBUG_LIB_PATH)
+    return _debug_lib
 
 
 # ---- raw C-ABI calls (integer device addresses) ------------------------------------

@@ -4,6 +4,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -175,6 +176,15 @@ int check_args(const void* q, const void* k, const void* v, const float* g, cons
   return validate(q, k, v, g, beta, state_in, out, state_out, B, H, T, S, D, dtype, mode, p, need_gates);
 }
 size_t scratch_bytes(const Problem& p) { return workspace_for(p); }
+
+size_t debug_shrink() {
+#if GDN_DEBUG
+  const char* e = std::getenv("GDN_DEBUG_SHRINK");
+  return e ? (size_t)std::strtoull(e, nullptr, 10) : 0;
+#else
+  return 0;
+#endif
+}
 unsigned int* device_status_word() { return status_word(); }
 int run_forward(const Problem& p, void* ws, cudaStream_t st) { return forward(p, ws, st); }
 
@@ -274,6 +284,7 @@ const char* gdn_status_string(int status) {
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
     case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
     case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
+    case GDN_ERR_BOUNDS: return "GDN_ERR_BOUNDS";
     default: return "GDN_ERR_UNKNOWN";
   }
 }

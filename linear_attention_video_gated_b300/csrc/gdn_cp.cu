@@ -70,6 +70,7 @@ extern "C" int gdn_summary_apply(const float* A, const float* b, const float* st
   if (!A || !b || !state_out) return kInvalidArg;
   if (!aligned16(A) || !aligned16(b) || !aligned16(state_out) || (state_in && !aligned16(state_in)))
     return kMisaligned;
+  const size_t span = (size_t)B * H * D * D * sizeof(float);
   return launch_chunk_fold(A, b, (long long)D * D, D, 1, state_in, nullptr, state_out, nullptr, nullptr,
-                           (long long)B * H, D, static_cast<cudaStream_t>(stream));
+                           (long long)B * H, D, static_cast<cudaStream_t>(stream), span, span, 0);
 }

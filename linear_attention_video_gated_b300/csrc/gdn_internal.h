@@ -46,7 +46,7 @@ struct Problem {
 
 // Status codes (mirror gdn_status_t).
 enum Status {
-  kOk = 0, kInvalidArg = 1, kUnsupported = 2, kMisaligned = 3, kCuda = 4, kTimeout = 5, kWorkspace = 6
+  kOk = 0, kInvalidArg = 1, kUnsupported = 2, kMisaligned = 3, kCuda = 4, kTimeout = 5, kWorkspace = 6, kBounds = 7
 };
 
 // The gate prologue fused into the kernels (gdn_frame_fwd_from_logits): raw
@@ -74,6 +74,34 @@ __device__ __forceinline__ void from_f32(__nv_bfloat16& d, float x) { d = __floa
 __device__ __forceinline__ void report_device_error(unsigned int* status, unsigned int code) {
   atomicCAS(status, 0u, code);
 }
+
+// The debug build (nvcc -DGDN_DEBUG=1: libgdn_debug.so) checks every scratch
+// offset a kernel computes against the extent of its region as the host's
+// layout gives it: `end`, one past the last byte the access touches relative to
+// the region's start, must not pass `span` (0: not given, not checked).  A failed
+// check records GDN_ERR_BOUNDS and the access is skipped (a skipped copy then
+// ends in a bounded wait that gives up); nothing traps.  Compiled out otherwise.
+#ifndef GDN_DEBUG
+#define GDN_DEBUG 0
+#endif
+__device__ __forceinline__ bool in_region(size_t end, size_t span, unsigned int* status) {
+#if GDN_DEBUG
+  if (span != 0 && end > span) {
+    if (status) report_device_error(status, kBounds);
+    return false;
+  }
+#else
+  (void)end;
+  (void)span;
+  (void)status;
+#endif
+  return true;
+}
+
+// Debug build only: bytes taken off the read-out's image region extent before it
+// is passed to the kernel (GDN_DEBUG_SHRINK in the environment), so that a test
+// can see a check fire; 0 in the release build.
+size_t debug_shrink();
 
 // ---- argument checks and dispatch (gdn_api.cu), for the other C-ABI files -------
 // Validates the arguments of a forward call and fills `p` (returns a Status).
@@ -123,7 +151,7 @@ int simt_chunk_maps(const Problem& p, void* ws, float** maps, int* nchunks, cuda
 // composed map of all chunks -> A_out, b_out ([BH][D][D] each).
 int launch_chunk_fold(const float* A, const float* b, long long chunk_stride, int ld, int nchunks,
                       const float* state_in, float* starts, float* x_out, float* A_out, float* b_out, long long BH,
-                      int D, cudaStream_t st);
+                      int D, cudaStream_t st, size_t a_span = 0, size_t b_span = 0, size_t starts_span = 0);
 
 // ---- tensor-core path (bf16 I/O) ------------------------------------------------
 size_t tc_workspace_bytes(const Problem& p, int mode);

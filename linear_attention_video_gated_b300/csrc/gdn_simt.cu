@@ -345,6 +345,8 @@ struct FoldArgs {
   float* x_out;
   float* A_out;
   float* b_out;
+  unsigned int* status;
+  size_t a_span, b_span, starts_span;  // extents (bytes) from A, b and starts (debug checks)
 };
 
 constexpr int kFoldThreads = 128;
@@ -372,7 +374,8 @@ __global__ void __launch_bounds__(kFoldThreads) chunk_fold_kernel(FoldArgs a) {
   for (int c = 0; c < a.nchunks; ++c) {
     const size_t mo = (size_t)(bh * a.nchunks + c) * a.chunk_stride;
     if (row) {
-      if (a.starts) {
+      if (a.starts && in_region((((size_t)(bh * a.nchunks + c) * D + i) * D + 16 * cb + 16) * 4, a.starts_span,
+                                a.status)) {
         float* dst = a.starts + ((size_t)(bh * a.nchunks + c) * D + i) * D + 16 * cb;
 #pragma unroll
         for (int j = 0; j < 16; ++j) dst[j] = x[j];
@@ -380,7 +383,8 @@ __global__ void __launch_bounds__(kFoldThreads) chunk_fold_kernel(FoldArgs a) {
 #pragma unroll
       for (int j = 0; j < 16; ++j) sx[i * 16 + j] = x[j];
       const float4* ar = reinterpret_cast<const float4*>(a.A + mo + (size_t)i * a.ld);
-      for (int k4 = 0; k4 < D / 4; ++k4) {
+      const bool a_ok = in_region((mo + (size_t)i * a.ld + D) * 4, a.a_span, a.status);
+      for (int k4 = 0; a_ok && k4 < D / 4; ++k4) {
         const float4 w = ar[k4];
         sA[i * (D + 1) + 4 * k4] = w.x;
         sA[i * (D + 1) + 4 * k4 + 1] = w.y;
@@ -392,8 +396,9 @@ __global__ void __launch_bounds__(kFoldThreads) chunk_fold_kernel(FoldArgs a) {
     if (row) {
       float y[16];
       const float* br = a.b + mo + (size_t)i * a.ld + 16 * cb;
+      const bool b_ok = !ident && in_region((mo + (size_t)i * a.ld + 16 * cb + 16) * 4, a.b_span, a.status);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) y[j] = ident ? 0.f : br[j];
+      for (int j = 0; j < 16; ++j) y[j] = b_ok ? br[j] : 0.f;
       for (int k = 0; k < D; ++k) {
         const float aik = sA[i * (D + 1) + k];
         const float4* xr = reinterpret_cast<const float4*>(sx + k * 16);
@@ -531,11 +536,12 @@ int run(const Problem& p, void* ws, cudaStream_t st) {
 
 int launch_chunk_fold(const float* A, const float* b, long long chunk_stride, int ld, int nchunks,
                       const float* state_in, float* starts, float* x_out, float* A_out, float* b_out, long long BH,
-                      int D, cudaStream_t st) {
+                      int D, cudaStream_t st, size_t a_span, size_t b_span, size_t starts_span) {
   const int smem = (D * (D + 1) + D * 16) * (int)sizeof(float);
   if (cudaFuncSetAttribute(chunk_fold_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return kCuda;
-  FoldArgs fa{A, b, chunk_stride, ld, nchunks, D, state_in, starts, x_out, A_out, b_out};
+  FoldArgs fa{A, b, chunk_stride, ld, nchunks, D, state_in, starts, x_out, A_out, b_out, device_status_word(),
+              a_span, b_span, starts_span};
   const long long ctas = BH * (D / 16) * (A_out ? 2 : 1);
   ProfScope ps(st, A_out ? "chunk_fold_summary" : "chunk_fold");
   chunk_fold_kernel<<<(unsigned)ctas, kFoldThreads, smem, st>>>(fa);

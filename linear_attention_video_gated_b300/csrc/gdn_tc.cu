@@ -205,6 +205,7 @@ struct GramArgs {
   // dO); no M image.  The A operand is then exact in bf16, so its lo part is zero
   // and its MMA is skipped.
   int b_only;
+  size_t m_span, b_span;  // extents (bytes) of the M image and b block regions (debug checks)
 };
 
 __global__ void __launch_bounds__(kGramThreads, 1)
@@ -430,7 +431,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         float v[16];
         tmem_ld16(acc + NA * 64 + 16 * cb, v);
         tmem_ld_wait();
-        if (i < D) {
+        if (i < D && in_region(((((size_t)f * ncb + cb) * D + i) * 16 + 16) * 4, a.b_span, a.status)) {
           float4* dst = reinterpret_cast<float4*>(a.b_blk + (((size_t)f * ncb + cb) * D + i) * 16);
 #pragma unroll
           for (int q = 0; q < 4; ++q)
@@ -445,7 +446,8 @@ __global__ void __launch_bounds__(kGramThreads, 1)
       fence_proxy_async_smem();
       named_barrier(1, 128);
       if (threadIdx.x == 0 && !a.b_only) {
-        bulk_s2g(a.m_img + (size_t)f * NA * D * 128, smem_u32(mstage), NA * D * 128);
+        if (in_region(((size_t)f + 1) * NA * D * 128, a.m_span, a.status))
+          bulk_s2g(a.m_img + (size_t)f * NA * D * 128, smem_u32(mstage), NA * D * 128);
         bulk_commit();
       }
     }
@@ -516,6 +518,9 @@ struct ScanArgs {
   // grid then has 2 D/16 column blocks per chunk (A's, then b's) and no image or
   // state_out is written.
   float* maps;
+  // extents (bytes) of the M image, b block, state image, maps and starts regions
+  // (debug checks)
+  size_t m_span, b_span, s_span, maps_span, starts_span;
 };
 
 template <int STAGES>
@@ -587,9 +592,10 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
         const uint32_t fb = smem_u32(&full[r.stage]);
         mbar_arrive_expect_tx(fb, NA * D * 128 + (use_b ? D * 64 : 0));
         const uint8_t* src = a.m_img + (size_t)f * NA * D * 128;
-        for (int at = 0; at < NA; ++at)
-          bulk_g2s(smem_u32(mring + r.stage * kScanMStage + at * 128 * 128), src + at * D * 128, D * 128, fb);
-        if (use_b)
+        if (in_region(((size_t)f + 1) * NA * D * 128, a.m_span, a.status))
+          for (int at = 0; at < NA; ++at)
+            bulk_g2s(smem_u32(mring + r.stage * kScanMStage + at * 128 * 128), src + at * D * 128, D * 128, fb);
+        if (use_b && in_region(((size_t)fbk * ncb + cb + 1) * D * 64, a.b_span, a.status))
           bulk_g2s(smem_u32(bring + r.stage * kScanBStage), a.b_blk + ((size_t)fbk * ncb + cb) * D * 16, D * 64, fb);
         r.mark_issued();
         r.advance();
@@ -607,8 +613,9 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       // gradient U it holds)
       auto store_block = [&](int u) {
         const long long f = bh * T + (a.reverse ? T - 2 - u : t0 + u);
-        bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(img + ((u + 1) & 1) * kScanImg),
-                 NA * 32 * 128);
+        if (in_region(((size_t)f * ncb + cb + 1) * NA * (32 * 128), a.s_span, a.status))
+          bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(img + ((u + 1) & 1) * kScanImg),
+                   NA * 32 * 128);
         bulk_commit();
       };
       // Descriptors of stage 0 / buffer 0; the other stages and buffers only move
@@ -651,7 +658,9 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
     for (int j = 0; j < 16; ++j) x[j] = (ident && i == 16 * cb + j) ? 1.f : 0.f;
     const float* s_init = a.starts ? a.starts + (size_t)(bh * a.nchunks + chunk_id) * D * D
                                    : (a.maps ? nullptr : (a.state_in ? a.state_in + (size_t)bh * D * D : nullptr));
-    if (row && s_init) {
+    const bool init_ok = !a.starts || in_region(((size_t)(bh * a.nchunks + chunk_id) * D * D + (size_t)i * D +
+                                                 16 * cb + 16) * 4, a.starts_span, a.status);
+    if (row && s_init && init_ok) {
       const float4* si = reinterpret_cast<const float4*>(s_init + (size_t)i * D + 16 * cb);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
@@ -744,10 +753,12 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       if (lane == 0) mbar_arrive(smem_u32(sready));
     }
     if (row && a.maps) {
-      float4* mo = reinterpret_cast<float4*>(a.maps + ((size_t)(bh * a.nchunks + chunk_id) * D + i) * 2 * D +
-                                             (ident ? 0 : D) + 16 * cb);
+      const size_t mo_end = ((size_t)(bh * a.nchunks + chunk_id) * D + i) * 2 * D + (ident ? 0 : D) + 16 * cb + 16;
+      float4* mo = reinterpret_cast<float4*>(a.maps + mo_end - 16);
+      if (in_region(mo_end * 4, a.maps_span, a.status)) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) mo[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        for (int q = 0; q < 4; ++q) mo[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+      }
     } else if (row && a.state_out && chunk_id == a.nchunks - 1) {
       float4* so = reinterpret_cast<float4*>(a.state_out + ((size_t)bh * D + i) * D + 16 * cb);
 #pragma unroll
@@ -790,6 +801,7 @@ struct OutArgs {
   // 1: multiply by S_t^T instead (the backward's dQ = dO S_t^T / sqrt(D)): the
   // same image read as an MN-major B operand.
   int transpose_s;
+  size_t s_span;  // extent (bytes) of the state image region (debug checks)
 };
 
 __global__ void __launch_bounds__(kOutThreads, 1)
@@ -858,11 +870,12 @@ __global__ void __launch_bounds__(kOutThreads, 1)
         mbar_arrive_expect_tx(afb, img_bytes);
         // block cb of the scan = [atom][hi 16 rows | lo 16 rows][128 B]
         const uint8_t* src = a.s_img + (size_t)f * img_bytes;
-        for (int cb = 0; cb < D / 16; ++cb)
-          for (int at = 0; at < NA; ++at)
-            for (int hl = 0; hl < 2; ++hl)
-              bulk_g2s(smem_u32(imgs + ra.stage * img_stride + (hl * NA + at) * D * 128 + cb * 16 * 128),
-                       src + ((size_t)cb * NA + at) * (32 * 128) + hl * 16 * 128, 16 * 128, afb);
+        if (in_region(((size_t)f + 1) * img_bytes, a.s_span, a.status))
+          for (int cb = 0; cb < D / 16; ++cb)
+            for (int at = 0; at < NA; ++at)
+              for (int hl = 0; hl < 2; ++hl)
+                bulk_g2s(smem_u32(imgs + ra.stage * img_stride + (hl * NA + at) * D * 128 + cb * 16 * 128),
+                         src + ((size_t)cb * NA + at) * (32 * 128) + hl * 16 * 128, 16 * 128, afb);
         ra.mark_issued();
         ra.advance();
         for (int tile = 0; tile < ntiles; ++tile) {
@@ -1005,15 +1018,20 @@ done:
 // states; the gram's b-only form gives E_t = Q_t^T dO_t / sqrt(D); the scan's
 // reverse form runs the state gradient U back through the adjoint map; the
 // read-out's transposed form gives dQ = dO S_t^T / sqrt(D).  The kernel below
-// does the rest, per frame-head and 128-token tile (K~ = K / sqrt(D*S)):
-//   P = K~ S_{t-1},  dR = K~ U_t                       (tensor core, hi + lo)
-//   R = beta (V - g P),  dP = -g beta dR,  dV = beta dR,
-//   dbeta_s = <dR_s, V_s - g P_s>,  dg partial = -sum_s beta_s <dR_s, P_s>
-//                                                      (fp32 registers)
-//   dK~ = R U_t^T + dP S_{t-1}^T                       (tensor core: R and dP as
-//                                                       bf16 A operands, the
-//                                                       images read MN-major)
-// plus <U_t, S_{t-1}> from the two images, added to tile 0's dg partial.
+// does the rest.  With K~ = K / sqrt(D*S), P = K~ S_{t-1} and dR = K~ U_t, the
+// gradients of a frame are
+//   dV = diag(beta) dR,
+//   dK~ = diag(beta) ((V - g P) U_t^T - g dR S_{t-1}^T),
+//   dbeta_s = <dR_s, V_s - g P_s>,  dg = <U_t, S_{t-1}> - sum_s beta_s <dR_s, P_s>.
+// With the symmetric D x D matrix W_t = S_{t-1} U_t^T + U_t S_{t-1}^T, formed once
+// per frame-head,  P U_t^T + dR S_{t-1}^T = K~ W_t,  <dR_s, P_s> = k~_s W_t k~_s^T / 2
+// and <U_t, S_{t-1}> = tr(W_t) / 2, so
+//   dK~ = diag(beta) (V U_t^T - g K~ W_t),
+//   dbeta_s = <k~_s, (V U_t^T)_s> - (g / 2) <k~_s, (K~ W_t)_s>,
+//   dg = tr(W_t) / 2 - (1 / 2) sum_s beta_s <k~_s, (K~ W_t)_s>:
+// three products per token tile, K U_t, V U_t^T and K W_t, whose A operands are
+// the bf16 inputs themselves (exact) and whose B operands are bf16 hi + lo images,
+// then element-wise work in fp32 registers.
 // =============================================================================
 
 // The initial state of every head as a scan block image (bf16 hi + lo), the
@@ -1040,7 +1058,9 @@ __global__ void __launch_bounds__(128) tc_state_image_kernel(const float* __rest
 }
 
 constexpr int kKvTok = 128;      // tokens per tile (MMA M)
-constexpr int kKvThreads = 448;  // 8 element-wise warps, 4 dK warps, 1 copy warp, 1 MMA warp
+constexpr int kKvThreads = 320;  // 8 element-wise warps, 1 MMA warp, 1 copy warp
+// TMEM columns: X1 = K U_t, X2 = V U_t^T, X3 = K W_t (one tile each), W_t
+constexpr uint32_t kTX1 = 0, kTX2 = 128, kTX3 = 256, kTW = 384;
 
 struct KvArgs {
   const uint8_t* s_img;   // S_t images (F slots, the scan's block layout)
@@ -1059,22 +1079,22 @@ struct KvArgs {
   int T, S, D, NA;
   float ck;  // 1/sqrt(D*S)
   unsigned int* status;
+  size_t s_span, s0_span, u_span;  // extents (bytes) of the image regions (debug checks)
 };
 
-// Persistent CTAs over frame-heads.  Per frame-head the S_{t-1} and U_t images
-// (bf16 hi + lo) are gathered once; then its 128-token tiles run through a
-// software pipeline:
-//   tensor core : P_b = K S_{t-1}, dR_b = K U_t for tile n (TMEM buffer b = n % 2,
-//                 hi and lo parts accumulated) issued before tile n - 1's
-//                 dK~ = R U_t^T + dP S_{t-1}^T (into tile n - 1's P buffer), so
-//                 the first MMAs of a tile overlap the element-wise stage of the
-//                 one before;
-//   warps 0-7   : the element-wise stage (two warps per TMEM lane quadrant,
-//                 alternate 16-column chunks): R over V in place, dP, dV, dbeta,
-//                 the dg partial sums;
-//   warps 8-11  : dK~ out of TMEM, scaled, to global memory;
-//   warp 12     : copies in, one slot each for K, V (then R) and dP.
-// dK and dV go to global memory straight from registers (one token row per thread).
+// Persistent CTAs over frame-heads.  Per frame-head: the S_{t-1} and U_t images
+// (bf16 hi + lo) are gathered; the MMA warp forms W_t in TMEM (six products per
+// K-step: S_hi U_hi, S_hi U_lo, S_lo U_hi and the same with S and U swapped); the
+// element-wise warps turn it into a bf16 hi + lo image in place of S_{t-1}'s
+// (row i of W is row i of its K-major image, W being symmetric) and sum its
+// trace.  Then per 128-token tile (K in a 2-deep ring, V single):
+//   warp 8 (MMA)    : X1 = K U_t, X3 = K W_t (K-major images), X2 = V U_t^T (U_t
+//                     read MN-major), all into TMEM;
+//   warps 0-7       : two per TMEM lane quadrant, alternate 16-column chunks:
+//                     dV, dK~ straight from registers to global memory, the
+//                     partial dots of dbeta and dg (halves combined in shared
+//                     memory, fixed order);
+//   warp 9 (copies) : K and V tiles by TMA, the images by bulk copies.
 __global__ void __launch_bounds__(kKvThreads, 1)
     tc_kv_grad_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV, KvArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -1083,50 +1103,49 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   const int img_bytes = 2 * NA * D * 128;  // one image: hi, then lo (a multiple of 1024)
   const int lo = NA * D * 128;             // offset of the lo part
   const int tile_bytes = NA * kKvTok * 128;
-  uint8_t* imgS = smem;
-  uint8_t* imgU = imgS + img_bytes;
-  uint8_t* tK = imgU + img_bytes;
-  uint8_t* tV = tK + tile_bytes;
-  uint8_t* tP = tV + tile_bytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(tP + tile_bytes);
-  uint64_t* ifull = bars;
-  uint64_t* iempty = bars + 1;
-  uint64_t* kfull = bars + 2;
-  uint64_t* kempty = bars + 3;
-  uint64_t* vfull = bars + 4;
-  uint64_t* vempty = bars + 5;   // V slot free: the tile's MMA2 has read R (and dP)
-  uint64_t* mma1 = bars + 8;     // [2] per TMEM buffer
-  uint64_t* mma2 = bars + 10;    // [2] per TMEM buffer
-  uint64_t* dkfree = bars + 12;  // [2] the dK warps have read that buffer's dK~
-  uint64_t* epi1 = bars + 14;
-  uint64_t* mma_done = bars + 15;
-  // per tile parity (a warp can start tile n + 1 while others still read tile n's):
-  float* red = reinterpret_cast<float*>(bars + 16);  // [2][8] per-warp partial sums of dg
-  float* dbh = red + 2 * 8;                          // [2][128] dbeta halves of the odd-chunk warps
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(dbh + 2 * kKvTok);
+  uint8_t* imgU = smem;
+  uint8_t* imgW = imgU + img_bytes;  // S_{t-1}, then W_t
+  uint8_t* tK = imgW + img_bytes;    // 2 slots
+  uint8_t* tV = tK + 2 * tile_bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(tV + tile_bytes);
+  uint64_t* ifull = bars;        // images landed
+  uint64_t* iempty = bars + 1;   // images free (the frame-head's last MMAs done)
+  uint64_t* wacc = bars + 2;     // W_t in TMEM
+  uint64_t* wimg = bars + 3;     // W_t image written (8 warps)
+  uint64_t* kfull = bars + 4;    // [2]
+  uint64_t* kempty = bars + 6;   // [2] (8 warps: K rows read after the tile's MMAs)
+  uint64_t* vfull = bars + 8;
+  uint64_t* vempty = bars + 9;   // the tile's MMAs done
+  uint64_t* xfull = bars + 10;   // X1..X3 in TMEM
+  uint64_t* xempty = bars + 11;  // X1..X3 read (8 warps)
+  uint64_t* mma_done = bars + 12;
+  float* red = reinterpret_cast<float*>(bars + 16);  // [2][8] per-warp dg partial sums, by tile parity
+  float* dbh = red + 2 * 8;                          // [2][128] dbeta halves of warps 4-7, by tile parity
+  float* trw = dbh + 2 * kKvTok;                     // [2][8] trace partials of W, by frame-head parity
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(trw + 2 * 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
-  constexpr int wcopy = 12, wmma = 13;
+  constexpr int wmma = 8, wcopy = 9;
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(ifull), 1);
     mbar_init(smem_u32(iempty), 1);
-    mbar_init(smem_u32(kfull), 1);
-    mbar_init(smem_u32(kempty), 1);
+    mbar_init(smem_u32(wacc), 1);
+    mbar_init(smem_u32(wimg), 8);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(smem_u32(&kfull[b]), 1);
+      mbar_init(smem_u32(&kempty[b]), 8);
+    }
     mbar_init(smem_u32(vfull), 1);
     mbar_init(smem_u32(vempty), 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(smem_u32(&mma1[b]), 1);
-      mbar_init(smem_u32(&mma2[b]), 1);
-      mbar_init(smem_u32(&dkfree[b]), 4);
-    }
-    mbar_init(smem_u32(epi1), 8);
+    mbar_init(smem_u32(xfull), 1);
+    mbar_init(smem_u32(xempty), 8);
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == wmma) {
-    tmem_alloc(smem_u32(tmem_slot), 512);  // buffer b: P (256b + 0..127, later dK~), dR (256b + 128..255)
+    tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -1140,18 +1159,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     if (lane == 0) {
       prefetch_tmap(&mapK);
       prefetch_tmap(&mapV);
-      Ring<1> ri, rk, rv;
+      Ring<1> ri, rv;
+      Ring<2> rk;
       bool ok = true;
       for (long long f = blockIdx.x; ok && f < a.nitems; f += gridDim.x) {
         for (int tile = 0; ok && tile < ntiles; ++tile) {
-          if (!wait_or_abort(smem_u32(kempty), rk.phase ^ 1, abort_flag, a.status)) {
+          if (!wait_or_abort(smem_u32(&kempty[rk.stage]), rk.phase ^ 1, abort_flag, a.status)) {
             ok = false;
             break;
           }
-          const uint32_t kb = smem_u32(kfull);
+          const uint32_t kb = smem_u32(&kfull[rk.stage]);
           mbar_arrive_expect_tx(kb, tile_bytes);
           for (int at = 0; at < NA; ++at)
-            tma_load_3d(smem_u32(tK + at * kKvTok * 128), &mapK, kb, 64 * at, tile * kKvTok, (int)f);
+            tma_load_3d(smem_u32(tK + rk.stage * tile_bytes + at * kKvTok * 128), &mapK, kb, 64 * at,
+                        tile * kKvTok, (int)f);
           rk.mark_issued();
           rk.advance();
           {  // into L2: this tile's V rows and the next tile's K rows (contiguous in memory)
@@ -1175,14 +1196,17 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const uint8_t* srcU = a.u_img + (size_t)f * img_bytes;
             const uint32_t ib = smem_u32(ifull);
             mbar_arrive_expect_tx(ib, 2 * img_bytes);
+            const bool s_ok = t > 0 ? in_region((size_t)f * img_bytes, a.s_span, a.status)
+                                    : in_region((size_t)(f / T + 1) * img_bytes, a.s0_span, a.status);
+            const bool u_ok = in_region(((size_t)f + 1) * img_bytes, a.u_span, a.status);
             // block cb of the scan = [atom][hi 16 rows | lo 16 rows][128 B]
             for (int cb = 0; cb < D / 16; ++cb)
               for (int at = 0; at < NA; ++at)
                 for (int hl = 0; hl < 2; ++hl) {
                   const size_t so = ((size_t)cb * NA + at) * (32 * 128) + hl * 16 * 128;
                   const uint32_t dof = hl * lo + at * D * 128 + cb * 16 * 128;
-                  bulk_g2s(smem_u32(imgS + dof), srcS + so, 16 * 128, ib);
-                  bulk_g2s(smem_u32(imgU + dof), srcU + so, 16 * 128, ib);
+                  if (s_ok) bulk_g2s(smem_u32(imgW + dof), srcS + so, 16 * 128, ib);
+                  if (u_ok) bulk_g2s(smem_u32(imgU + dof), srcU + so, 16 * 128, ib);
                 }
             ri.mark_issued();
             ri.advance();
@@ -1211,227 +1235,188 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       rv.drain(vfull);
     }
   } else if (warp == wmma) {
-    // ---------------- MMAs, software-pipelined: MMA1(n) goes out before MMA2(n - 1)
-    // (except at a frame-head boundary, where MMA2 of the previous head's last tile
-    // must finish before the new images may land)
+    // ---------------- MMAs
     if (lane == 0) {
-      const uint32_t idK = idesc_bf16(128, D, 0, 0);  // B = image, K-major (K = key dim)
-      const uint32_t idT = idesc_bf16(128, D, 0, 1);  // B = image, MN-major (K = value dim)
-      const uint32_t sS = smem_u32(imgS), sU = smem_u32(imgU);
-      const uint32_t aK = smem_u32(tK), aV = smem_u32(tV), aP = smem_u32(tP);
-      long long n = 0;        // tiles of this CTA so far
-      bool pending = false;   // tile n - 1 still needs its MMA2
-      bool pend_last = false;  // ... and it is its frame-head's last tile
-      uint32_t iph = 0;
-      // MMA2 of tile m: dK~ = R U^T + dP S^T into the P columns of buffer m % 2
-      auto mma2_of = [&](long long m, bool last_of_item) -> bool {
-        if (!wait_or_abort(smem_u32(epi1), (uint32_t)(m & 1), abort_flag, a.status)) return false;
-        tc_fence_after();
-        const int bm = (int)(m & 1);
-        const uint32_t acc = tmem + 256 * bm;
-        for (int kk = 0; kk < KS; ++kk) {
-          const uint32_t ko = (kk >> 2) * (kKvTok * 128) + (kk & 3) * 32;
-          const uint32_t mo = kk * 2048;
-          const uint64_t ar = smem_desc(aV + ko, 16, 1024), ap = smem_desc(aP + ko, 16, 1024);
-          mma_bf16(acc, ar, smem_desc(sU + mo, D * 128, 1024), idT, kk > 0 ? 1u : 0u);
-          mma_bf16(acc, ar, smem_desc(sU + lo + mo, D * 128, 1024), idT, 1u);
-          mma_bf16(acc, ap, smem_desc(sS + mo, D * 128, 1024), idT, 1u);
-          mma_bf16(acc, ap, smem_desc(sS + lo + mo, D * 128, 1024), idT, 1u);
-        }
-        mma_commit(smem_u32(&mma2[bm]));
-        mma_commit(smem_u32(vempty));
-        if (last_of_item) mma_commit(smem_u32(iempty));
-        return true;
-      };
+      const uint32_t idK = idesc_bf16(128, D, 0, 0);  // A K-major (tile), B K-major (image, K = key dim)
+      const uint32_t idT = idesc_bf16(128, D, 0, 1);  // A K-major (V tile), B MN-major (U image, K = value dim)
+      const uint32_t idW = idesc_bf16(128, D, 1, 1);  // A and B MN-major (images, K = value dim)
+      const uint32_t sU = smem_u32(imgU), sW = smem_u32(imgW);
+      const uint32_t aV = smem_u32(tV);
+      int ks = 0;
+      uint32_t kph = 0, vph = 0, xph = 0, iph = 0, wph = 0;
       for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
-        for (int tile = 0; tile < ntiles; ++tile, ++n) {
-          const int b = (int)(n & 1);
-          const uint32_t bph = (uint32_t)((n >> 1) & 1);
-          if (!wait_or_abort(smem_u32(kfull), (uint32_t)(n & 1), abort_flag, a.status)) goto done;
-          if (tile == 0) {
-            if (pending && !mma2_of(n - 1, pend_last)) goto done;
-            pending = false;
-            if (!wait_or_abort(smem_u32(ifull), iph, abort_flag, a.status)) goto done;
-            iph ^= 1;
-          }
-          // buffer b was last used by tile n - 2: its dK~ must have been read out
-          if (!wait_or_abort(smem_u32(&dkfree[b]), bph ^ 1, abort_flag, a.status)) goto done;
+        if (!wait_or_abort(smem_u32(ifull), iph, abort_flag, a.status)) goto done;
+        iph ^= 1;
+        tc_fence_after();
+        // W_t = S U^T + U S^T (K = value dim j; the images are [j][i], so both
+        // operands are MN-major); the lo x lo terms are below fp32 rounding
+        for (int kk = 0; kk < KS; ++kk) {
+          const uint32_t mo = kk * 2048;
+          const uint64_t sh = smem_desc(sW + mo, D * 128, 1024), sl = smem_desc(sW + lo + mo, D * 128, 1024);
+          const uint64_t uh = smem_desc(sU + mo, D * 128, 1024), ul = smem_desc(sU + lo + mo, D * 128, 1024);
+          mma_bf16(tmem + kTW, sh, uh, idW, kk > 0 ? 1u : 0u);
+          mma_bf16(tmem + kTW, sh, ul, idW, 1u);
+          mma_bf16(tmem + kTW, sl, uh, idW, 1u);
+          mma_bf16(tmem + kTW, uh, sh, idW, 1u);
+          mma_bf16(tmem + kTW, uh, sl, idW, 1u);
+          mma_bf16(tmem + kTW, ul, sh, idW, 1u);
+        }
+        mma_commit(smem_u32(wacc));
+        // the W image replaces S_{t-1}'s
+        if (!wait_or_abort(smem_u32(wimg), wph, abort_flag, a.status)) goto done;
+        wph ^= 1;
+        for (int tile = 0; tile < ntiles; ++tile) {
+          if (!wait_or_abort(smem_u32(&kfull[ks]), kph, abort_flag, a.status)) goto done;
+          if (!wait_or_abort(smem_u32(vfull), vph, abort_flag, a.status)) goto done;
+          if (!wait_or_abort(smem_u32(xempty), xph ^ 1, abort_flag, a.status)) goto done;
           tc_fence_after();
-          // P = K S_{t-1}, dR = K U_t (the key scale is applied by the element-wise warps)
-          for (int kk = 0; kk < KS; ++kk) {
+          const uint32_t aK = smem_u32(tK + ks * tile_bytes);
+          for (int kk = 0; kk < KS; ++kk) {  // K-dim = key dim i
             const uint32_t ko = (kk >> 2) * (kKvTok * 128) + (kk & 3) * 32;
             const uint32_t so = (kk >> 2) * (D * 128) + (kk & 3) * 32;
             const uint64_t ad = smem_desc(aK + ko, 16, 1024);
-            mma_bf16(tmem + 256 * b, ad, smem_desc(sS + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
-            mma_bf16(tmem + 256 * b, ad, smem_desc(sS + lo + so, 16, 1024), idK, 1u);
-            mma_bf16(tmem + 256 * b + 128, ad, smem_desc(sU + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
-            mma_bf16(tmem + 256 * b + 128, ad, smem_desc(sU + lo + so, 16, 1024), idK, 1u);
+            mma_bf16(tmem + kTX1, ad, smem_desc(sU + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + kTX1, ad, smem_desc(sU + lo + so, 16, 1024), idK, 1u);
+            mma_bf16(tmem + kTX3, ad, smem_desc(sW + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + kTX3, ad, smem_desc(sW + lo + so, 16, 1024), idK, 1u);
           }
-          mma_commit(smem_u32(&mma1[b]));
-          mma_commit(smem_u32(kempty));
-          if (pending && !mma2_of(n - 1, pend_last)) goto done;
-          pending = true;
-          pend_last = tile == ntiles - 1;
+          for (int kk = 0; kk < KS; ++kk) {  // K-dim = value dim j
+            const uint32_t ko = (kk >> 2) * (kKvTok * 128) + (kk & 3) * 32;
+            const uint32_t mo = kk * 2048;
+            const uint64_t ad = smem_desc(aV + ko, 16, 1024);
+            mma_bf16(tmem + kTX2, ad, smem_desc(sU + mo, D * 128, 1024), idT, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + kTX2, ad, smem_desc(sU + lo + mo, D * 128, 1024), idT, 1u);
+          }
+          mma_commit(smem_u32(xfull));
+          mma_commit(smem_u32(vempty));
+          if (tile == ntiles - 1) mma_commit(smem_u32(iempty));
+          xph ^= 1;
+          vph ^= 1;
+          if (++ks == 2) { ks = 0; kph ^= 1; }
         }
       }
-      if (pending && !mma2_of(n - 1, pend_last)) goto done;
     }
   } else if (warp < 8) {
-    // ---------------- element-wise stage: warp w owns token rows 32 (w % 4) .. + 31
-    // (its TMEM lane quadrant) and the 16-column chunks c with c % 2 == w / 4
+    // ---------------- element-wise: warp w owns TMEM lane quadrant w % 4 (token rows
+    // 32 (w % 4) .. + 31, or key rows of W) and the 16-column chunks c with c % 2 == w / 4
     const int quad = warp & 3, half = warp >> 2;
     const int row = quad * 32 + lane;
     const int et = threadIdx.x;  // 0 .. 255
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    long long n = 0;
-    uint32_t iph = 0;
-    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+    const float ck = a.ck;
+    long long n = 0;  // tiles of this CTA so far
+    int ks = 0;
+    uint32_t kph = 0, xph = 0, wph = 0;
+    int fpar = 0;  // frame-head parity (trace buffers)
+    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x, fpar ^= 1) {
       const float gt = decay_of(__ldg(a.g + f), a.gate_logits);
+      // ---- W_t out of TMEM into its hi + lo image (row i of W = image row i)
+      if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(wacc), wph, abort_flag, a.status))) goto done;
+      wph ^= 1;
+      tc_fence_after();
+      float tr = 0.f;
+      for (int c0 = 16 * half; c0 < D; c0 += 32) {
+        float w[16];
+        tmem_ld16(tmem + lane_base + kTW + c0, w);
+        tmem_ld_wait();
+        if (row < D) {
+          uint8_t* at = imgW + (c0 >> 6) * (D * 128);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            uint32_t hv[4], lv[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split2(w[8 * h + 2 * e], w[8 * h + 2 * e + 1], hv[e], lv[e]);
+            const uint32_t off = sw128_off(row, (c0 & 63) + 8 * h);
+            *reinterpret_cast<uint4*>(at + off) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
+            *reinterpret_cast<uint4*>(at + lo + off) = make_uint4(lv[0], lv[1], lv[2], lv[3]);
+          }
+          if (row >= c0 && row < c0 + 16) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (row == c0 + e) tr += w[e];
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) tr += __shfl_xor_sync(0xffffffffu, tr, o);
+      if (lane == 0) trw[8 * fpar + warp] = tr;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(wimg));
+      // ---- the frame-head's tiles
       for (int tile = 0; tile < ntiles; ++tile, ++n) {
-        const int b = (int)(n & 1);
-        const uint32_t bph = (uint32_t)((n >> 1) & 1);
+        const int par = (int)(n & 1);
         const int s = tile * kKvTok + row;
         const bool valid = s < S;
         const float bt = valid ? beta_of(__ldg(a.beta + f * S + s), a.gate_logits) : 0.f;
-        __nv_bfloat16* dvrow = a.dv + (f * S + s) * D;
-        // this tile's V (loaded once the previous tile's MMA2 had read the V and
-        // dP slots) and its first MMAs
-        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(vfull), (uint32_t)(n & 1), abort_flag, a.status) &&
-                                         wait_or_abort(smem_u32(&mma1[b]), bph, abort_flag, a.status)))
-          goto done;
+        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(xfull), xph, abort_flag, a.status))) goto done;
+        xph ^= 1;
         tc_fence_after();
-        uint8_t* vslot = tV;
-        uint8_t* pslot = tP;
-        float part = 0.f;
-        if (tile == 0) {
-          // <U_t, S_{t-1}> over the images (positions past D excluded: never written)
-          if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(ifull), iph, abort_flag, a.status))) goto done;
-          const int nch = NA * D * 8;  // 16-byte chunks of one hi (or lo) part
-          for (int c = et; c < nch; c += 256) {
-            const int at = c / (D * 8), r = (c / 8) % D, pc = c % 8;
-            if (64 * at + 8 * (pc ^ (r & 7)) >= D) continue;
-            const uint32_t off = (uint32_t)c * 16;
-            const uint4 sh = *reinterpret_cast<const uint4*>(imgS + off);
-            const uint4 sl = *reinterpret_cast<const uint4*>(imgS + lo + off);
-            const uint4 uh = *reinterpret_cast<const uint4*>(imgU + off);
-            const uint4 ul = *reinterpret_cast<const uint4*>(imgU + lo + off);
-            const uint32_t w[4][4] = {{sh.x, sh.y, sh.z, sh.w}, {sl.x, sl.y, sl.z, sl.w},
-                                      {uh.x, uh.y, uh.z, uh.w}, {ul.x, ul.y, ul.z, ul.w}};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 a0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[0][e]));
-              const float2 a1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[1][e]));
-              const float2 b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[2][e]));
-              const float2 b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[3][e]));
-              part = fmaf(a0.x + a1.x, b0.x + b1.x, part);
-              part = fmaf(a0.y + a1.y, b0.y + b1.y, part);
-            }
-          }
-          iph ^= 1;
-        }
-        float db = 0.f, dgp = 0.f;
+        const uint8_t* kt = tK + ks * (NA * kKvTok * 128);
+        __nv_bfloat16* dvrow = a.dv + (f * S + s) * D;
+        __nv_bfloat16* dkrow = a.dk + (f * S + s) * D;
+        float dot2 = 0.f, dot3 = 0.f;
         for (int c0 = 16 * half; c0 < D; c0 += 32) {
-          float pv[16], rv[16];
-          tmem_ld16(tmem + lane_base + 256 * b + c0, pv);
-          tmem_ld16(tmem + lane_base + 256 * b + 128 + c0, rv);
+          float x1[16], x2[16], x3[16];
+          tmem_ld16(tmem + lane_base + kTX1 + c0, x1);
+          tmem_ld16(tmem + lane_base + kTX2 + c0, x2);
+          tmem_ld16(tmem + lane_base + kTX3 + c0, x3);
           tmem_ld_wait();
-          const uint32_t ab = (c0 >> 6) * (kKvTok * 128);
-          uint4 dvo[2];
+          uint32_t ov[8], ok[8];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint32_t off = ab + sw128_off(row, (c0 & 63) + 8 * h);
-            const uint4 vv = *reinterpret_cast<const uint4*>(vslot + off);
-            const uint32_t vw[4] = {vv.x, vv.y, vv.z, vv.w};
-            uint32_t ro[4], po[4], vo[4];
+            const uint4 kv = *reinterpret_cast<const uint4*>(kt + (c0 >> 6) * (kKvTok * 128) +
+                                                             sw128_off(row, (c0 & 63) + 8 * h));
+            const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float2 v2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vw[e]));
-              const float p0 = a.ck * pv[8 * h + 2 * e], p1 = a.ck * pv[8 * h + 2 * e + 1];
-              const float d0 = a.ck * rv[8 * h + 2 * e], d1 = a.ck * rv[8 * h + 2 * e + 1];
-              const float r0 = v2.x - gt * p0, r1 = v2.y - gt * p1;
-              db = fmaf(d0, r0, fmaf(d1, r1, db));
-              dgp = fmaf(d0, p0, fmaf(d1, p1, dgp));
-              ro[e] = pack_bf16(bt * r0, bt * r1);
-              po[e] = pack_bf16(-gt * bt * d0, -gt * bt * d1);
-              vo[e] = pack_bf16(bt * d0, bt * d1);
+              const float2 k2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&kw[e]));
+              const int j = 8 * h + 2 * e;
+              dot2 = fmaf(k2.x, x2[j], fmaf(k2.y, x2[j + 1], dot2));
+              dot3 = fmaf(k2.x, x3[j], fmaf(k2.y, x3[j + 1], dot3));
+              ov[4 * h + e] = pack_bf16(bt * ck * x1[j], bt * ck * x1[j + 1]);
+              ok[4 * h + e] = pack_bf16(bt * ck * fmaf(-gt * ck, x3[j], x2[j]),
+                                        bt * ck * fmaf(-gt * ck, x3[j + 1], x2[j + 1]));
             }
-            *reinterpret_cast<uint4*>(vslot + off) = make_uint4(ro[0], ro[1], ro[2], ro[3]);
-            *reinterpret_cast<uint4*>(pslot + off) = make_uint4(po[0], po[1], po[2], po[3]);
-            dvo[h] = make_uint4(vo[0], vo[1], vo[2], vo[3]);
           }
           if (valid) {
-            reinterpret_cast<uint4*>(dvrow + c0)[0] = dvo[0];
-            reinterpret_cast<uint4*>(dvrow + c0)[1] = dvo[1];
+            reinterpret_cast<uint4*>(dvrow + c0)[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+            reinterpret_cast<uint4*>(dvrow + c0)[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+            reinterpret_cast<uint4*>(dkrow + c0)[0] = make_uint4(ok[0], ok[1], ok[2], ok[3]);
+            reinterpret_cast<uint4*>(dkrow + c0)[1] = make_uint4(ok[4], ok[5], ok[6], ok[7]);
           }
         }
-        float* redb = red + 8 * b;
-        float* dbhb = dbh + kKvTok * b;
-        if (half == 1) dbhb[row] = db;
-        part -= bt * dgp;
+        // this tile's TMEM and K rows are read
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(xempty));
+          mbar_arrive(smem_u32(&kempty[ks]));
+        }
+        if (++ks == 2) { ks = 0; kph ^= 1; }
+        // dbeta_s = ck <k_s, X2_s> - (g / 2) ck^2 <k_s, X3_s>, this half's columns
+        const float db = ck * dot2 - 0.5f * gt * ck * ck * dot3;
+        // dg partial: -(1/2) ck^2 sum_s beta_s <k_s, X3_s> (rows past S have beta 0)
+        float part = -0.5f * ck * ck * bt * dot3;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-        if (lane == 0) redb[warp] = part;
-        tc_fence_before();
-        fence_proxy_async_smem();
-        named_barrier(1, 256);  // R, dP written; dbeta halves and partial sums in place
+        if (lane == 0) red[8 * par + warp] = part;
+        if (half == 1) dbh[kKvTok * par + row] = db;
+        named_barrier(1, 256);  // partial sums and dbeta halves in place
         if (half == 0 && valid) {
-          const float dbt = db + dbhb[row];
+          const float dbt = db + dbh[kKvTok * par + row];
           a.dbeta[f * S + s] = a.gate_logits ? dbt * bt * (1.f - bt) : dbt;
         }
         if (et == 0) {
           float tot = 0.f;
-          for (int w = 0; w < 8; ++w) tot += redb[w];
+          for (int w8 = 0; w8 < 8; ++w8) tot += red[8 * par + w8];
+          if (tile == 0) {  // <U_t, S_{t-1}> = tr(W_t) / 2
+            float t2 = 0.f;
+            for (int w8 = 0; w8 < 8; ++w8) t2 += trw[8 * fpar + w8];
+            tot += 0.5f * t2;
+          }
           a.dg_part[f * ntiles + tile] = tot;
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(epi1));
-      }
-    }
-  } else if (warp < 12) {
-    // ---------------- dK: warp 8 + q drains rows 32q .. 32q + 31 of dK~
-    const int quad = warp - 8;
-    const int row = quad * 32 + lane;
-    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    long long n = 0;
-    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
-      for (int tile = 0; tile < ntiles; ++tile, ++n) {
-        const int b = (int)(n & 1);
-        const int s = tile * kKvTok + row;
-        const bool valid = s < S;
-        __nv_bfloat16* dkrow = a.dk + (f * S + s) * D;
-        if (!__all_sync(0xffffffffu,
-                        wait_or_abort(smem_u32(&mma2[b]), (uint32_t)((n >> 1) & 1), abort_flag, a.status)))
-          goto done;
-        tc_fence_after();
-        // two rounds of up to four 16-column chunks: all of a round's loads go out
-        // before its first wait
-#pragma unroll
-        for (int r = 0; r < 2; ++r) {
-          float kv[4][16];
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (16 * (4 * r + c) < D) tmem_ld16(tmem + lane_base + 256 * b + 16 * (4 * r + c), kv[c]);
-#pragma unroll
-          for (int c = 0; c < 4; ++c)
-            if (16 * (4 * r + c) < D) tmem_ld_wait_regs(kv[c]);
-          if (r == 1) {  // every TMEM read of this buffer is done
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&dkfree[b]));
-          }
-          if (valid) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-              const int col = 16 * (4 * r + c);
-              if (col < D) {
-                uint32_t o[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) o[e] = pack_bf16(a.ck * kv[c][2 * e], a.ck * kv[c][2 * e + 1]);
-                reinterpret_cast<uint4*>(dkrow + col)[0] = make_uint4(o[0], o[1], o[2], o[3]);
-                reinterpret_cast<uint4*>(dkrow + col)[1] = make_uint4(o[4], o[5], o[6], o[7]);
-              }
-            }
-          }
         }
       }
     }
@@ -1462,7 +1447,7 @@ int num_sms() {
 }
 
 constexpr int kBarBytes = 256;
-constexpr int kKvBarBytes = 1536;  // barriers, partial sums and dbeta halves of tc_kv_grad_kernel
+constexpr int kKvBarBytes = 1792;  // barriers, partial sums, dbeta halves and trace partials of tc_kv_grad_kernel
 
 // Every kernel here asks for more than half of the SM's shared memory, so two of
 // them never share an SM (the gram and read-out kernels allocate all of TMEM).
@@ -1470,6 +1455,7 @@ int gram_smem(int NA, int D) {
   return kGramRaw * kRawStage + kGramConv * kConvStage + NA * D * 128 + kBetaRing + kBarBytes + 1024;
 }
 int kv_smem(int NA, int D) { return 4 * NA * D * 128 + 3 * NA * kKvTok * 128 + kKvBarBytes + 1024; }
+static_assert(4 * 2 * 128 * 128 + 3 * 2 * kKvTok * 128 + 1792 + 1024 <= 232448, "kv_grad shared memory at D = 128");
 template <int STAGES>
 int scan_smem() { return STAGES * (kScanMStage + kScanBStage) + 2 * kScanImg + kBarBytes + 1024; }
 
@@ -1484,6 +1470,7 @@ ScanArgs one_pass(const uint8_t* m_img, const float* b_blk, const float* g, int 
   sa.nchunks = 1;
   sa.starts = nullptr;
   sa.maps = nullptr;
+  sa.m_span = sa.b_span = sa.s_span = sa.maps_span = sa.starts_span = 0;
   return sa;
 }
 
@@ -1510,8 +1497,9 @@ size_t tc_workspace_bytes(const Problem& p, int mode) { return tc_layout(p, mode
 
 namespace {
 
-// The gram over every frame-head of the call: the M_t images and b_t blocks.
-int launch_gram(const Problem& p, uint8_t* m_img, float* b_mat, cudaStream_t st) {
+// The gram over every frame-head of the call: the M_t images and b_t blocks
+// (regions of m_span and b_span bytes).
+int launch_gram(const Problem& p, uint8_t* m_img, float* b_mat, size_t m_span, size_t b_span, cudaStream_t st) {
   const int NA = num_atoms(p.D);
   const long long F = p.BHT();
   CUtensorMap mapK, mapV;
@@ -1520,7 +1508,7 @@ int launch_gram(const Problem& p, uint8_t* m_img, float* b_mat, cudaStream_t st)
   if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return kCuda;
   GramArgs ga{p.beta, p.gate_logits, p.variant, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale,
-              p.key_scale, p.status};
+              p.key_scale, p.status, 0, m_span, b_span};
   const int nsm = num_sms();
   const unsigned grid = (unsigned)(F < nsm ? F : nsm);
   ProfScope ps(st, "tc_gram");
@@ -1529,13 +1517,16 @@ int launch_gram(const Problem& p, uint8_t* m_img, float* b_mat, cudaStream_t st)
 }
 
 // The chunked scan's summary form: [A_c | b_c] of every (head, chunk) into `maps`.
-int launch_chunk_summaries(const Problem& p, const uint8_t* m_img, const float* b_mat, float* maps, int nch,
-                           cudaStream_t st) {
+int launch_chunk_summaries(const Problem& p, const TcLayout& L, const uint8_t* m_img, const float* b_mat,
+                           float* maps, int nch, cudaStream_t st) {
   ScanArgs sa = one_pass(m_img, b_mat, p.g, p.gate_logits, p.variant, nullptr, nullptr, nullptr, p.T, p.D,
                          p.status, 0);
   sa.chunk = kTcChunk;
   sa.nchunks = nch;
   sa.maps = maps;
+  sa.m_span = L.b_off - L.m_off;
+  sa.b_span = L.s_off - L.b_off;
+  sa.maps_span = L.starts_off - L.maps_off;
   return launch_scan<2>(sa, p.BH() * nch * 2 * (p.D / 16), st, "tc_chunk_summary");
 }
 
@@ -1546,9 +1537,10 @@ int tc_chunk_maps(const Problem& p, void* ws, float** maps, int* nchunks, cudaSt
   uint8_t* w = static_cast<uint8_t*>(ws);
   const int nch = (p.T + kTcChunk - 1) / kTcChunk;
   float* mp = reinterpret_cast<float*>(w + L.maps_off);
-  int rc = launch_gram(p, w + L.m_off, reinterpret_cast<float*>(w + L.b_off), st);
+  int rc = launch_gram(p, w + L.m_off, reinterpret_cast<float*>(w + L.b_off), L.b_off - L.m_off, L.s_off - L.b_off,
+                       st);
   if (rc != kOk) return rc;
-  rc = launch_chunk_summaries(p, w + L.m_off, reinterpret_cast<float*>(w + L.b_off), mp, nch, st);
+  rc = launch_chunk_summaries(p, L, w + L.m_off, reinterpret_cast<float*>(w + L.b_off), mp, nch, st);
   if (rc != kOk) return rc;
   *maps = mp;
   *nchunks = nch;
@@ -1568,7 +1560,9 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
   CUtensorMap mapQ, mapO;
   if (!make_map(&mapQ, p.q, p.D, p.S, F, kOutTok) || !make_map(&mapO, p.out, p.D, p.S, F, 32)) return kCuda;
 
-  int rc = launch_gram(p, m_img, b_mat, st);
+  const size_t m_span = L.b_off - L.m_off, b_span = L.s_off - L.b_off;
+  const size_t s_span = (p.mode == GDN_MODE_PREFIX ? L.maps_off : L.total) - L.s_off;
+  int rc = launch_gram(p, m_img, b_mat, m_span, b_span, st);
   if (rc != kOk) return rc;
   if (p.mode == GDN_MODE_PREFIX) {
     // chunk summaries [A_c | b_c] -> the fold over chunk boundaries (float32) ->
@@ -1576,21 +1570,29 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
     const int nch = (p.T + kTcChunk - 1) / kTcChunk;
     float* maps = reinterpret_cast<float*>(w + L.maps_off);
     float* starts = reinterpret_cast<float*>(w + L.starts_off);
-    rc = launch_chunk_summaries(p, m_img, b_mat, maps, nch, st);
+    rc = launch_chunk_summaries(p, L, m_img, b_mat, maps, nch, st);
     if (rc != kOk) return rc;
+    const size_t maps_span = L.starts_off - L.maps_off, starts_span = L.total - L.starts_off;
     rc = launch_chunk_fold(maps, maps + p.D, 2LL * p.D * p.D, 2 * p.D, nch, p.state_in, starts, nullptr, nullptr,
-                           nullptr, p.BH(), p.D, st);
+                           nullptr, p.BH(), p.D, st, maps_span, maps_span - p.D * 4, starts_span);
     if (rc != kOk) return rc;
     ScanArgs sa = one_pass(m_img, b_mat, p.g, p.gate_logits, p.variant, nullptr, s_img, p.state_out, p.T, p.D,
                            p.status, 0);
     sa.chunk = kTcChunk;
     sa.nchunks = nch;
     sa.starts = starts;
+    sa.m_span = m_span;
+    sa.b_span = b_span;
+    sa.s_span = s_span;
+    sa.starts_span = starts_span;
     rc = launch_scan<2>(sa, p.BH() * nch * (p.D / 16), st, "tc_chunk_replay");
     if (rc != kOk) return rc;
   } else {
     ScanArgs sa = one_pass(m_img, b_mat, p.g, p.gate_logits, p.variant, p.state_in, s_img, p.state_out, p.T, p.D,
                            p.status, 0);
+    sa.m_span = m_span;
+    sa.b_span = b_span;
+    sa.s_span = s_span;
     rc = launch_scan<4>(sa, p.BH() * (p.D / 16), st, "tc_scan");
     if (rc != kOk) return rc;
   }
@@ -1598,7 +1600,9 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
     const int smem = out_smem(NA, p.D);
     if (cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
-    OutArgs oa{s_img, p.variant, static_cast<__nv_bfloat16*>(p.out), F, p.S, p.D, NA, p.out_scale, p.status};
+    const size_t shrink = debug_shrink();
+    OutArgs oa{s_img, p.variant, static_cast<__nv_bfloat16*>(p.out), F, p.S, p.D, NA, p.out_scale, p.status, 0,
+               s_span > shrink ? s_span - shrink : 1};
     const unsigned grid = (unsigned)(F < nsm ? F : nsm);
     ProfScope ps(st, "tc_readout");
     tc_readout_kernel<<<grid, kOutThreads, smem, st>>>(mapQ, mapO, oa);
@@ -1678,28 +1682,33 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st,
   if (!states_ready) {
     {
       GramArgs ga{p.beta, p.gate_logits, kGdn, m_img, e_blk, F, p.S, D, NA, p.key_scale * p.key_scale, p.key_scale,
-                  p.status, 0};
+                  p.status, 0, L.e_off - L.m_off, L.s_off - L.e_off};
       ProfScope ps(st, "tc_gram");
       tc_gram_kernel<<<pgrid, kGramThreads, gsmem, st>>>(mapK, mapV, ga);
     }
     if (cudaGetLastError() != cudaSuccess) return kCuda;
-    const int rc = launch_scan<4>(one_pass(m_img, e_blk, p.g, p.gate_logits, kGdn, p.state_in, s_img, nullptr, p.T,
-                                           D, p.status, 0),
-                                  sgrid, st, "tc_scan");
+    ScanArgs sa = one_pass(m_img, e_blk, p.g, p.gate_logits, kGdn, p.state_in, s_img, nullptr, p.T, D, p.status, 0);
+    sa.m_span = L.e_off - L.m_off;
+    sa.b_span = L.s_off - L.e_off;
+    sa.s_span = L.u_off - L.s_off;
+    const int rc = launch_scan<4>(sa, sgrid, st, "tc_scan");
     if (rc != kOk) return rc;
   }
   // E_t = Q_t^T dO_t / sqrt(D) (overwrites b_t, which the scan has consumed)
   {
-    GramArgs ga{nullptr, 0, kGdn, nullptr, e_blk, F, p.S, D, NA, 0.f, p.out_scale, p.status, 1};
+    GramArgs ga{nullptr, 0, kGdn, nullptr, e_blk, F, p.S, D, NA, 0.f, p.out_scale, p.status, 1, 0, L.s_off - L.e_off};
     ProfScope ps(st, "tc_bwd_qdo");
     tc_gram_kernel<<<pgrid, kGramThreads, gsmem, st>>>(mapQ, mapDO, ga);
   }
   if (cudaGetLastError() != cudaSuccess) return kCuda;
   // U_t for every frame and dS_0, by the reverse scan
   {
-    const int rc = launch_scan<4>(one_pass(m_img, e_blk, p.g, p.gate_logits, kGdn, gr.dstate_out, u_img,
-                                           gr.dstate_in, p.T, D, p.status, 1),
-                                  sgrid, st, "tc_bwd_rscan");
+    ScanArgs sa = one_pass(m_img, e_blk, p.g, p.gate_logits, kGdn, gr.dstate_out, u_img, gr.dstate_in, p.T, D,
+                           p.status, 1);
+    sa.m_span = L.e_off - L.m_off;
+    sa.b_span = L.s_off - L.e_off;
+    sa.s_span = L.s0_off - L.u_off;
+    const int rc = launch_scan<4>(sa, sgrid, st, "tc_bwd_rscan");
     if (rc != kOk) return rc;
   }
   {
@@ -1714,7 +1723,8 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st,
     KvArgs ka{s_img, s0_img, u_img, p.g, p.beta, static_cast<const __nv_bfloat16*>(p.k),
               static_cast<const __nv_bfloat16*>(p.v), p.gate_logits,
               static_cast<__nv_bfloat16*>(gr.dk),
-              static_cast<__nv_bfloat16*>(gr.dv), gr.dbeta, dg_part, F, p.T, p.S, D, NA, p.key_scale, p.status};
+              static_cast<__nv_bfloat16*>(gr.dv), gr.dbeta, dg_part, F, p.T, p.S, D, NA, p.key_scale, p.status,
+              L.u_off - L.s_off, L.dg_off - L.s0_off, L.s0_off - L.u_off};
     ProfScope ps(st, "tc_bwd_kv_grad");
     tc_kv_grad_kernel<<<pgrid, kKvThreads, smem, st>>>(mapK128, mapV128, ka);
   }
@@ -1724,7 +1734,8 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st,
     const int smem = out_smem(NA, D);
     if (cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
       return kCuda;
-    OutArgs oa{s_img, kGdn, static_cast<__nv_bfloat16*>(gr.dq), F, p.S, D, NA, p.out_scale, p.status, 1};
+    OutArgs oa{s_img, kGdn, static_cast<__nv_bfloat16*>(gr.dq), F, p.S, D, NA, p.out_scale, p.status, 1,
+               L.u_off - L.s_off};
     ProfScope ps(st, "tc_bwd_q_grad");
     tc_readout_kernel<<<pgrid, kOutThreads, smem, st>>>(mapDO128, mapDQ, oa);
   }

@@ -41,12 +41,17 @@ def test_header_declares_the_boundary():
         assert required in names
 
 
-def test_library_exports_every_declared_symbol(lib):
-    out = subprocess.run(["nm", "-D", "--defined-only", binding.LIB_PATH], capture_output=True, text=True).stdout
+@pytest.mark.parametrize("debug", [False, True], ids=["release", "debug"])
+def test_library_exports_every_declared_symbol(lib, debug):
+    path = binding.DEBUG_LIB_PATH if debug else binding.LIB_PATH
+    if debug:
+        build_lib.build(debug=True)
+    handle = binding.debug_lib() if debug else lib
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
     exported = set(re.findall(r"\bT (gdn_\w+)$", out, flags=re.M))
     for name in declared_functions():
         assert name in exported, name
-        assert hasattr(lib, name)
+        assert hasattr(handle, name)
 
 
 def test_status_strings(lib):
