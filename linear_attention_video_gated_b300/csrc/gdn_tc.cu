@@ -188,8 +188,6 @@ constexpr int kGramRaw = 4;
 constexpr int kGramConv = 2;
 constexpr int kRawStage = 4 * kGramRegion;   // K atoms (NA) then V atoms (NA): 32 KB
 constexpr int kConvStage = 4 * kGramRegion;  // AH atoms (2) then AL atoms (2): 32 KB
-constexpr int kBetaAhead = 3;                // beta fetched this many 64-token chunks ahead
-constexpr int kBetaRing = (kBetaAhead + 1) * kGramTok * 4;  // its shared-memory ring, bytes
 
 struct GramArgs {
   const float* beta;
@@ -216,8 +214,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   uint8_t* raw = smem;
   uint8_t* conv = raw + kGramRaw * kRawStage;
   uint8_t* mstage = conv + kGramConv * kConvStage;  // NA x D rows x 128 B
-  float* bring = reinterpret_cast<float*>(mstage + NA * D * 128);  // beta: (kBetaAhead + 1) x 64 tokens
-  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(bring) + kBetaRing);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(mstage + NA * D * 128);
   uint64_t* raw_full = bars;
   uint64_t* raw_empty = raw_full + kGramRaw;
   uint64_t* conv_full = raw_empty + kGramRaw;
@@ -335,44 +332,29 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     int rs = 0, cs = 0;
     uint32_t rph = 0, cph = 0;
     const int units = NA * kGramTok * 8;  // 16-byte chunks of K per tile
-    // This thread's chunks lie in tile rows r0 and r0 + 32.  Their beta values
-    // reach shared memory by asynchronous copies kBetaAhead chunks ahead (one
-    // lane of each group of 8 fetches its rows for the warp), so no register
-    // waits on a global load.  Rows past S (or past the last frame-head) read
-    // as -inf, which maps to 0.
+    // This thread's chunks lie in tile rows r0 and r0 + 32; their beta values are
+    // loaded one tile ahead so the load latency stays off the critical path.
     const int r0 = ct >> 3;
-    const bool unit_beta = a.variant == kReluLinear || a.b_only;
-    const bool copier = (lane & 7) == 0 && !unit_beta;
-    long long fl = blockIdx.x;  // the chunk whose beta is fetched next
-    int cl = 0;
-    auto fetch = [&](int slot) {
-      if (copier) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int rw = r0 + 32 * h;
-          const int s = cl * kGramTok + rw;
-          float* dst = bring + slot * kGramTok + rw;
-          if (fl < a.nitems && s < S)
-            cp_async4(smem_u32(dst), a.beta + fl * S + s);
-          else
-            *dst = -INFINITY;
-        }
-      }
-      cp_async_commit();
-      if (++cl == nchunks) { cl = 0; fl += gridDim.x; }
+    auto beta_at = [&](long long f, int c, int rw) {
+      const int s = c * kGramTok + rw;
+      // raw value, mapped when used: mapping here would wait for the load
+      if (!(f < a.nitems && s < S)) return -INFINITY;
+      return (a.variant == kReluLinear || a.b_only) ? 1.f : __ldg(a.beta + f * S + s);
     };
-    auto mapped = [&](float x) { return x == -INFINITY ? 0.f : beta_of(x, a.gate_logits); };
-    for (int d = 0; d < kBetaAhead; ++d) fetch(d);
-    int n = 0;  // chunks converted so far
+    long long fn = blockIdx.x;
+    int cn = 0;
+    // beta of token rows r0 and r0 + 32: raw values loaded one tile ahead, mapped
+    // (rows past S, loaded as -inf, give 0) after the current tile is converted.
+    auto mapped = [&](float x) {
+      return x == -INFINITY ? 0.f : ((a.variant == kReluLinear || a.b_only) ? x : beta_of(x, a.gate_logits));
+    };
+    float bn0 = beta_at(fn, 0, r0), bn1 = beta_at(fn, 0, r0 + 32);
+    float b0 = mapped(bn0), b1 = mapped(bn1);
     for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
-      for (int c = 0; c < nchunks; ++c, ++n) {
-        __syncwarp();  // every lane has read the slot the next fetch overwrites
-        fetch((n + kBetaAhead) % (kBetaAhead + 1));
-        cp_async_wait<kBetaAhead>();  // this chunk's copies have landed
-        __syncwarp();
-        const float* bsl = bring + (n % (kBetaAhead + 1)) * kGramTok;
-        const float b0 = unit_beta ? (c * kGramTok + r0 < S ? 1.f : 0.f) : mapped(bsl[r0]);
-        const float b1 = unit_beta ? (c * kGramTok + r0 + 32 < S ? 1.f : 0.f) : mapped(bsl[r0 + 32]);
+      for (int c = 0; c < nchunks; ++c) {
+        if (++cn == nchunks) { cn = 0; fn += gridDim.x; }
+        bn0 = beta_at(fn, cn, r0);
+        bn1 = beta_at(fn, cn, r0 + 32);
         const bool ok = wait_or_abort(smem_u32(&raw_full[rs]), rph, abort_flag, a.status) &&
                         wait_or_abort(smem_u32(&conv_empty[cs]), cph ^ 1, abort_flag, a.status);
         if (!__all_sync(0xffffffffu, ok)) goto done;
@@ -396,6 +378,8 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         if (lane == 0) mbar_arrive(smem_u32(&conv_full[cs]));
         if (++rs == kGramRaw) { rs = 0; rph ^= 1; }
         if (++cs == kGramConv) { cs = 0; cph ^= 1; }
+        b0 = mapped(bn0);
+        b1 = mapped(bn1);
       }
     }
   } else {
@@ -453,7 +437,6 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     }
   }
 done:
-  cp_async_wait_all();  // the beta copies still in flight (converter lanes) have landed
   if (threadIdx.x == 0) bulk_wait0();  // M image stores complete
   if (warp == 13 && lane == 0) {  // every MMA this CTA issued has completed
     mma_commit(smem_u32(mma_done));
@@ -488,7 +471,7 @@ done:
 //   replay  : each chunk from its true initial state (`starts`), writing the
 //             S_t images as the single pass does.
 // =============================================================================
-constexpr int kScanThreads = 192;         // 4 epilogue, 1 copy, 1 MMA warps
+constexpr int kScanThreads = 192;         // 4 epilogue warps (thread 0 issues the MMAs), 1 copy warp, 1 TMEM warp
 constexpr int kScanMStage = 2 * 128 * 128;  // M image: 2 atoms x 128 rows x 128 B
 constexpr int kScanBStage = 128 * 64;       // b block: up to 128 rows x 16 floats
 constexpr int kScanImg = 2 * 32 * 128;      // state block image: 2 atoms x 32 rows (hi 0-15, lo 16-31) x 128 B
@@ -536,8 +519,7 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
   uint64_t* full = bars;
   uint64_t* empty = full + STAGES;
   uint64_t* pfull = empty + STAGES;
-  uint64_t* sready = pfull + 1;
-  uint64_t* mma_done = sready + 1;
+  uint64_t* mma_done = pfull + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -560,14 +542,18 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       mbar_init(smem_u32(&empty[s]), 5);  // the MMA's commit + the 4 epilogue warps (b read)
     }
     mbar_init(smem_u32(pfull), 1);
-    mbar_init(smem_u32(sready), 4);  // each epilogue warp, once its rows of the state image are written
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  // M image rows D..127 (never copied in) must be finite: zero them once.
-  for (int idx = threadIdx.x; idx < STAGES * kScanMStage / 16; idx += blockDim.x)
-    reinterpret_cast<uint4*>(mring)[idx] = make_uint4(0, 0, 0, 0);
+  // M image rows D..127 of each atom (never copied in) must be finite: zero them once.
+  {
+    const int tail = (128 - D) * 8;  // 16-byte chunks per atom
+    for (int idx = threadIdx.x; idx < STAGES * 2 * tail; idx += blockDim.x) {
+      const int region = idx / tail, c = idx % tail;  // region = stage * 2 + atom
+      reinterpret_cast<uint4*>(mring + region * (128 * 128) + D * 128)[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
   fence_proxy_async_smem();
   if (warp == 5) {
     tmem_alloc(smem_u32(tmem_slot), 32);  // P_hi (columns 0-15) and P_lo (16-31)
@@ -602,64 +588,66 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       }
       r.drain(full);
     }
-  } else if (warp == 5) {
-    // ---------------- MMA: P = M_t S_{t-1}[:, J]
-    if (lane == 0) {
-      const uint32_t id = idesc_bf16(128, 32, 0, 0);
-      const bool store = a.s_img != nullptr;
-      // the state block after step u (image buffer (u + 1) & 1; u = -1 is the
-      // initial state) to global memory, laid out as in shared memory: the slot
-      // of frame t0 + u, or in reverse slot T - 2 - u (the frame index of the
-      // gradient U it holds)
-      auto store_block = [&](int u) {
-        const long long f = bh * T + (a.reverse ? T - 2 - u : t0 + u);
-        if (in_region(((size_t)f * ncb + cb + 1) * NA * (32 * 128), a.s_span, a.status))
-          bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(img + ((u + 1) & 1) * kScanImg),
-                   NA * 32 * 128);
-        bulk_commit();
-      };
-      // Descriptors of stage 0 / buffer 0; the other stages and buffers only move
-      // the start address (a 16-byte-unit field, well inside its 14 bits here).
-      uint64_t ad0[8], bd0[8];
+  } else if (warp < 4) {
+    // ---------------- epilogue (4 warps): thread i owns row i of the column block.
+    // Thread 0 also issues each step's MMA, once the 4 warps have written the
+    // state image it reads (a named barrier among them, no hand-off to another warp).
+    const int i = threadIdx.x;
+    const bool row = i < D;
+    const bool store = a.s_img != nullptr;
+    bool fail = false;  // thread 0: an MMA step could not be issued (wait gave up)
+    // Thread 0's MMA state: the ring position of the next step's M_t image and
+    // b_t block, and the descriptors of stage 0 / image buffer 0 (the other
+    // stages and buffers only move the start address, a 16-byte-unit field well
+    // inside its 14 bits here).
+    int mstage = 0;
+    uint32_t mphase = 0;
+    uint64_t ad0[8], bd0[8];
+    const uint32_t id = idesc_bf16(128, 32, 0, 0);
+    if (i == 0) {
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         ad0[kk] = smem_desc(smem_u32(mring) + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
         bd0[kk] = smem_desc(smem_u32(img) + (kk >> 2) * (32 * 128) + (kk & 3) * 32, 16, 1024);
       }
-      int stage = 0;
-      uint32_t phase = 0;
-      for (int j = 0; j < nsteps; ++j) {
-        if (!wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status)) goto done;
-        if (!wait_or_abort(smem_u32(sready), j & 1, abort_flag, a.status)) goto done;
-        tc_fence_after();
-        const uint64_t ao = (uint64_t)((stage * kScanMStage) >> 4);
-        const uint64_t bo = (uint64_t)(((j & 1) * kScanImg) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          if (kk < KS) mma_bf16(tmem, ad0[kk] + ao, bd0[kk] + bo, id, kk > 0 ? 1u : 0u);
-        if (store && (j >= 1 || a.reverse)) store_block(j - 1);
-        // The store of S_{j-2} has read its buffer, which S_j may now overwrite.
-        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-        mma_commit(smem_u32(pfull));
-        mma_commit(smem_u32(&empty[stage]));
-        if (++stage == STAGES) { stage = 0; phase ^= 1; }
-      }
-      if (store && nsteps > 0 && !a.reverse) {  // the reverse scan's last result is dS_0 (state_out only)
-        if (!wait_or_abort(smem_u32(sready), nsteps & 1, abort_flag, a.status)) goto done;
-        store_block(nsteps - 1);
-      }
     }
-  } else {
-    // ---------------- epilogue (4 warps): thread i owns row i of the column block
-    const int i = threadIdx.x;
-    const bool row = i < D;
+    // the state block after step u (image buffer (u + 1) & 1; u = -1 is the
+    // initial state) to global memory, laid out as in shared memory: the slot
+    // of frame t0 + u, or in reverse slot T - 2 - u (the frame index of the
+    // gradient U it holds)
+    auto store_block = [&](int u) {
+      const long long f = bh * T + (a.reverse ? T - 2 - u : t0 + u);
+      if (in_region(((size_t)f * ncb + cb + 1) * NA * (32 * 128), a.s_span, a.status))
+        bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(img + ((u + 1) & 1) * kScanImg),
+                 NA * 32 * 128);
+      bulk_commit();
+    };
+    // thread 0: step j's MMA, P = M_t S_{j-1}[:, J], reading image buffer j & 1
+    auto issue = [&](int j) -> bool {
+      if (!wait_or_abort(smem_u32(&full[mstage]), mphase, abort_flag, a.status)) return false;
+      tc_fence_after();
+      const uint64_t ao = (uint64_t)((mstage * kScanMStage) >> 4);
+      const uint64_t bo = (uint64_t)(((j & 1) * kScanImg) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)
+        if (kk < KS) mma_bf16(tmem, ad0[kk] + ao, bd0[kk] + bo, id, kk > 0 ? 1u : 0u);
+      if (store && (j >= 1 || a.reverse)) store_block(j - 1);
+      // The store of S_{j-2} has read its buffer, which S_j may now overwrite.
+      asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+      mma_commit(smem_u32(pfull));
+      mma_commit(smem_u32(&empty[mstage]));
+      if (++mstage == STAGES) { mstage = 0; mphase ^= 1; }
+      return true;
+    };
     float x[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) x[j] = (ident && i == 16 * cb + j) ? 1.f : 0.f;
     const float* s_init = a.starts ? a.starts + (size_t)(bh * a.nchunks + chunk_id) * D * D
                                    : (a.maps ? nullptr : (a.state_in ? a.state_in + (size_t)bh * D * D : nullptr));
-    const bool init_ok = !a.starts || in_region(((size_t)(bh * a.nchunks + chunk_id) * D * D + (size_t)i * D +
-                                                 16 * cb + 16) * 4, a.starts_span, a.status);
+    // (rows past D read nothing, so they check nothing)
+    const bool init_ok = !a.starts || !row ||
+                         in_region(((size_t)(bh * a.nchunks + chunk_id) * D * D + (size_t)i * D + 16 * cb + 16) * 4,
+                                   a.starts_span, a.status);
     if (row && s_init && init_ok) {
       const float4* si = reinterpret_cast<const float4*>(s_init + (size_t)i * D + 16 * cb);
 #pragma unroll
@@ -699,58 +687,61 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
     };
     write_img(img);  // the initial state into buffer 0
     fence_proxy_async_smem();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(sready));
-    int stage = 0;
-    uint32_t phase = 0;
+    named_barrier(1, 128);
+    if (i == 0 && nsteps > 0) fail = !issue(0);
     const bool relu_lin = a.variant == kReluLinear;  // g = 1, no delta-rule term
     // raw decay of the next step's frame; mapped when used
     float gnext = (nsteps > 0 && !relu_lin) ? __ldg(a.g + bh * T + (a.reverse ? T - 1 : t0)) : 0.f;
+    int stage = 0;
+    uint32_t phase = 0;
     for (int j = 0; j < nsteps; ++j) {  // j counts steps; the step's frame is fr
       const int fr = a.reverse ? T - 1 - j : t0 + j;
       const long long f = bh * T + fr;
       const float gt = relu_lin ? 1.f : decay_of(gnext, a.gate_logits);
       if (j + 1 < nsteps && !relu_lin) gnext = __ldg(a.g + (a.reverse ? f - 1 : f + 1));
       const bool add_b = use_b && !(a.reverse && fr == 0);  // E_{-1} = 0
-      const bool ok = wait_or_abort(smem_u32(pfull), j & 1, abort_flag, a.status) &&
+      const bool ok = !fail && wait_or_abort(smem_u32(pfull), j & 1, abort_flag, a.status) &&
                       wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
-      if (__all_sync(0xffffffffu, ok)) {
-        tc_fence_after();
-        float p[16], pl[16];
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), p);
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16, pl);
-        float bv[16];
-#pragma unroll
-        for (int q = 0; q < 16; ++q) bv[q] = 0.f;
-        if (row && use_b) {
-          const float4* bp = reinterpret_cast<const float4*>(bring + stage * kScanBStage + i * 64);
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float4 w = bp[q];
-            bv[4 * q] = w.x;
-            bv[4 * q + 1] = w.y;
-            bv[4 * q + 2] = w.z;
-            bv[4 * q + 3] = w.w;
-          }
-        }
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
-        if (row) {
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            x[jj] = relu_lin ? x[jj] + bv[jj] : fmaf(gt, x[jj] - (p[jj] + pl[jj]), add_b ? bv[jj] : 0.f);
-        }
-        // S_j goes into the buffer of S_{j-2}, whose store has read it (the MMA
-        // thread waited for that before committing pfull(j)).
-        write_img(img + ((j + 1) & 1) * kScanImg);
-        fence_proxy_async_smem();
-      }
-      if (++stage == STAGES) { stage = 0; phase ^= 1; }
       if (!__all_sync(0xffffffffu, ok)) goto done;
+      tc_fence_after();
+      float p[16], pl[16];
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), p);
+      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16, pl);
+      float bv[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) bv[q] = 0.f;
+      if (row && use_b) {
+        const float4* bp = reinterpret_cast<const float4*>(bring + stage * kScanBStage + i * 64);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 w = bp[q];
+          bv[4 * q] = w.x;
+          bv[4 * q + 1] = w.y;
+          bv[4 * q + 2] = w.z;
+          bv[4 * q + 3] = w.w;
+        }
+      }
+      tmem_ld_wait();
+      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(sready));
+      if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+      if (row) {
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj)
+          x[jj] = relu_lin ? x[jj] + bv[jj] : fmaf(gt, x[jj] - (p[jj] + pl[jj]), add_b ? bv[jj] : 0.f);
+      }
+      // S_j goes into the buffer of S_{j-2}, whose store has read it (thread 0
+      // waited for that before committing pfull(j)).
+      write_img(img + ((j + 1) & 1) * kScanImg);
+      fence_proxy_async_smem();
+      if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      named_barrier(1, 128);  // S_j's image is complete; every TMEM read of step j is done
+      if (i == 0) {
+        if (j + 1 < nsteps)
+          fail = !issue(j + 1);
+        else if (store && !a.reverse)  // the reverse scan's last result is dS_0 (state_out only)
+          store_block(nsteps - 1);
+      }
     }
     if (row && a.maps) {
       const size_t mo_end = ((size_t)(bh * a.nchunks + chunk_id) * D + i) * 2 * D + (ident ? 0 : D) + 16 * cb + 16;
@@ -766,8 +757,8 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
     }
   }
 done:
-  if (warp == 5 && lane == 0) {
-    bulk_wait0();  // state block stores complete
+  if (threadIdx.x == 0) {  // the thread that issued the MMAs and the image stores
+    bulk_wait0();          // state block stores complete
     mma_commit(smem_u32(mma_done));
     wait_bounded(smem_u32(mma_done), 0, 500000000ull);
   }
@@ -1452,7 +1443,7 @@ constexpr int kKvBarBytes = 1792;  // barriers, partial sums, dbeta halves and t
 // Every kernel here asks for more than half of the SM's shared memory, so two of
 // them never share an SM (the gram and read-out kernels allocate all of TMEM).
 int gram_smem(int NA, int D) {
-  return kGramRaw * kRawStage + kGramConv * kConvStage + NA * D * 128 + kBetaRing + kBarBytes + 1024;
+  return kGramRaw * kRawStage + kGramConv * kConvStage + NA * D * 128 + kBarBytes + 1024;
 }
 int kv_smem(int NA, int D) { return 4 * NA * D * 128 + 3 * NA * kKvTok * 128 + kKvBarBytes + 1024; }
 static_assert(4 * 2 * 128 * 128 + 3 * 2 * kKvTok * 128 + 1792 + 1024 <= 232448, "kv_grad shared memory at D = 128");

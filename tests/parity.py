@@ -3,20 +3,22 @@ tolerance checks.
 
 Tolerances (written here, used by every parity test):
   * float32 I/O: max |gpu - oracle| <= 1e-4, for out and for the final state.
-  * bf16 I/O, strict (the five named workloads): max |gpu - oracle| / rms(oracle)
-    <= 2e-2, per tensor (out and the final state separately).
-  * bf16 I/O, edge shapes (arbitrary initial states and shapes): an element of a
-    bf16 output can never be closer to the exact value than half a bf16 ulp, and
-    when the output's distribution is heavy-tailed (e.g. a large initial state
-    dominating the first frames) that representation error alone exceeds
-    2e-2 x rms at the largest elements.  There the bound is
-    |gpu - oracle| <= 0.5 ulp_bf16(oracle) + 2e-2 x rms(oracle) per element.
-  * bf16 I/O, always: rms(gpu - oracle) / rms(oracle) <= 5e-3.  Derivation: RNE
+  * bf16 outputs: the error beyond the output type's own representation,
+    max(|gpu - oracle| - 0.5 ulp_bf16(oracle)) <= 2e-2 x rms(oracle), per tensor.
+    No bf16 output can be closer to the exact value than half an ulp, so the part
+    of the error within half an ulp is the output type's, not the kernel's; where
+    the largest outputs are many times the rms that part alone exceeds
+    2e-2 x rms: on the one-minute workload, head (0, 6) has outputs of 8-16 x rms,
+    the correctly rounded exact result itself misses the plain max-abs form, and
+    the kernels' outputs there were 0.0225 x rms from the oracle of which
+    6.4e-5 x rms lay beyond half an ulp.
+  * bf16 outputs, also: rms(gpu - oracle) / rms(oracle) <= 5e-3.  Derivation: RNE
     rounding of the outputs gives ~1.6e-3 (uniform error of up to 2^-9 relative,
     averaged over the significand range); the kernels' bf16 hi+lo operand splits
     add < 1e-4; single-bf16 operands where a split is needed would add ~1e-3 on
     top and still pass, a wrong or dropped term would not.
-The final state is float32 and always held to the strict bound.
+  * The final state (float32) of a bf16 call: max |gpu - oracle| <= 2e-2 x rms and
+    the plain form (no representation allowance).
 """
 from __future__ import annotations
 
@@ -147,9 +149,8 @@ def errors(gpu, ref):
             "finite": bool(np.all(np.isfinite(gpu)))}
 
 
-def assert_parity(wl_dtype, out_gpu, out_ref, st_gpu, st_ref, what="", strict=True):
-    """strict=True: the named workloads' bound; strict=False: edge shapes, with the
-    half-ulp representation allowance on bf16 outputs (see the module docstring)."""
+def assert_parity(wl_dtype, out_gpu, out_ref, st_gpu, st_ref, what=""):
+    """The bounds of the module docstring, for the outputs and the final state."""
     eo = errors(out_gpu, out_ref)
     es = errors(st_gpu, st_ref)
     assert eo["finite"] and es["finite"], f"{what}: non-finite values"
@@ -158,8 +159,7 @@ def assert_parity(wl_dtype, out_gpu, out_ref, st_gpu, st_ref, what="", strict=Tr
         assert es["max_abs"] <= F32_MAX_ABS, f"{what}: state {es}"
         return eo, es
     if eo["rms_ref"] > 0:
-        key = "max_abs_over_rms" if strict else "max_beyond_half_ulp_over_rms"
-        assert eo[key] <= BF16_MAX_ABS_OVER_RMS, f"{what}: out {eo}"
+        assert eo["max_beyond_half_ulp_over_rms"] <= BF16_MAX_ABS_OVER_RMS, f"{what}: out {eo}"
         assert eo["rms_err_over_rms"] <= BF16_RMS_ERR_OVER_RMS, f"{what}: out {eo}"
     else:
         assert eo["max_abs"] == 0.0, f"{what}: out {eo}"

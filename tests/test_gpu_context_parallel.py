@@ -11,7 +11,8 @@ rank's own compose, exactly, into the state entering its range).
   * the rank driver, context_parallel.frame_fwd_cp, with two processes sharing
     the GPU and exchanging their summaries through gloo on the host (the kernels
     of the two processes never wait on each other), against the oracle.
-Tolerances as tests/parity.py (float32 I/O 1e-4 max-abs; bf16 2e-2 x rms)."""
+Tolerances as tests/parity.py (float32 I/O 1e-4 max-abs; bf16 outputs 2e-2 x rms
+beyond their own representation; float32 maps of bf16 calls 2e-2 x rms)."""
 import os
 import socket
 
@@ -146,7 +147,7 @@ def test_ranges_in_one_process_equal_the_single_pass(case, mode):
         ro, rs = oracle.frame_fwd_from_logits(x["q"], x["k"], x["v"], lg["g_logit"], lg["beta_logit"], S0)
     else:
         ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0)
-    eo, es = parity.assert_parity(dt, np_(out), ro, np_(state), rs, f"ranges {case} mode={mode}", strict=not nz)
+    eo, es = parity.assert_parity(dt, np_(out), ro, np_(state), rs, f"ranges {case} mode={mode}")
     print(f"ranges {case} mode={mode}: out {eo} state {es}")
 
 

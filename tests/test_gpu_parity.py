@@ -77,8 +77,7 @@ def test_edge_shapes(case, mode):
     si = None if S0 is None else torch.from_numpy(S0).cuda()
     out, st = run(*parity.upload(wl, x), state_in=si, mode=mode)
     ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0)
-    # the half-ulp allowance only where a non-zero initial state makes the outputs heavy-tailed
-    eo, es = parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"edge {case} mode={mode}", strict=not nz)
+    eo, es = parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"edge {case} mode={mode}")
     print(f"edge {case} mode={mode}: out {eo} state {es}")
 
 
@@ -137,7 +136,7 @@ def test_relu_linear_baseline(case, mode):
     torch.cuda.synchronize()
     parity.check_status()
     ro, rs = oracle.relu_linear_fwd(x["q"], x["k"], x["v"], S0)
-    eo, es = parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"relu-linear {case} mode={mode}", strict=not nz)
+    eo, es = parity.assert_parity(dt, np_(out), ro, np_(st), rs, f"relu-linear {case} mode={mode}")
     print(f"relu-linear {case} mode={mode}: out {eo} state {es}")
 
 

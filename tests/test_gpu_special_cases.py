@@ -6,8 +6,8 @@ writes only the beta-weighted residual, keys are scaled by 1/sqrt(D*S)).
 Each case runs through the CUDA path (every algorithm form, float32 and bf16
 I/O) and is compared element by element with the fp64 oracle on the same
 seeded inputs (tolerances in tests/parity.py: 1e-4 max-abs for float32 I/O,
-2e-2 x rms for bf16 I/O, the half-ulp allowance only where a non-zero initial
-state makes the outputs heavy-tailed), and, where the special case fixes the
+2e-2 x rms beyond the output's own bf16 representation for bf16 I/O), and,
+where the special case fixes the
 result in closed form, with that closed form too (computed here in float64 from
 the inputs, not through the oracle):
 
@@ -70,13 +70,11 @@ def check(wl, x, S0, mode, what, closed=None):
     """GPU vs oracle (and vs the closed form `closed` = (out, state), float64)."""
     out, st = run(wl, x, S0, mode)
     ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"], S0)
-    strict = S0 is None
-    eo, es = parity.assert_parity(wl.dtype, np_(out), ro, np_(st), rs, f"{what} mode={mode} vs oracle", strict)
+    eo, es = parity.assert_parity(wl.dtype, np_(out), ro, np_(st), rs, f"{what} mode={mode} vs oracle")
     print(f"{what} mode={mode}: vs oracle out {eo} state {es}")
     if closed is not None:
         co, cs = closed
-        eo, es = parity.assert_parity(wl.dtype, np_(out), co, np_(st), cs, f"{what} mode={mode} vs closed form",
-                                      strict)
+        eo, es = parity.assert_parity(wl.dtype, np_(out), co, np_(st), cs, f"{what} mode={mode} vs closed form")
         print(f"{what} mode={mode}: vs closed form out {eo} state {es}")
     return out, st
 
@@ -116,7 +114,7 @@ def test_g_zero_is_memoryless(case, mode):
     kt = x["k"].astype(np.float64) / np.sqrt(D * S)
     St = np.einsum("bhtsi,bhts,bhtsj->bhtij", kt, x["beta"].astype(np.float64), x["v"].astype(np.float64))
     co = np.einsum("bhtsi,bhtij->bhtsj", x["q"].astype(np.float64), St) / np.sqrt(D)
-    # S_0 has no effect: compared strictly (the outputs do not depend on it)
+    # S_0 has no effect: the call from S_0 equals the zero-state call bit for bit
     out_a, st_a = run(wl, x, S0, mode)
     out_b, st_b = check(wl, x, None, mode, f"g=0 {case}", closed=(co, St[:, :, -1]))
     assert torch.equal(out_a, out_b) and torch.equal(st_a, st_b), "the initial state leaked through g = 0"
