@@ -49,6 +49,7 @@ struct TcLayout {
   size_t m_off, b_off, s_off, total;
   size_t m_bytes, b_bytes, s_bytes;  // per frame-head
   size_t maps_off, starts_off;       // prefix form: chunk maps [A|b] and chunk starts
+  size_t carry_off;                  // pipelined form: the state carried between frame chunks
 };
 
 constexpr int kTcChunkFrames = 16;  // frames per chunk of the prefix form
@@ -70,6 +71,10 @@ TcLayout tc_layout(const Problem& p, int mode = GDN_MODE_SPLIT) {
     L.maps_off = L.total;
     L.starts_off = align_up(L.maps_off + (size_t)p.BH() * nch * 2 * mat, 1024);
     L.total = align_up(L.starts_off + (size_t)p.BH() * nch * mat, 1024);
+  }
+  if (mode == GDN_MODE_PIPELINED) {
+    L.carry_off = L.total;
+    L.total = align_up(L.carry_off + (size_t)p.BH() * p.D * p.D * 4, 1024);
   }
   return L;
 }
@@ -158,6 +163,15 @@ struct Ring {
   }
 };
 
+// Work items of the persistent gram and read-out kernels: item i is frame-head i,
+// or (L > 0: one frame chunk of every head) frame t0 + i % L of head i / L.
+struct ItemMap {
+  int T, t0, L;
+  __host__ __device__ long long f(long long it) const {
+    return L ? (long long)((int)it / L) * T + t0 + (int)it % L : it;  // items < 2^31 (validated)
+  }
+};
+
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&v);
@@ -204,6 +218,7 @@ struct GramArgs {
   // and its MMA is skipped.
   int b_only;
   size_t m_span, b_span;  // extents (bytes) of the M image and b block regions (debug checks)
+  ItemMap map;            // items -> frame-heads (zero: item i is frame-head i)
 };
 
 __global__ void __launch_bounds__(kGramThreads, 1)
@@ -267,7 +282,8 @@ __global__ void __launch_bounds__(kGramThreads, 1)
       prefetch_tmap(&mapV);
       Ring<kGramRaw> r;
       bool ok = true;
-      for (long long f = blockIdx.x; ok && f < a.nitems; f += gridDim.x) {
+      for (long long it = blockIdx.x; ok && it < a.nitems; it += gridDim.x) {
+        const long long f = a.map.f(it);
         for (int c = 0; c < nchunks; ++c) {
           if (!wait_or_abort(smem_u32(&raw_empty[r.stage]), r.phase ^ 1, abort_flag, a.status)) {
             ok = false;
@@ -293,7 +309,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
       const uint32_t id2 = idesc_bf16(128, D, 1, 1);
       int rs = 0, cs = 0, ab = 0;
       uint32_t rph = 0, cph = 0, aph = 0;
-      for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+      for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
         if (!wait_or_abort(smem_u32(&accempty[ab]), aph ^ 1, abort_flag, a.status)) goto done;
         tc_fence_after();
         const uint32_t acc = tmem + ab * 256;
@@ -331,15 +347,16 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     const int ct = threadIdx.x - 128;
     int rs = 0, cs = 0;
     uint32_t rph = 0, cph = 0;
-    const int units = NA * kGramTok * 8;  // 16-byte chunks of K per tile
+    const int units = NA * kGramTok * 8;  // 16-byte chunks of K per tile (at most 4 per thread)
+    const bool relu_k = a.variant == kReluLinear;
     // This thread's chunks lie in tile rows r0 and r0 + 32; their beta values are
     // loaded one tile ahead so the load latency stays off the critical path.
     const int r0 = ct >> 3;
-    auto beta_at = [&](long long f, int c, int rw) {
+    auto beta_at = [&](long long it, int c, int rw) {
       const int s = c * kGramTok + rw;
       // raw value, mapped when used: mapping here would wait for the load
-      if (!(f < a.nitems && s < S)) return -INFINITY;
-      return (a.variant == kReluLinear || a.b_only) ? 1.f : __ldg(a.beta + f * S + s);
+      if (!(it < a.nitems && s < S)) return -INFINITY;
+      return (a.variant == kReluLinear || a.b_only) ? 1.f : __ldg(a.beta + a.map.f(it) * S + s);
     };
     long long fn = blockIdx.x;
     int cn = 0;
@@ -350,7 +367,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     };
     float bn0 = beta_at(fn, 0, r0), bn1 = beta_at(fn, 0, r0 + 32);
     float b0 = mapped(bn0), b1 = mapped(bn1);
-    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+    for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
       for (int c = 0; c < nchunks; ++c) {
         if (++cn == nchunks) { cn = 0; fn += gridDim.x; }
         bn0 = beta_at(fn, cn, r0);
@@ -360,16 +377,32 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         if (!__all_sync(0xffffffffu, ok)) goto done;
         const uint8_t* kt = raw + rs * kRawStage;
         uint8_t* ah = conv + cs * kConvStage;
-        for (int u = ct, rr = 0; u < units; u += 256, ++rr) {
-          const float bs = (rr & 1) ? b1 : b0;
-          const uint4 kv = *reinterpret_cast<const uint4*>(kt + u * 16);
-          const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
-          uint32_t hi[4], lo[4];
+        // This thread's (at most four) 16-byte chunks: every load issued before any
+        // arithmetic, so the shared-memory latencies overlap.
+        uint4 kv[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
-            split2(bs * relu_if(x.x, a.variant), bs * relu_if(x.y, a.variant), hi[e], lo[e]);
+        for (int rr = 0; rr < 4; ++rr)
+          if (ct + 256 * rr < units) kv[rr] = *reinterpret_cast<const uint4*>(kt + (ct + 256 * rr) * 16);
+#pragma unroll
+        for (int rr = 0; rr < 4; ++rr) {
+          if (ct + 256 * rr >= units) break;
+          const float bs = (rr & 1) ? b1 : b0;
+          const uint32_t w[4] = {kv[rr].x, kv[rr].y, kv[rr].z, kv[rr].w};
+          uint32_t hi[4], lo[4];
+          if (relu_k) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+              split2(bs * fmaxf(x.x, 0.f), bs * fmaxf(x.y, 0.f), hi[e], lo[e]);
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+              split2(bs * x.x, bs * x.y, hi[e], lo[e]);
+            }
           }
+          const int u = ct + 256 * rr;
           *reinterpret_cast<uint4*>(ah + u * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(ah + 2 * kGramRegion + u * 16) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
@@ -388,7 +421,8 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     const int ncb = D / 16;
     int ab = 0;
     uint32_t aph = 0;
-    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+    for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
+      const long long f = a.map.f(it);
       if (threadIdx.x == 0) bulk_wait_read0();  // the previous M image store has read the stage
       const bool ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[ab]), aph, abort_flag, a.status));
       if (barrier_any(1, 128, !ok || *abort_flag)) goto done;
@@ -471,7 +505,7 @@ done:
 //   replay  : each chunk from its true initial state (`starts`), writing the
 //             S_t images as the single pass does.
 // =============================================================================
-constexpr int kScanThreads = 192;         // 4 epilogue warps (thread 0 issues the MMAs), 1 copy warp, 1 TMEM warp
+constexpr int kScanThreads = 192;         // 4 epilogue, 1 copy, 1 MMA warps
 constexpr int kScanMStage = 2 * 128 * 128;  // M image: 2 atoms x 128 rows x 128 B
 constexpr int kScanBStage = 128 * 64;       // b block: up to 128 rows x 16 floats
 constexpr int kScanImg = 2 * 32 * 128;      // state block image: 2 atoms x 32 rows (hi 0-15, lo 16-31) x 128 B
@@ -519,7 +553,8 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
   uint64_t* full = bars;
   uint64_t* empty = full + STAGES;
   uint64_t* pfull = empty + STAGES;
-  uint64_t* mma_done = pfull + 1;
+  uint64_t* sready = pfull + 1;
+  uint64_t* mma_done = sready + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -542,6 +577,7 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       mbar_init(smem_u32(&empty[s]), 5);  // the MMA's commit + the 4 epilogue warps (b read)
     }
     mbar_init(smem_u32(pfull), 1);
+    mbar_init(smem_u32(sready), 4);  // each epilogue warp, once its rows of the state image are written
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -588,57 +624,57 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       }
       r.drain(full);
     }
-  } else if (warp < 4) {
-    // ---------------- epilogue (4 warps): thread i owns row i of the column block.
-    // Thread 0 also issues each step's MMA, once the 4 warps have written the
-    // state image it reads (a named barrier among them, no hand-off to another warp).
-    const int i = threadIdx.x;
-    const bool row = i < D;
-    const bool store = a.s_img != nullptr;
-    bool fail = false;  // thread 0: an MMA step could not be issued (wait gave up)
-    // Thread 0's MMA state: the ring position of the next step's M_t image and
-    // b_t block, and the descriptors of stage 0 / image buffer 0 (the other
-    // stages and buffers only move the start address, a 16-byte-unit field well
-    // inside its 14 bits here).
-    int mstage = 0;
-    uint32_t mphase = 0;
-    uint64_t ad0[8], bd0[8];
-    const uint32_t id = idesc_bf16(128, 32, 0, 0);
-    if (i == 0) {
+  } else if (warp == 5) {
+    // ---------------- MMA: P = M_t S_{t-1}[:, J]
+    if (lane == 0) {
+      const uint32_t id = idesc_bf16(128, 32, 0, 0);
+      const bool store = a.s_img != nullptr;
+      // the state block after step u (image buffer (u + 1) & 1; u = -1 is the
+      // initial state) to global memory, laid out as in shared memory: the slot
+      // of frame t0 + u, or in reverse slot T - 2 - u (the frame index of the
+      // gradient U it holds)
+      auto store_block = [&](int u) {
+        const long long f = bh * T + (a.reverse ? T - 2 - u : t0 + u);
+        if (in_region(((size_t)f * ncb + cb + 1) * NA * (32 * 128), a.s_span, a.status))
+          bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(img + ((u + 1) & 1) * kScanImg),
+                   NA * 32 * 128);
+        bulk_commit();
+      };
+      // Descriptors of stage 0 / buffer 0; the other stages and buffers only move
+      // the start address (a 16-byte-unit field, well inside its 14 bits here).
+      uint64_t ad0[8], bd0[8];
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) {
         ad0[kk] = smem_desc(smem_u32(mring) + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
         bd0[kk] = smem_desc(smem_u32(img) + (kk >> 2) * (32 * 128) + (kk & 3) * 32, 16, 1024);
       }
-    }
-    // the state block after step u (image buffer (u + 1) & 1; u = -1 is the
-    // initial state) to global memory, laid out as in shared memory: the slot
-    // of frame t0 + u, or in reverse slot T - 2 - u (the frame index of the
-    // gradient U it holds)
-    auto store_block = [&](int u) {
-      const long long f = bh * T + (a.reverse ? T - 2 - u : t0 + u);
-      if (in_region(((size_t)f * ncb + cb + 1) * NA * (32 * 128), a.s_span, a.status))
-        bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(img + ((u + 1) & 1) * kScanImg),
-                 NA * 32 * 128);
-      bulk_commit();
-    };
-    // thread 0: step j's MMA, P = M_t S_{j-1}[:, J], reading image buffer j & 1
-    auto issue = [&](int j) -> bool {
-      if (!wait_or_abort(smem_u32(&full[mstage]), mphase, abort_flag, a.status)) return false;
-      tc_fence_after();
-      const uint64_t ao = (uint64_t)((mstage * kScanMStage) >> 4);
-      const uint64_t bo = (uint64_t)(((j & 1) * kScanImg) >> 4);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int j = 0; j < nsteps; ++j) {
+        if (!wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status)) goto done;
+        if (!wait_or_abort(smem_u32(sready), j & 1, abort_flag, a.status)) goto done;
+        tc_fence_after();
+        const uint64_t ao = (uint64_t)((stage * kScanMStage) >> 4);
+        const uint64_t bo = (uint64_t)(((j & 1) * kScanImg) >> 4);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk)
-        if (kk < KS) mma_bf16(tmem, ad0[kk] + ao, bd0[kk] + bo, id, kk > 0 ? 1u : 0u);
-      if (store && (j >= 1 || a.reverse)) store_block(j - 1);
-      // The store of S_{j-2} has read its buffer, which S_j may now overwrite.
-      asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-      mma_commit(smem_u32(pfull));
-      mma_commit(smem_u32(&empty[mstage]));
-      if (++mstage == STAGES) { mstage = 0; mphase ^= 1; }
-      return true;
-    };
+        for (int kk = 0; kk < 8; ++kk)
+          if (kk < KS) mma_bf16(tmem, ad0[kk] + ao, bd0[kk] + bo, id, kk > 0 ? 1u : 0u);
+        if (store && (j >= 1 || a.reverse)) store_block(j - 1);
+        // The store of S_{j-2} has read its buffer, which S_j may now overwrite.
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+        mma_commit(smem_u32(pfull));
+        mma_commit(smem_u32(&empty[stage]));
+        if (++stage == STAGES) { stage = 0; phase ^= 1; }
+      }
+      if (store && nsteps > 0 && !a.reverse) {  // the reverse scan's last result is dS_0 (state_out only)
+        if (!wait_or_abort(smem_u32(sready), nsteps & 1, abort_flag, a.status)) goto done;
+        store_block(nsteps - 1);
+      }
+    }
+  } else {
+    // ---------------- epilogue (4 warps): thread i owns row i of the column block
+    const int i = threadIdx.x;
+    const bool row = i < D;
     float x[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) x[j] = (ident && i == 16 * cb + j) ? 1.f : 0.f;
@@ -687,61 +723,58 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
     };
     write_img(img);  // the initial state into buffer 0
     fence_proxy_async_smem();
-    named_barrier(1, 128);
-    if (i == 0 && nsteps > 0) fail = !issue(0);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(sready));
+    int stage = 0;
+    uint32_t phase = 0;
     const bool relu_lin = a.variant == kReluLinear;  // g = 1, no delta-rule term
     // raw decay of the next step's frame; mapped when used
     float gnext = (nsteps > 0 && !relu_lin) ? __ldg(a.g + bh * T + (a.reverse ? T - 1 : t0)) : 0.f;
-    int stage = 0;
-    uint32_t phase = 0;
     for (int j = 0; j < nsteps; ++j) {  // j counts steps; the step's frame is fr
       const int fr = a.reverse ? T - 1 - j : t0 + j;
       const long long f = bh * T + fr;
       const float gt = relu_lin ? 1.f : decay_of(gnext, a.gate_logits);
       if (j + 1 < nsteps && !relu_lin) gnext = __ldg(a.g + (a.reverse ? f - 1 : f + 1));
       const bool add_b = use_b && !(a.reverse && fr == 0);  // E_{-1} = 0
-      const bool ok = !fail && wait_or_abort(smem_u32(pfull), j & 1, abort_flag, a.status) &&
+      const bool ok = wait_or_abort(smem_u32(pfull), j & 1, abort_flag, a.status) &&
                       wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
-      if (!__all_sync(0xffffffffu, ok)) goto done;
-      tc_fence_after();
-      float p[16], pl[16];
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), p);
-      tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16, pl);
-      float bv[16];
+      if (__all_sync(0xffffffffu, ok)) {
+        tc_fence_after();
+        float p[16], pl[16];
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), p);
+        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16, pl);
+        float bv[16];
 #pragma unroll
-      for (int q = 0; q < 16; ++q) bv[q] = 0.f;
-      if (row && use_b) {
-        const float4* bp = reinterpret_cast<const float4*>(bring + stage * kScanBStage + i * 64);
+        for (int q = 0; q < 16; ++q) bv[q] = 0.f;
+        if (row && use_b) {
+          const float4* bp = reinterpret_cast<const float4*>(bring + stage * kScanBStage + i * 64);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 w = bp[q];
-          bv[4 * q] = w.x;
-          bv[4 * q + 1] = w.y;
-          bv[4 * q + 2] = w.z;
-          bv[4 * q + 3] = w.w;
+          for (int q = 0; q < 4; ++q) {
+            const float4 w = bp[q];
+            bv[4 * q] = w.x;
+            bv[4 * q + 1] = w.y;
+            bv[4 * q + 2] = w.z;
+            bv[4 * q + 3] = w.w;
+          }
         }
-      }
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
-      if (row) {
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+        if (row) {
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj)
-          x[jj] = relu_lin ? x[jj] + bv[jj] : fmaf(gt, x[jj] - (p[jj] + pl[jj]), add_b ? bv[jj] : 0.f);
+          for (int jj = 0; jj < 16; ++jj)
+            x[jj] = relu_lin ? x[jj] + bv[jj] : fmaf(gt, x[jj] - (p[jj] + pl[jj]), add_b ? bv[jj] : 0.f);
+        }
+        // S_j goes into the buffer of S_{j-2}, whose store has read it (the MMA
+        // thread waited for that before committing pfull(j)).
+        write_img(img + ((j + 1) & 1) * kScanImg);
+        fence_proxy_async_smem();
       }
-      // S_j goes into the buffer of S_{j-2}, whose store has read it (thread 0
-      // waited for that before committing pfull(j)).
-      write_img(img + ((j + 1) & 1) * kScanImg);
-      fence_proxy_async_smem();
       if (++stage == STAGES) { stage = 0; phase ^= 1; }
-      named_barrier(1, 128);  // S_j's image is complete; every TMEM read of step j is done
-      if (i == 0) {
-        if (j + 1 < nsteps)
-          fail = !issue(j + 1);
-        else if (store && !a.reverse)  // the reverse scan's last result is dS_0 (state_out only)
-          store_block(nsteps - 1);
-      }
+      if (!__all_sync(0xffffffffu, ok)) goto done;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(sready));
     }
     if (row && a.maps) {
       const size_t mo_end = ((size_t)(bh * a.nchunks + chunk_id) * D + i) * 2 * D + (ident ? 0 : D) + 16 * cb + 16;
@@ -757,8 +790,8 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
     }
   }
 done:
-  if (threadIdx.x == 0) {  // the thread that issued the MMAs and the image stores
-    bulk_wait0();          // state block stores complete
+  if (warp == 5 && lane == 0) {
+    bulk_wait0();  // state block stores complete
     mma_commit(smem_u32(mma_done));
     wait_bounded(smem_u32(mma_done), 0, 500000000ull);
   }
@@ -767,6 +800,256 @@ done:
   if (warp == 5) {
     tc_fence_after();
     tmem_dealloc(tmem, 32);
+  }
+}
+
+// =============================================================================
+// head scan: the frame loop of one whole head per CTA (every column block), for
+// the pipelined form, where it runs on a few SMs beside the gram and the
+// read-out of other frame chunks.  The arithmetic is the column-split scan's:
+// per frame P = M_t [S_{t-1} image] on the tensor core, now as one MMA chain
+// with N = 2D (the hi and lo rows of every 16-column block side by side, block
+// cb at rows 32 cb .. 32 cb + 31), then S <- g (S - P) + b_t in fp32 registers
+// (thread = state row, four warps per TMEM lane quadrant, two blocks each at
+// most), and the new image to the read-out's per-(frame-head, column-block)
+// blocks.  The state enters from and leaves to float32 [D][D] buffers, so a
+// sequence runs as consecutive launches over its frame chunks.  D <= 112.
+// =============================================================================
+constexpr int kHScanThreads = 544;  // 16 epilogue warps (thread 0 also issues MMAs and stores), 1 copy warp
+constexpr int kHScanStages = 2;
+constexpr int kHScanMaxD = 112;  // the whole-head b_t ring and image must fit beside the M ring
+
+struct HScanArgs {
+  const uint8_t* m_img;
+  const float* b_blk;
+  const float* g;
+  int gate_logits;
+  int variant;
+  const float* state_src;  // [BH][D][D]: the state entering the chunk (null: zeros)
+  float* state_dst;        // [BH][D][D]: the state leaving it (may alias state_src)
+  uint8_t* s_img;
+  int T, D, NA, t0, nsteps;
+  unsigned int* status;
+  size_t m_span, b_span, s_span;  // region extents (debug checks)
+};
+
+__global__ void __launch_bounds__(kHScanThreads, 1) tc_hscan_kernel(HScanArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  const int NA = a.NA, D = a.D, T = a.T, KS = D / 16, ncb = D / 16;
+  const int img_atom = 2 * D * 128;  // one atom of the whole-head image: 2D rows x 128 B (1024-aligned)
+  const int bstage = D * D * 4;      // b_t of one frame-head, [cb][i][16] float32
+  uint8_t* mring = smem;
+  uint8_t* bring = mring + kHScanStages * kScanMStage;
+  uint8_t* img = bring + ((kHScanStages * bstage + 1023) & ~1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(img + NA * img_atom);
+  uint64_t* full = bars;
+  uint64_t* empty = full + kHScanStages;
+  uint64_t* pfull = empty + kHScanStages;
+  uint64_t* mma_done = pfull + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const long long bh = blockIdx.x;
+  const int nsteps = a.nsteps, t0 = a.t0;
+  if (threadIdx.x == 0) {
+    for (int st = 0; st < kHScanStages; ++st) {
+      mbar_init(smem_u32(&full[st]), 1);
+      mbar_init(smem_u32(&empty[st]), 17);  // the MMA's commit + the 16 epilogue warps (b read)
+    }
+    mbar_init(smem_u32(pfull), 1);
+    mbar_init(smem_u32(mma_done), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  {  // M image rows D..127 of each atom (never copied in) must be finite
+    const int tail = (128 - D) * 8;
+    for (int idx = threadIdx.x; idx < kHScanStages * 2 * tail; idx += blockDim.x) {
+      const int region = idx / tail, c = idx % tail;
+      reinterpret_cast<uint4*>(mring + region * (128 * 128) + D * 128)[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
+  fence_proxy_async_smem();
+  if (warp == 0) {
+    tmem_alloc(smem_u32(tmem_slot), 256);  // P: hi and lo of every column block, 2D columns
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 16) {
+    // ---------------- copies in: the M_t image and the whole b_t
+    if (lane == 0) {
+      Ring<kHScanStages> r;
+      for (int j = 0; j < nsteps; ++j) {
+        if (!wait_or_abort(smem_u32(&empty[r.stage]), r.phase ^ 1, abort_flag, a.status)) break;
+        const long long f = bh * T + t0 + j;
+        const uint32_t fb = smem_u32(&full[r.stage]);
+        mbar_arrive_expect_tx(fb, NA * D * 128 + bstage);
+        const uint8_t* src = a.m_img + (size_t)f * NA * D * 128;
+        if (in_region(((size_t)f + 1) * NA * D * 128, a.m_span, a.status))
+          for (int at = 0; at < NA; ++at)
+            bulk_g2s(smem_u32(mring + r.stage * kScanMStage + at * 128 * 128), src + at * D * 128, D * 128, fb);
+        if (in_region(((size_t)f + 1) * bstage, a.b_span, a.status))
+          bulk_g2s(smem_u32(bring + r.stage * bstage), a.b_blk + (size_t)f * D * D, bstage, fb);
+        r.mark_issued();
+        r.advance();
+      }
+      r.drain(full);
+    }
+  } else if (warp < 16) {
+    const int q = warp & 3, cg = warp >> 2;
+    const int i = q * 32 + lane;
+    const bool row = i < D;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    const int nb = (cg < ncb ? 1 : 0) + (cg + 4 < ncb ? 1 : 0);  // column blocks cg and cg + 4
+    bool fail = false;
+    int mstage = 0;
+    uint32_t mphase = 0;
+    const uint32_t id = idesc_bf16(128, 2 * D, 0, 0);
+    // the image of S_u (u = frame index in the chunk) to the read-out's blocks
+    auto store_img = [&](int u) {
+      const long long f = bh * T + t0 + u;
+      if (in_region(((size_t)f + 1) * ncb * NA * (32 * 128), a.s_span, a.status))
+        for (int cb = 0; cb < ncb; ++cb)
+          for (int at = 0; at < NA; ++at)
+            bulk_s2g(a.s_img + (((size_t)f * ncb + cb) * NA + at) * (32 * 128),
+                     smem_u32(img + at * img_atom + cb * 32 * 128), 32 * 128);
+      bulk_commit();
+    };
+    // thread 0: step j's MMA chain, P = M_t S_{j-1}, then the store of S_{j-1}'s image
+    auto issue = [&](int j) -> bool {
+      if (!wait_or_abort(smem_u32(&full[mstage]), mphase, abort_flag, a.status)) return false;
+      tc_fence_after();
+      const uint32_t mb = smem_u32(mring + mstage * kScanMStage), ib = smem_u32(img);
+      for (int kk = 0; kk < KS; ++kk)
+        mma_bf16(tmem, smem_desc(mb + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024),
+                 smem_desc(ib + (kk >> 2) * img_atom + (kk & 3) * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
+      if (j >= 1) store_img(j - 1);
+      // the stores have read the image, which S_j may then overwrite
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      mma_commit(smem_u32(pfull));
+      mma_commit(smem_u32(&empty[mstage]));
+      if (++mstage == kHScanStages) { mstage = 0; mphase ^= 1; }
+      return true;
+    };
+    float x[2][16];
+    const float* src = a.state_src ? a.state_src + (size_t)bh * D * D : nullptr;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int cb = cg + 4 * u;
+#pragma unroll
+      for (int jj = 0; jj < 16; ++jj) x[u][jj] = 0.f;
+      if (u < nb && row && src) {
+        const float4* si = reinterpret_cast<const float4*>(src + (size_t)i * D + 16 * cb);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 w = si[e];
+          x[u][4 * e] = w.x;
+          x[u][4 * e + 1] = w.y;
+          x[u][4 * e + 2] = w.z;
+          x[u][4 * e + 3] = w.w;
+        }
+      }
+    }
+    auto write_img = [&]() {
+      if (!row) return;
+      uint8_t* at = img + (i >> 6) * img_atom;
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (u >= nb) break;
+        const int r0 = 32 * (cg + 4 * u);
+#pragma unroll
+        for (int n = 0; n < 16; n += 2) {
+          uint32_t hv, lv;
+          split2(x[u][n], x[u][n + 1], hv, lv);
+          *reinterpret_cast<uint16_t*>(at + sw128_off(r0 + n, i & 63)) = (uint16_t)(hv & 0xFFFF);
+          *reinterpret_cast<uint16_t*>(at + sw128_off(r0 + n + 1, i & 63)) = (uint16_t)(hv >> 16);
+          *reinterpret_cast<uint16_t*>(at + sw128_off(r0 + 16 + n, i & 63)) = (uint16_t)(lv & 0xFFFF);
+          *reinterpret_cast<uint16_t*>(at + sw128_off(r0 + 17 + n, i & 63)) = (uint16_t)(lv >> 16);
+        }
+      }
+    };
+    write_img();
+    fence_proxy_async_smem();
+    named_barrier(1, 512);
+    if (threadIdx.x == 0 && nsteps > 0) fail = !issue(0);
+    const bool relu_lin = a.variant == kReluLinear;
+    float gnext = (nsteps > 0 && !relu_lin) ? __ldg(a.g + bh * T + t0) : 0.f;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int j = 0; j < nsteps; ++j) {
+      const long long f = bh * T + t0 + j;
+      const float gt = relu_lin ? 1.f : decay_of(gnext, a.gate_logits);
+      if (j + 1 < nsteps && !relu_lin) gnext = __ldg(a.g + f + 1);
+      const bool ok = !fail && wait_or_abort(smem_u32(pfull), j & 1, abort_flag, a.status) &&
+                      wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, ok)) goto done;
+      tc_fence_after();
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (u >= nb) break;
+        const int cb = cg + 4 * u;
+        float p[16], pl[16];
+        tmem_ld16(tmem + lane_base + 32 * cb, p);
+        tmem_ld16(tmem + lane_base + 32 * cb + 16, pl);
+        float bv[16];
+        if (row) {
+          const float4* bp = reinterpret_cast<const float4*>(bring + stage * bstage + ((size_t)cb * D + i) * 64);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float4 w = bp[e];
+            bv[4 * e] = w.x;
+            bv[4 * e + 1] = w.y;
+            bv[4 * e + 2] = w.z;
+            bv[4 * e + 3] = w.w;
+          }
+        }
+        tmem_ld_wait();
+        if (row) {
+#pragma unroll
+          for (int jj = 0; jj < 16; ++jj)
+            x[u][jj] = relu_lin ? x[u][jj] + bv[jj] : fmaf(gt, x[u][jj] - (p[jj] + pl[jj]), bv[jj]);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
+      write_img();  // S_j over S_{j-1}: MMA j and the store of S_{j-1} have read it (pfull(j))
+      fence_proxy_async_smem();
+      if (++stage == kHScanStages) { stage = 0; phase ^= 1; }
+      named_barrier(1, 512);  // S_j's image is complete; every TMEM read of step j is done
+      if (threadIdx.x == 0) {
+        if (j + 1 < nsteps)
+          fail = !issue(j + 1);
+        else
+          store_img(j);
+      }
+    }
+    if (a.state_dst && row) {
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (u >= nb) break;
+        float4* so = reinterpret_cast<float4*>(a.state_dst + ((size_t)bh * D + i) * D + 16 * (cg + 4 * u));
+#pragma unroll
+        for (int e = 0; e < 4; ++e) so[e] = make_float4(x[u][4 * e], x[u][4 * e + 1], x[u][4 * e + 2], x[u][4 * e + 3]);
+      }
+    }
+  }
+done:
+  if (threadIdx.x == 0) {  // the thread that issued the MMAs and the image stores
+    bulk_wait0();
+    mma_commit(smem_u32(mma_done));
+    wait_bounded(smem_u32(mma_done), 0, 500000000ull);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
   }
 }
 
@@ -793,6 +1076,7 @@ struct OutArgs {
   // same image read as an MN-major B operand.
   int transpose_s;
   size_t s_span;  // extent (bytes) of the state image region (debug checks)
+  ItemMap map;    // items -> frame-heads (zero: item i is frame-head i)
 };
 
 __global__ void __launch_bounds__(kOutThreads, 1)
@@ -855,7 +1139,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       Ring<2> ra;
       Ring<kOutQStages> rq;
       bool ok = true;
-      for (long long f = blockIdx.x; ok && f < a.nitems; f += gridDim.x) {
+      for (long long it = blockIdx.x; ok && it < a.nitems; it += gridDim.x) {
+        const long long f = a.map.f(it);
         if (!wait_or_abort(smem_u32(&aempty[ra.stage]), ra.phase ^ 1, abort_flag, a.status)) break;
         const uint32_t afb = smem_u32(&afull[ra.stage]);
         mbar_arrive_expect_tx(afb, img_bytes);
@@ -892,7 +1177,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       const uint32_t id = idesc_bf16(128, D, 0, a.transpose_s ? 1 : 0);
       int ab = 0, qs = 0, cb = 0;
       uint32_t aph = 0, qph = 0, cph = 0;
-      for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+      for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
         if (!wait_or_abort(smem_u32(&afull[ab]), aph, abort_flag, a.status)) goto done;
         const uint32_t im = smem_u32(imgs + ab * img_stride);
         for (int tile = 0; tile < ntiles; ++tile) {
@@ -927,7 +1212,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       int qs = 0;
       uint32_t qph = 0;
       const __nv_bfloat162 zero = __floats2bfloat162_rn(0.f, 0.f);
-      for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+      for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
         for (int tile = 0; tile < ntiles; ++tile) {
           if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&qfull[qs]), qph, abort_flag, a.status))) goto done;
           uint4* qt = reinterpret_cast<uint4*>(qst + qs * q_bytes);
@@ -950,7 +1235,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     const int row = warp * 32 + lane;
     int cb = 0;
     uint32_t cph = 0;
-    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
+    for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
+      const long long f = a.map.f(it);
       for (int tile = 0; tile < ntiles; ++tile) {
         if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[cb]), cph, abort_flag, a.status))) goto done;
         tc_fence_after();
@@ -1488,23 +1774,137 @@ size_t tc_workspace_bytes(const Problem& p, int mode) { return tc_layout(p, mode
 
 namespace {
 
-// The gram over every frame-head of the call: the M_t images and b_t blocks
-// (regions of m_span and b_span bytes).
-int launch_gram(const Problem& p, uint8_t* m_img, float* b_mat, size_t m_span, size_t b_span, cudaStream_t st) {
+// The gram over the call's frame-heads (`map`: all of them, or one frame chunk of
+// every head, `nitems` items on at most `max_ctas` persistent CTAs): the M_t
+// images and b_t blocks (regions of m_span and b_span bytes).
+int launch_gram(const Problem& p, const CUtensorMap& mapK, const CUtensorMap& mapV, uint8_t* m_img, float* b_mat,
+                size_t m_span, size_t b_span, cudaStream_t st, ItemMap map, long long nitems, int max_ctas) {
   const int NA = num_atoms(p.D);
-  const long long F = p.BHT();
-  CUtensorMap mapK, mapV;
-  if (!make_map(&mapK, p.k, p.D, p.S, F, kGramTok) || !make_map(&mapV, p.v, p.D, p.S, F, kGramTok)) return kCuda;
   const int smem = gram_smem(NA, p.D);
   if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return kCuda;
-  GramArgs ga{p.beta, p.gate_logits, p.variant, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale,
-              p.key_scale, p.status, 0, m_span, b_span};
-  const int nsm = num_sms();
-  const unsigned grid = (unsigned)(F < nsm ? F : nsm);
+  GramArgs ga{p.beta, p.gate_logits, p.variant, m_img, b_mat, nitems, p.S, p.D, NA, p.key_scale * p.key_scale,
+              p.key_scale, p.status, 0, m_span, b_span, map};
+  const unsigned grid = (unsigned)(nitems < max_ctas ? nitems : max_ctas);
   ProfScope ps(st, "tc_gram");
   tc_gram_kernel<<<grid, kGramThreads, smem, st>>>(mapK, mapV, ga);
   return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
+
+int launch_gram(const Problem& p, uint8_t* m_img, float* b_mat, size_t m_span, size_t b_span, cudaStream_t st) {
+  const long long F = p.BHT();
+  CUtensorMap mapK, mapV;
+  if (!make_map(&mapK, p.k, p.D, p.S, F, kGramTok) || !make_map(&mapV, p.v, p.D, p.S, F, kGramTok)) return kCuda;
+  return launch_gram(p, mapK, mapV, m_img, b_mat, m_span, b_span, st, ItemMap{0, 0, 0}, F, num_sms());
+}
+
+// The read-out over the call's frame-heads (`map`, `nitems`, `max_ctas` as launch_gram).
+int launch_readout(const Problem& p, const CUtensorMap& mapQ, const CUtensorMap& mapO, const uint8_t* s_img,
+                   size_t s_span, cudaStream_t st, ItemMap map, long long nitems, int max_ctas) {
+  const int NA = num_atoms(p.D);
+  const int smem = out_smem(NA, p.D);
+  if (cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return kCuda;
+  const size_t shrink = debug_shrink();
+  OutArgs oa{s_img, p.variant, static_cast<__nv_bfloat16*>(p.out), nitems, p.S, p.D, NA, p.out_scale, p.status, 0,
+             s_span > shrink ? s_span - shrink : 1, map};
+  const unsigned grid = (unsigned)(nitems < max_ctas ? nitems : max_ctas);
+  ProfScope ps(st, "tc_readout");
+  tc_readout_kernel<<<grid, kOutThreads, smem, st>>>(mapQ, mapO, oa);
+  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+}
+
+// ---- pipelined form --------------------------------------------------------------
+// Frames in chunks of kPipeFrames.  The gram and read-out of each chunk (every
+// head) run on the caller's stream over num_sms - BH SMs, the head scan of chunk c
+// (one CTA per head) on a second stream, after the gram of c (an event) and before
+// the read-out of c (an event back): the scan of one chunk overlaps the gram of the
+// next and the read-out of the one before.  No kernel waits on another.
+constexpr int kPipeFrames = 32;
+
+bool pipeline_fits(const Problem& p) {
+  return p.dtype == GDN_BF16 && p.D <= kHScanMaxD && p.BH() * 4 <= num_sms() && p.T > kPipeFrames;
+}
+
+int hscan_smem(int NA, int D) {
+  return kHScanStages * kScanMStage + ((kHScanStages * D * D * 4 + 1023) & ~1023) + NA * 2 * D * 128 + kBarBytes +
+         1024;
+}
+
+// The second stream and the events of the pipelined form, per device (created on
+// first use, kept for the process).  Their users hold `mu` while they enqueue, so
+// each record is waited on before it is recorded again.
+struct PipeRes {
+  std::mutex mu;
+  cudaStream_t aux = nullptr;
+  cudaEvent_t start = nullptr, gram = nullptr, scan = nullptr;
+};
+
+PipeRes* pipe_res() {
+  static PipeRes res[64];
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  PipeRes& r = res[dev];
+  if (!r.aux) {
+    if (cudaStreamCreateWithFlags(&r.aux, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
+    if (cudaEventCreateWithFlags(&r.start, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&r.gram, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&r.scan, cudaEventDisableTiming) != cudaSuccess)
+      return nullptr;
+  }
+  return &r;
+}
+
+int pipelined_forward(const Problem& p, const TcLayout& L, uint8_t* w, const CUtensorMap& mapQ,
+                      const CUtensorMap& mapO, cudaStream_t st) {
+  const long long F = p.BHT(), BH = p.BH();
+  CUtensorMap mapK, mapV;
+  if (!make_map(&mapK, p.k, p.D, p.S, F, kGramTok) || !make_map(&mapV, p.v, p.D, p.S, F, kGramTok)) return kCuda;
+  PipeRes* pr = pipe_res();
+  if (!pr) return kCuda;
+  std::lock_guard<std::mutex> lock(pr->mu);
+  const int NA = num_atoms(p.D);
+  uint8_t* m_img = w + L.m_off;
+  float* b_mat = reinterpret_cast<float*>(w + L.b_off);
+  uint8_t* s_img = w + L.s_off;
+  float* carry = reinterpret_cast<float*>(w + L.carry_off);
+  const size_t m_span = L.b_off - L.m_off, b_span = L.s_off - L.b_off, s_span = L.carry_off - L.s_off;
+  const int ctas = num_sms() - (int)BH;
+  const int smem = hscan_smem(NA, p.D);
+  if (cudaFuncSetAttribute(tc_hscan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return kCuda;
+  const int nch = (p.T + kPipeFrames - 1) / kPipeFrames;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  // the second stream starts after the caller's work so far
+  if (!ok(cudaEventRecord(pr->start, st)) || !ok(cudaStreamWaitEvent(pr->aux, pr->start, 0))) return kCuda;
+  for (int c = 0; c <= nch; ++c) {
+    if (c < nch) {
+      const int t0 = c * kPipeFrames, n = p.T - t0 < kPipeFrames ? p.T - t0 : kPipeFrames;
+      int rc = launch_gram(p, mapK, mapV, m_img, b_mat, m_span, b_span, st, ItemMap{p.T, t0, n}, BH * n, ctas);
+      if (rc != kOk) return rc;
+      if (!ok(cudaEventRecord(pr->gram, st)) || !ok(cudaStreamWaitEvent(pr->aux, pr->gram, 0))) return kCuda;
+    }
+    if (c >= 1) {  // the read-out of the chunk before, once its scan is done
+      const int t0 = (c - 1) * kPipeFrames, n = p.T - t0 < kPipeFrames ? p.T - t0 : kPipeFrames;
+      if (!ok(cudaStreamWaitEvent(st, pr->scan, 0))) return kCuda;
+      const int rc = launch_readout(p, mapQ, mapO, s_img, s_span, st, ItemMap{p.T, t0, n}, BH * n, ctas);
+      if (rc != kOk) return rc;
+    }
+    if (c < nch) {
+      const int t0 = c * kPipeFrames, n = p.T - t0 < kPipeFrames ? p.T - t0 : kPipeFrames;
+      HScanArgs ha{m_img, b_mat, p.g, p.gate_logits, p.variant, c == 0 ? p.state_in : carry,
+                   c == nch - 1 ? p.state_out : carry, s_img, p.T, p.D, NA, t0, n, p.status, m_span, b_span, s_span};
+      {
+        ProfScope ps(pr->aux, "tc_hscan");
+        tc_hscan_kernel<<<(unsigned)BH, kHScanThreads, smem, pr->aux>>>(ha);
+      }
+      if (cudaGetLastError() != cudaSuccess) return kCuda;
+      if (!ok(cudaEventRecord(pr->scan, pr->aux))) return kCuda;
+    }
+  }
+  return kOk;
 }
 
 // The chunked scan's summary form: [A_c | b_c] of every (head, chunk) into `maps`.
@@ -1550,9 +1950,11 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
 
   CUtensorMap mapQ, mapO;
   if (!make_map(&mapQ, p.q, p.D, p.S, F, kOutTok) || !make_map(&mapO, p.out, p.D, p.S, F, 32)) return kCuda;
+  if (p.mode == GDN_MODE_PIPELINED && pipeline_fits(p)) return pipelined_forward(p, L, w, mapQ, mapO, st);
 
   const size_t m_span = L.b_off - L.m_off, b_span = L.s_off - L.b_off;
-  const size_t s_span = (p.mode == GDN_MODE_PREFIX ? L.maps_off : L.total) - L.s_off;
+  const size_t s_span =
+      (p.mode == GDN_MODE_PREFIX ? L.maps_off : (p.mode == GDN_MODE_PIPELINED ? L.carry_off : L.total)) - L.s_off;
   int rc = launch_gram(p, m_img, b_mat, m_span, b_span, st);
   if (rc != kOk) return rc;
   if (p.mode == GDN_MODE_PREFIX) {
@@ -1587,19 +1989,7 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
     rc = launch_scan<4>(sa, p.BH() * (p.D / 16), st, "tc_scan");
     if (rc != kOk) return rc;
   }
-  {
-    const int smem = out_smem(NA, p.D);
-    if (cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-      return kCuda;
-    const size_t shrink = debug_shrink();
-    OutArgs oa{s_img, p.variant, static_cast<__nv_bfloat16*>(p.out), F, p.S, p.D, NA, p.out_scale, p.status, 0,
-               s_span > shrink ? s_span - shrink : 1};
-    const unsigned grid = (unsigned)(F < nsm ? F : nsm);
-    ProfScope ps(st, "tc_readout");
-    tc_readout_kernel<<<grid, kOutThreads, smem, st>>>(mapQ, mapO, oa);
-  }
-  if (cudaGetLastError() != cudaSuccess) return kCuda;
-  return kOk;
+  return launch_readout(p, mapQ, mapO, s_img, s_span, st, ItemMap{0, 0, 0}, F, nsm);
 }
 
 
