@@ -24,6 +24,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <utility>
 
 #include "../../include/gdn.h"
 #include "gdn_internal.h"
@@ -274,6 +275,10 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int nchunks = (S + kGramTok - 1) / kGramTok;
+  // (launched with programmatic stream serialization: everything above overlaps
+  // the preceding kernel; no global memory is touched before this wait)
+  griddep_wait();
+  griddep_launch_dependents();
 
   if (warp == 12) {
     // ---------------- TMA producer
@@ -307,6 +312,15 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     if (lane == 0) {
       const uint32_t id1 = idesc_bf16(128, NA * 64 + D, 1, 1);
       const uint32_t id2 = idesc_bf16(128, D, 1, 1);
+      // Descriptors of ring stage 0 and K-step 0; a stage or K-step only moves the
+      // start address (the low 14-bit field, in 16-byte units; every address here
+      // stays below 2^18, so the sum never carries into the next field).  Building
+      // each descriptor afresh per MMA cost the issuing warp ~100 cycles an MMA.
+      const uint64_t dK0 = smem_desc(smem_u32(raw), kGramRegion, 1024);
+      const uint64_t dV0 = smem_desc(smem_u32(raw + NA * kGramRegion), kGramRegion, 1024);
+      const uint64_t dH0 = smem_desc(smem_u32(conv), kGramRegion, 1024);
+      const uint64_t dL0 = smem_desc(smem_u32(conv + 2 * kGramRegion), kGramRegion, 1024);
+      const uint32_t accb = NA * 64;
       int rs = 0, cs = 0, ab = 0;
       uint32_t rph = 0, cph = 0, aph = 0;
       for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
@@ -316,20 +330,17 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         for (int c = 0; c < nchunks; ++c) {
           if (!wait_or_abort(smem_u32(&conv_full[cs]), cph, abort_flag, a.status)) goto done;
           tc_fence_after();
-          const uint32_t rb = smem_u32(raw + rs * kRawStage);
-          const uint32_t ah = smem_u32(conv + cs * kConvStage), al = ah + 2 * kGramRegion;
+          const uint64_t ro = (uint64_t)((rs * kRawStage) >> 4), co = (uint64_t)((cs * kConvStage) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kGramTok / 16; ++kk) {
-            const uint32_t off = kk * 2048;
+            const uint64_t ko = (uint64_t)((kk * 2048) >> 4);
+            const uint32_t accum = (c > 0 || kk > 0) ? 1u : 0u;
             if (a.b_only) {
-              mma_bf16(acc + NA * 64, smem_desc(ah + off, kGramRegion, 1024),
-                       smem_desc(rb + NA * kGramRegion + off, kGramRegion, 1024), id2, (c > 0 || kk > 0) ? 1u : 0u);
+              mma_bf16(acc + accb, dH0 + co + ko, dV0 + ro + ko, id2, accum);
               continue;
             }
-            mma_bf16(acc, smem_desc(ah + off, kGramRegion, 1024), smem_desc(rb + off, kGramRegion, 1024), id1,
-                     (c > 0 || kk > 0) ? 1u : 0u);
-            mma_bf16(acc + NA * 64, smem_desc(al + off, kGramRegion, 1024),
-                     smem_desc(rb + NA * kGramRegion + off, kGramRegion, 1024), id2, 1u);
+            mma_bf16(acc, dH0 + co + ko, dK0 + ro + ko, id1, accum);
+            mma_bf16(acc + accb, dL0 + co + ko, dV0 + ro + ko, id2, 1u);
           }
           mma_commit(smem_u32(&raw_empty[rs]));
           mma_commit(smem_u32(&conv_empty[cs]));
@@ -599,6 +610,8 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // no global memory is touched before the preceding kernel completes
+  griddep_launch_dependents();
 
   if (warp == 4) {
     // ---------------- copies in: M_t image (NA atoms of D rows) and the b_t block
@@ -879,6 +892,8 @@ __global__ void __launch_bounds__(kHScanThreads, 1) tc_hscan_kernel(HScanArgs a)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  griddep_wait();  // no global memory is touched before the preceding kernel completes
+  griddep_launch_dependents();
 
   if (warp == 16) {
     // ---------------- copies in: the M_t image and the whole b_t
@@ -1131,6 +1146,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ntiles = (S + kOutTok - 1) / kOutTok;
+  griddep_wait();  // no global memory is touched before the preceding kernel completes
+  griddep_launch_dependents();
 
   if (warp == 4) {
     // ---------------- producer: S image per frame-head, Q tiles per tile
@@ -1175,26 +1192,30 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     // ---------------- MMA: O_tile (128 tokens x D) = Q_tile S_hi + Q_tile S_lo
     if (lane == 0) {
       const uint32_t id = idesc_bf16(128, D, 0, a.transpose_s ? 1 : 0);
+      // Descriptors of buffer 0 / stage 0 / K-step 0; the rest only move the start
+      // address (the low 14-bit field in 16-byte units; no carry below 2^18).
+      // K-major image: rows = value columns, K-steps of 16 key dims inside an atom;
+      // MN-major (transposed): K-steps of 16 rows (value columns), LBO = atom stride.
+      const uint64_t dQ0 = smem_desc(smem_u32(qst), 16, 1024);
+      const uint64_t dI0 = smem_desc(smem_u32(imgs), a.transpose_s ? D * 128 : 16, 1024);
+      const uint64_t lo_off = (uint64_t)((NA * D * 128) >> 4);
       int ab = 0, qs = 0, cb = 0;
       uint32_t aph = 0, qph = 0, cph = 0;
       for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
         if (!wait_or_abort(smem_u32(&afull[ab]), aph, abort_flag, a.status)) goto done;
-        const uint32_t im = smem_u32(imgs + ab * img_stride);
+        const uint64_t io = (uint64_t)((ab * img_stride) >> 4);
         for (int tile = 0; tile < ntiles; ++tile) {
           if (!wait_or_abort(smem_u32(&accempty[cb]), cph ^ 1, abort_flag, a.status)) goto done;
           if (!wait_or_abort(smem_u32(relu_q ? &qready[qs] : &qfull[qs]), qph, abort_flag, a.status)) goto done;
           tc_fence_after();
-          const uint32_t qb = smem_u32(qst + qs * q_bytes);
+          const uint64_t qo = (uint64_t)((qs * q_bytes) >> 4);
           const uint32_t acc = tmem + cb * 128;
           for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t ko = (kk >> 2) * (kOutTok * 128) + (kk & 3) * 32;
-            const uint64_t ad = smem_desc(qb + ko, 16, 1024);
-            // K-major: rows = value columns, K-steps of 16 key dims inside an atom;
-            // MN-major (transposed): K-steps of 16 rows (value columns), LBO = atom stride
+            const uint64_t ad = dQ0 + qo + (uint64_t)(((kk >> 2) * (kOutTok * 128) + (kk & 3) * 32) >> 4);
             const uint32_t so = a.transpose_s ? kk * 2048 : (kk >> 2) * (D * 128) + (kk & 3) * 32;
-            const uint32_t lbo = a.transpose_s ? D * 128 : 16;
-            mma_bf16(acc, ad, smem_desc(im + so, lbo, 1024), id, kk > 0 ? 1u : 0u);
-            mma_bf16(acc, ad, smem_desc(im + NA * D * 128 + so, lbo, 1024), id, 1u);
+            const uint64_t bd = dI0 + io + (uint64_t)(so >> 4);
+            mma_bf16(acc, ad, bd, id, kk > 0 ? 1u : 0u);
+            mma_bf16(acc, ad, bd + lo_off, id, 1u);
           }
           mma_commit(smem_u32(&qempty[qs]));
           mma_commit(smem_u32(&accfull[cb]));
@@ -1517,8 +1538,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const uint32_t idK = idesc_bf16(128, D, 0, 0);  // A K-major (tile), B K-major (image, K = key dim)
       const uint32_t idT = idesc_bf16(128, D, 0, 1);  // A K-major (V tile), B MN-major (U image, K = value dim)
       const uint32_t idW = idesc_bf16(128, D, 1, 1);  // A and B MN-major (images, K = value dim)
-      const uint32_t sU = smem_u32(imgU), sW = smem_u32(imgW);
-      const uint32_t aV = smem_u32(tV);
+      // Descriptors at offset 0 of each region; offsets only move the start address
+      // (the low 14-bit field in 16-byte units; no carry below 2^18).
+      const uint64_t uK = smem_desc(smem_u32(imgU), 16, 1024), wK = smem_desc(smem_u32(imgW), 16, 1024);
+      const uint64_t uM = smem_desc(smem_u32(imgU), D * 128, 1024), wM = smem_desc(smem_u32(imgW), D * 128, 1024);
+      const uint64_t tK0 = smem_desc(smem_u32(tK), 16, 1024), tV0 = smem_desc(smem_u32(tV), 16, 1024);
+      const uint64_t lo16 = (uint64_t)(lo >> 4);
       int ks = 0;
       uint32_t kph = 0, vph = 0, xph = 0, iph = 0, wph = 0;
       for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
@@ -1528,9 +1553,9 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // W_t = S U^T + U S^T (K = value dim j; the images are [j][i], so both
         // operands are MN-major); the lo x lo terms are below fp32 rounding
         for (int kk = 0; kk < KS; ++kk) {
-          const uint32_t mo = kk * 2048;
-          const uint64_t sh = smem_desc(sW + mo, D * 128, 1024), sl = smem_desc(sW + lo + mo, D * 128, 1024);
-          const uint64_t uh = smem_desc(sU + mo, D * 128, 1024), ul = smem_desc(sU + lo + mo, D * 128, 1024);
+          const uint64_t mo = (uint64_t)((kk * 2048) >> 4);
+          const uint64_t sh = wM + mo, sl = wM + lo16 + mo;
+          const uint64_t uh = uM + mo, ul = uM + lo16 + mo;
           mma_bf16(tmem + kTW, sh, uh, idW, kk > 0 ? 1u : 0u);
           mma_bf16(tmem + kTW, sh, ul, idW, 1u);
           mma_bf16(tmem + kTW, sl, uh, idW, 1u);
@@ -1547,22 +1572,22 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           if (!wait_or_abort(smem_u32(vfull), vph, abort_flag, a.status)) goto done;
           if (!wait_or_abort(smem_u32(xempty), xph ^ 1, abort_flag, a.status)) goto done;
           tc_fence_after();
-          const uint32_t aK = smem_u32(tK + ks * tile_bytes);
+          const uint64_t kso = (uint64_t)((ks * tile_bytes) >> 4);
           for (int kk = 0; kk < KS; ++kk) {  // K-dim = key dim i
-            const uint32_t ko = (kk >> 2) * (kKvTok * 128) + (kk & 3) * 32;
-            const uint32_t so = (kk >> 2) * (D * 128) + (kk & 3) * 32;
-            const uint64_t ad = smem_desc(aK + ko, 16, 1024);
-            mma_bf16(tmem + kTX1, ad, smem_desc(sU + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
-            mma_bf16(tmem + kTX1, ad, smem_desc(sU + lo + so, 16, 1024), idK, 1u);
-            mma_bf16(tmem + kTX3, ad, smem_desc(sW + so, 16, 1024), idK, kk > 0 ? 1u : 0u);
-            mma_bf16(tmem + kTX3, ad, smem_desc(sW + lo + so, 16, 1024), idK, 1u);
+            const uint64_t ko = (uint64_t)((((kk >> 2) * (kKvTok * 128) + (kk & 3) * 32)) >> 4);
+            const uint64_t so = (uint64_t)((((kk >> 2) * (D * 128) + (kk & 3) * 32)) >> 4);
+            const uint64_t ad = tK0 + kso + ko;
+            mma_bf16(tmem + kTX1, ad, uK + so, idK, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + kTX1, ad, uK + lo16 + so, idK, 1u);
+            mma_bf16(tmem + kTX3, ad, wK + so, idK, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + kTX3, ad, wK + lo16 + so, idK, 1u);
           }
           for (int kk = 0; kk < KS; ++kk) {  // K-dim = value dim j
-            const uint32_t ko = (kk >> 2) * (kKvTok * 128) + (kk & 3) * 32;
-            const uint32_t mo = kk * 2048;
-            const uint64_t ad = smem_desc(aV + ko, 16, 1024);
-            mma_bf16(tmem + kTX2, ad, smem_desc(sU + mo, D * 128, 1024), idT, kk > 0 ? 1u : 0u);
-            mma_bf16(tmem + kTX2, ad, smem_desc(sU + lo + mo, D * 128, 1024), idT, 1u);
+            const uint64_t ko = (uint64_t)((((kk >> 2) * (kKvTok * 128) + (kk & 3) * 32)) >> 4);
+            const uint64_t mo = (uint64_t)((kk * 2048) >> 4);
+            const uint64_t ad = tV0 + ko;
+            mma_bf16(tmem + kTX2, ad, uM + mo, idT, kk > 0 ? 1u : 0u);
+            mma_bf16(tmem + kTX2, ad, uM + lo16 + mo, idT, 1u);
           }
           mma_commit(smem_u32(xfull));
           mma_commit(smem_u32(vempty));
@@ -1711,6 +1736,25 @@ done:
   }
 }
 
+// Launches `kernel` with programmatic stream serialization: it may begin (its
+// prologue: barriers, TMEM, descriptors) while the preceding kernel in the stream
+// finishes; each such kernel waits (griddep_wait) before its first global access.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, int smem, cudaStream_t st,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = (size_t)smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -1757,8 +1801,7 @@ int launch_scan(const ScanArgs& sa, long long ctas, cudaStream_t st, const char*
   if (cudaFuncSetAttribute(tc_scan_kernel<STAGES>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return kCuda;
   ProfScope ps(st, name);
-  tc_scan_kernel<STAGES><<<(unsigned)ctas, kScanThreads, smem, st>>>(sa);
-  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+  return launch_pdl(tc_scan_kernel<STAGES>, (unsigned)ctas, kScanThreads, smem, st, sa) == cudaSuccess ? kOk : kCuda;
 }
 int out_smem(int NA, int D) {
   return 2 * ((2 * NA * D * 128 + 1023) & ~1023) + (kOutQStages + 1) * NA * kOutTok * 128 + kBarBytes + 1024;
@@ -1787,8 +1830,7 @@ int launch_gram(const Problem& p, const CUtensorMap& mapK, const CUtensorMap& ma
               p.key_scale, p.status, 0, m_span, b_span, map};
   const unsigned grid = (unsigned)(nitems < max_ctas ? nitems : max_ctas);
   ProfScope ps(st, "tc_gram");
-  tc_gram_kernel<<<grid, kGramThreads, smem, st>>>(mapK, mapV, ga);
-  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+  return launch_pdl(tc_gram_kernel, grid, kGramThreads, smem, st, mapK, mapV, ga) == cudaSuccess ? kOk : kCuda;
 }
 
 int launch_gram(const Problem& p, uint8_t* m_img, float* b_mat, size_t m_span, size_t b_span, cudaStream_t st) {
@@ -1810,8 +1852,7 @@ int launch_readout(const Problem& p, const CUtensorMap& mapQ, const CUtensorMap&
              s_span > shrink ? s_span - shrink : 1, map};
   const unsigned grid = (unsigned)(nitems < max_ctas ? nitems : max_ctas);
   ProfScope ps(st, "tc_readout");
-  tc_readout_kernel<<<grid, kOutThreads, smem, st>>>(mapQ, mapO, oa);
-  return cudaGetLastError() == cudaSuccess ? kOk : kCuda;
+  return launch_pdl(tc_readout_kernel, grid, kOutThreads, smem, st, mapQ, mapO, oa) == cudaSuccess ? kOk : kCuda;
 }
 
 // ---- pipelined form --------------------------------------------------------------
@@ -1898,9 +1939,8 @@ int pipelined_forward(const Problem& p, const TcLayout& L, uint8_t* w, const CUt
                    c == nch - 1 ? p.state_out : carry, s_img, p.T, p.D, NA, t0, n, p.status, m_span, b_span, s_span};
       {
         ProfScope ps(pr->aux, "tc_hscan");
-        tc_hscan_kernel<<<(unsigned)BH, kHScanThreads, smem, pr->aux>>>(ha);
+        if (launch_pdl(tc_hscan_kernel, (unsigned)BH, kHScanThreads, smem, pr->aux, ha) != cudaSuccess) return kCuda;
       }
-      if (cudaGetLastError() != cudaSuccess) return kCuda;
       if (!ok(cudaEventRecord(pr->scan, pr->aux))) return kCuda;
     }
   }

@@ -118,6 +118,16 @@ __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.
 // Wait until all committed bulk groups have fully completed (writes visible).
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// ---- programmatic dependent launch -------------------------------------------------
+// In a kernel launched with programmatic stream serialization: wait until the
+// preceding kernel in the stream has completed and its memory is visible (a no-op
+// in a kernel launched without it), and let the next kernel in the stream begin
+// launching (its own wait still holds it before its first global access).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- tcgen05: tensor memory -----------------------------------------------------------
 // Allocation and deallocation are warp-collective.
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
