@@ -307,7 +307,7 @@ def config_of(wl, mode, gate_logits=False, relu_linear=False, backward=False, ro
     return {"workload": f"{wl.name}: B={wl.B} H={wl.H} T={wl.T} S={wl.S} D={wl.D} {wl.dtype} I/O, fp32 state, "
                         f"{calls}{gates}",
             "B": wl.B, "H": wl.H, "T": wl.T, "S": wl.S, "D": wl.D,
-            "mode": "backward" if backward else {0: "sequential", 1: "prefix", 2: "split", 3: "pipelined"}[mode],
+            "mode": "backward" if backward else {0: "sequential", 1: "prefix", 2: "split"}[mode],
             "l2": f"no flush: inputs larger than L2 "
                   f"({(alg_bytes_bwd(wl) if backward else alg_bytes(wl)) / 1e9:.1f} GB moved per step vs 126 MB L2)"}
 
@@ -569,7 +569,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="minute", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3])
+    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--frames", type=int, default=None,
                     help="run the workload's first N frames only (small cases for profiling)")
     ap.add_argument("--gate-logits", action="store_true",

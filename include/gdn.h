@@ -88,16 +88,7 @@ typedef enum {
    * (M_t = K~^T diag(beta) K~, b_t = K~^T diag(beta) V_t) for all frames in
    * parallel, the serial D x D recurrence, then the read-out for all frames in
    * parallel. */
-  GDN_MODE_SPLIT = 2,
-  /* The split form's kernels over frame chunks of 32 frames, pipelined: the gram
-   * and read-out of each chunk on the caller's stream over all SMs but B*H, the
-   * recurrence of a chunk (one CTA per head) on a second stream the library
-   * keeps per device, so the serial recurrence of one chunk overlaps the gram of
-   * the next and the read-out of the one before (events between the streams; no
-   * kernel waits on another).  bf16 I/O with D <= 112, 4 B H <= the SM count and
-   * T > 32; otherwise the split form runs.  Same results as the split form up to
-   * rounding, same workspace layout plus one state buffer. */
-  GDN_MODE_PIPELINED = 3
+  GDN_MODE_SPLIT = 2
   /* Any other value gives GDN_ERR_INVALID_ARG. */
 } gdn_mode_t;
 

@@ -18,7 +18,7 @@ DEBUG_LIB_PATH = os.path.join(PKG, "libgdn_debug.so")
 GDN_F32, GDN_BF16 = 0, 1
 GDN_BWD_STATES_IN_WORKSPACE, GDN_BWD_GATE_LOGITS = 1, 2
 GDN_SUMMARY_GATE_LOGITS = 1
-GDN_MODE_SEQUENTIAL, GDN_MODE_PREFIX, GDN_MODE_SPLIT, GDN_MODE_PIPELINED = 0, 1, 2, 3
+GDN_MODE_SEQUENTIAL, GDN_MODE_PREFIX, GDN_MODE_SPLIT = 0, 1, 2
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_MISALIGNED",
           4: "GDN_ERR_CUDA", 5: "GDN_ERR_TIMEOUT", 6: "GDN_ERR_WORKSPACE", 7: "GDN_ERR_BOUNDS"}
 
@@ -224,8 +224,8 @@ def frame_fwd(q, k, v, g, beta, state_in=None, out=None, state_out=None, mode=No
     q, k, v: [B,H,T,S,D] float32 or bfloat16, contiguous; g: [B,H,T] float32;
     beta: [B,H,T,S] float32; state_in: [B,H,D,D] float32 or None.  ``out`` and
     ``state_out`` are allocated if not given (state_out only if want_state).
-    mode=None calls gdn_frame_fwd (library-managed scratch); mode=0/1/2/3
-    (sequential, prefix, split, pipelined) calls gdn_frame_fwd_ex with ``workspace``
+    mode=None calls gdn_frame_fwd (library-managed scratch); mode=0/1/2
+    (sequential, prefix, split) calls gdn_frame_fwd_ex with ``workspace``
     (a uint8 CUDA tensor, allocated if None).
     gate_logits=True passes g and beta as raw logits to gdn_frame_fwd_from_logits
     (mode None then means the sequential form).

@@ -70,7 +70,7 @@ int validate(const void* q, const void* k, const void* v, const float* g, const 
              int mode, Problem* p, bool need_gates = true) {
   if (B < 1 || H < 1 || T < 0 || S < 1 || D < 1) return kInvalidArg;
   if (dtype != GDN_F32 && dtype != GDN_BF16) return kInvalidArg;
-  if (mode < GDN_MODE_SEQUENTIAL || mode > GDN_MODE_PIPELINED) return kInvalidArg;
+  if (mode < GDN_MODE_SEQUENTIAL || mode > GDN_MODE_SPLIT) return kInvalidArg;
   if (D % 16 != 0 || D > 128) return kUnsupported;
   // Counts must stay inside what the kernels index with 64-bit offsets and
   // 32-bit grid dimensions / tensor-map extents.

@@ -50,7 +50,6 @@ struct TcLayout {
   size_t m_off, b_off, s_off, total;
   size_t m_bytes, b_bytes, s_bytes;  // per frame-head
   size_t maps_off, starts_off;       // prefix form: chunk maps [A|b] and chunk starts
-  size_t carry_off;                  // pipelined form: the state carried between frame chunks
 };
 
 constexpr int kTcChunkFrames = 16;  // frames per chunk of the prefix form
@@ -72,10 +71,6 @@ TcLayout tc_layout(const Problem& p, int mode = GDN_MODE_SPLIT) {
     L.maps_off = L.total;
     L.starts_off = align_up(L.maps_off + (size_t)p.BH() * nch * 2 * mat, 1024);
     L.total = align_up(L.starts_off + (size_t)p.BH() * nch * mat, 1024);
-  }
-  if (mode == GDN_MODE_PIPELINED) {
-    L.carry_off = L.total;
-    L.total = align_up(L.carry_off + (size_t)p.BH() * p.D * p.D * 4, 1024);
   }
   return L;
 }
@@ -114,20 +109,21 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 // Bounded wait that also gives up when another role has aborted; a timeout is
-// recorded in the status word and raises the CTA's abort flag.
+// recorded in the status word and raises the CTA's abort flag.  After a first
+// check the thread waits suspended (try_wait with a suspend-time hint: the
+// hardware wakes it when the phase completes, or after the hint), so a waiting
+// warp does not take issue slots from the warps sharing its sub-partition.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                               unsigned int* status) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 63) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitTimeoutNs) {
-        report_device_error(status, kTimeout);
-        *abort_flag = 1;
-        return false;
-      }
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, kWaitSuspendNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer() - t0 > kWaitTimeoutNs) {
+      report_device_error(status, kTimeout);
+      *abort_flag = 1;
+      return false;
     }
   }
 }
@@ -161,15 +157,6 @@ struct Ring {
   __device__ void drain(const uint64_t* full) const {
     for (int s = 0; s < N; ++s)
       if (issued_mask & (1u << s)) wait_bounded(smem_u32(&full[s]), (last_phase_mask >> s) & 1u, 500000000ull);
-  }
-};
-
-// Work items of the persistent gram and read-out kernels: item i is frame-head i,
-// or (L > 0: one frame chunk of every head) frame t0 + i % L of head i / L.
-struct ItemMap {
-  int T, t0, L;
-  __host__ __device__ long long f(long long it) const {
-    return L ? (long long)((int)it / L) * T + t0 + (int)it % L : it;  // items < 2^31 (validated)
   }
 };
 
@@ -219,8 +206,9 @@ struct GramArgs {
   // and its MMA is skipped.
   int b_only;
   size_t m_span, b_span;  // extents (bytes) of the M image and b block regions (debug checks)
-  ItemMap map;            // items -> frame-heads (zero: item i is frame-head i)
 };
+
+constexpr int kGramTmaWarp = 12, kGramMmaWarp = 13;  // warps 0-3 epilogue, 4-11 converters
 
 __global__ void __launch_bounds__(kGramThreads, 1)
     tc_gram_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV, GramArgs a) {
@@ -259,14 +247,17 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (NA == 1)  // the A operands span 128 rows of M: key dims 64..127 are zero
+  // The A operands span 128 rows of M (key dims); with one atom (D <= 64) the
+  // second atom's rows are never converted: zero them once, so those accumulator
+  // rows, which nothing reads, stay finite.
+  if (NA == 1)
     for (int s = 0; s < kGramConv; ++s)
       for (int idx = threadIdx.x; idx < kGramRegion / 16; idx += blockDim.x) {
         reinterpret_cast<uint4*>(conv + s * kConvStage + kGramRegion)[idx] = make_uint4(0, 0, 0, 0);
         reinterpret_cast<uint4*>(conv + s * kConvStage + 3 * kGramRegion)[idx] = make_uint4(0, 0, 0, 0);
       }
   fence_proxy_async_smem();
-  if (warp == 13) {
+  if (warp == kGramMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 512);
     tmem_relinquish();
   }
@@ -280,15 +271,14 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   griddep_wait();
   griddep_launch_dependents();
 
-  if (warp == 12) {
+  if (warp == kGramTmaWarp) {
     // ---------------- TMA producer
     if (lane == 0) {
       prefetch_tmap(&mapK);
       prefetch_tmap(&mapV);
       Ring<kGramRaw> r;
       bool ok = true;
-      for (long long it = blockIdx.x; ok && it < a.nitems; it += gridDim.x) {
-        const long long f = a.map.f(it);
+      for (long long f = blockIdx.x; ok && f < a.nitems; f += gridDim.x) {
         for (int c = 0; c < nchunks; ++c) {
           if (!wait_or_abort(smem_u32(&raw_empty[r.stage]), r.phase ^ 1, abort_flag, a.status)) {
             ok = false;
@@ -307,7 +297,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
       }
       r.drain(raw_full);  // every issued load has landed before the CTA may exit
     }
-  } else if (warp == 13) {
+  } else if (warp == kGramMmaWarp) {
     // ---------------- MMA issuer
     if (lane == 0) {
       const uint32_t id1 = idesc_bf16(128, NA * 64 + D, 1, 1);
@@ -323,7 +313,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
       const uint32_t accb = NA * 64;
       int rs = 0, cs = 0, ab = 0;
       uint32_t rph = 0, cph = 0, aph = 0;
-      for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
+      for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
         if (!wait_or_abort(smem_u32(&accempty[ab]), aph ^ 1, abort_flag, a.status)) goto done;
         tc_fence_after();
         const uint32_t acc = tmem + ab * 256;
@@ -363,11 +353,11 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     // This thread's chunks lie in tile rows r0 and r0 + 32; their beta values are
     // loaded one tile ahead so the load latency stays off the critical path.
     const int r0 = ct >> 3;
-    auto beta_at = [&](long long it, int c, int rw) {
+    auto beta_at = [&](long long f, int c, int rw) {
       const int s = c * kGramTok + rw;
       // raw value, mapped when used: mapping here would wait for the load
-      if (!(it < a.nitems && s < S)) return -INFINITY;
-      return (a.variant == kReluLinear || a.b_only) ? 1.f : __ldg(a.beta + a.map.f(it) * S + s);
+      if (!(f < a.nitems && s < S)) return -INFINITY;
+      return (a.variant == kReluLinear || a.b_only) ? 1.f : __ldg(a.beta + f * S + s);
     };
     long long fn = blockIdx.x;
     int cn = 0;
@@ -378,7 +368,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     };
     float bn0 = beta_at(fn, 0, r0), bn1 = beta_at(fn, 0, r0 + 32);
     float b0 = mapped(bn0), b1 = mapped(bn1);
-    for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
+    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
       for (int c = 0; c < nchunks; ++c) {
         if (++cn == nchunks) { cn = 0; fn += gridDim.x; }
         bn0 = beta_at(fn, cn, r0);
@@ -389,7 +379,8 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         const uint8_t* kt = raw + rs * kRawStage;
         uint8_t* ah = conv + cs * kConvStage;
         // This thread's (at most four) 16-byte chunks: every load issued before any
-        // arithmetic, so the shared-memory latencies overlap.
+        // arithmetic, so the shared-memory latencies overlap.  (Chunks of key
+        // columns past D hold the tile's zero fill and convert to zeros.)
         uint4 kv[4];
 #pragma unroll
         for (int rr = 0; rr < 4; ++rr)
@@ -400,18 +391,13 @@ __global__ void __launch_bounds__(kGramThreads, 1)
           const float bs = (rr & 1) ? b1 : b0;
           const uint32_t w[4] = {kv[rr].x, kv[rr].y, kv[rr].z, kv[rr].w};
           uint32_t hi[4], lo[4];
-          if (relu_k) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+          for (int e = 0; e < 4; ++e) {
+            const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            if (relu_k)
               split2(bs * fmaxf(x.x, 0.f), bs * fmaxf(x.y, 0.f), hi[e], lo[e]);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 x = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[e]));
+            else
               split2(bs * x.x, bs * x.y, hi[e], lo[e]);
-            }
           }
           const int u = ct + 256 * rr;
           *reinterpret_cast<uint4*>(ah + u * 16) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
@@ -426,14 +412,13 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         b1 = mapped(bn1);
       }
     }
-  } else {
+  } else if (warp < 4) {
     // ---------------- epilogue: TMEM -> M image (bf16, staged) and b (fp32 column blocks)
     const int i = warp * 32 + lane;  // accumulator row = key index
     const int ncb = D / 16;
     int ab = 0;
     uint32_t aph = 0;
-    for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
-      const long long f = a.map.f(it);
+    for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
       if (threadIdx.x == 0) bulk_wait_read0();  // the previous M image store has read the stage
       const bool ok = __all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[ab]), aph, abort_flag, a.status));
       if (barrier_any(1, 128, !ok || *abort_flag)) goto done;
@@ -483,13 +468,13 @@ __global__ void __launch_bounds__(kGramThreads, 1)
   }
 done:
   if (threadIdx.x == 0) bulk_wait0();  // M image stores complete
-  if (warp == 13 && lane == 0) {  // every MMA this CTA issued has completed
+  if (warp == kGramMmaWarp && lane == 0) {  // every MMA this CTA issued has completed
     mma_commit(smem_u32(mma_done));
     wait_bounded(smem_u32(mma_done), 0, 500000000ull);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 13) {
+  if (warp == kGramMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -520,6 +505,7 @@ constexpr int kScanThreads = 192;         // 4 epilogue, 1 copy, 1 MMA warps
 constexpr int kScanMStage = 2 * 128 * 128;  // M image: 2 atoms x 128 rows x 128 B
 constexpr int kScanBStage = 128 * 64;       // b block: up to 128 rows x 16 floats
 constexpr int kScanImg = 2 * 32 * 128;      // state block image: 2 atoms x 32 rows (hi 0-15, lo 16-31) x 128 B
+constexpr int kScanImgBufs = 3;             // image buffers: MMA input, epilogue output, store in flight
 
 struct ScanArgs {
   const uint8_t* m_img;
@@ -559,8 +545,8 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
   const int ncb = D / 16, KS = D / 16;
   uint8_t* mring = smem;
   uint8_t* bring = mring + STAGES * kScanMStage;
-  uint8_t* img = bring + STAGES * kScanBStage;  // 2 buffers
-  uint64_t* bars = reinterpret_cast<uint64_t*>(img + 2 * kScanImg);
+  uint8_t* img = bring + STAGES * kScanBStage;  // kScanImgBufs buffers
+  uint64_t* bars = reinterpret_cast<uint64_t*>(img + kScanImgBufs * kScanImg);
   uint64_t* full = bars;
   uint64_t* empty = full + STAGES;
   uint64_t* pfull = empty + STAGES;
@@ -642,15 +628,15 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
     if (lane == 0) {
       const uint32_t id = idesc_bf16(128, 32, 0, 0);
       const bool store = a.s_img != nullptr;
-      // the state block after step u (image buffer (u + 1) & 1; u = -1 is the
+      // the state block after step u (image buffer (u + 1) % 3; u = -1 is the
       // initial state) to global memory, laid out as in shared memory: the slot
       // of frame t0 + u, or in reverse slot T - 2 - u (the frame index of the
       // gradient U it holds)
       auto store_block = [&](int u) {
         const long long f = bh * T + (a.reverse ? T - 2 - u : t0 + u);
         if (in_region(((size_t)f * ncb + cb + 1) * NA * (32 * 128), a.s_span, a.status))
-          bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128), smem_u32(img + ((u + 1) & 1) * kScanImg),
-                   NA * 32 * 128);
+          bulk_s2g(a.s_img + ((size_t)f * ncb + cb) * NA * (32 * 128),
+                   smem_u32(img + ((u + 1) % kScanImgBufs) * kScanImg), NA * 32 * 128);
         bulk_commit();
       };
       // Descriptors of stage 0 / buffer 0; the other stages and buffers only move
@@ -661,23 +647,27 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
         ad0[kk] = smem_desc(smem_u32(mring) + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024);
         bd0[kk] = smem_desc(smem_u32(img) + (kk >> 2) * (32 * 128) + (kk & 3) * 32, 16, 1024);
       }
-      int stage = 0;
+      int stage = 0, buf = 0;  // buf = j % 3: the image buffer S_{j-1} is in
       uint32_t phase = 0;
       for (int j = 0; j < nsteps; ++j) {
         if (!wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status)) goto done;
         if (!wait_or_abort(smem_u32(sready), j & 1, abort_flag, a.status)) goto done;
         tc_fence_after();
+        // The store of S_{j-3} (issued two steps ago) has read its buffer, which S_j
+        // may overwrite once pfull(j) fires; the store of S_{j-2} may still be
+        // reading.  Waiting here, before the MMAs, keeps the store issue below off
+        // the frame's critical path.
+        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         const uint64_t ao = (uint64_t)((stage * kScanMStage) >> 4);
-        const uint64_t bo = (uint64_t)(((j & 1) * kScanImg) >> 4);
+        const uint64_t bo = (uint64_t)((buf * kScanImg) >> 4);
+        if (++buf == kScanImgBufs) buf = 0;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           if (kk < KS) mma_bf16(tmem, ad0[kk] + ao, bd0[kk] + bo, id, kk > 0 ? 1u : 0u);
-        if (store && (j >= 1 || a.reverse)) store_block(j - 1);
-        // The store of S_{j-2} has read its buffer, which S_j may now overwrite.
-        asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
         mma_commit(smem_u32(pfull));
         mma_commit(smem_u32(&empty[stage]));
         if (++stage == STAGES) { stage = 0; phase ^= 1; }
+        if (store && (j >= 1 || a.reverse)) store_block(j - 1);
       }
       if (store && nsteps > 0 && !a.reverse) {  // the reverse scan's last result is dS_0 (state_out only)
         if (!wait_or_abort(smem_u32(sready), nsteps & 1, abort_flag, a.status)) goto done;
@@ -779,9 +769,9 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
           for (int jj = 0; jj < 16; ++jj)
             x[jj] = relu_lin ? x[jj] + bv[jj] : fmaf(gt, x[jj] - (p[jj] + pl[jj]), add_b ? bv[jj] : 0.f);
         }
-        // S_j goes into the buffer of S_{j-2}, whose store has read it (the MMA
+        // S_j goes into the buffer of S_{j-3}, whose store has read it (the MMA
         // thread waited for that before committing pfull(j)).
-        write_img(img + ((j + 1) & 1) * kScanImg);
+        write_img(img + ((j + 1) % kScanImgBufs) * kScanImg);
         fence_proxy_async_smem();
       }
       if (++stage == STAGES) { stage = 0; phase ^= 1; }
@@ -817,268 +807,41 @@ done:
 }
 
 // =============================================================================
-// head scan: the frame loop of one whole head per CTA (every column block), for
-// the pipelined form, where it runs on a few SMs beside the gram and the
-// read-out of other frame chunks.  The arithmetic is the column-split scan's:
-// per frame P = M_t [S_{t-1} image] on the tensor core, now as one MMA chain
-// with N = 2D (the hi and lo rows of every 16-column block side by side, block
-// cb at rows 32 cb .. 32 cb + 31), then S <- g (S - P) + b_t in fp32 registers
-// (thread = state row, four warps per TMEM lane quadrant, two blocks each at
-// most), and the new image to the read-out's per-(frame-head, column-block)
-// blocks.  The state enters from and leaves to float32 [D][D] buffers, so a
-// sequence runs as consecutive launches over its frame chunks.  D <= 112.
-// =============================================================================
-constexpr int kHScanThreads = 544;  // 16 epilogue warps (thread 0 also issues MMAs and stores), 1 copy warp
-constexpr int kHScanStages = 2;
-constexpr int kHScanMaxD = 112;  // the whole-head b_t ring and image must fit beside the M ring
-
-struct HScanArgs {
-  const uint8_t* m_img;
-  const float* b_blk;
-  const float* g;
-  int gate_logits;
-  int variant;
-  const float* state_src;  // [BH][D][D]: the state entering the chunk (null: zeros)
-  float* state_dst;        // [BH][D][D]: the state leaving it (may alias state_src)
-  uint8_t* s_img;
-  int T, D, NA, t0, nsteps;
-  unsigned int* status;
-  size_t m_span, b_span, s_span;  // region extents (debug checks)
-};
-
-__global__ void __launch_bounds__(kHScanThreads, 1) tc_hscan_kernel(HScanArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = align1024(smem_raw);
-  const int NA = a.NA, D = a.D, T = a.T, KS = D / 16, ncb = D / 16;
-  const int img_atom = 2 * D * 128;  // one atom of the whole-head image: 2D rows x 128 B (1024-aligned)
-  const int bstage = D * D * 4;      // b_t of one frame-head, [cb][i][16] float32
-  uint8_t* mring = smem;
-  uint8_t* bring = mring + kHScanStages * kScanMStage;
-  uint8_t* img = bring + ((kHScanStages * bstage + 1023) & ~1023);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(img + NA * img_atom);
-  uint64_t* full = bars;
-  uint64_t* empty = full + kHScanStages;
-  uint64_t* pfull = empty + kHScanStages;
-  uint64_t* mma_done = pfull + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = warp_id(), lane = lane_id();
-  const long long bh = blockIdx.x;
-  const int nsteps = a.nsteps, t0 = a.t0;
-  if (threadIdx.x == 0) {
-    for (int st = 0; st < kHScanStages; ++st) {
-      mbar_init(smem_u32(&full[st]), 1);
-      mbar_init(smem_u32(&empty[st]), 17);  // the MMA's commit + the 16 epilogue warps (b read)
-    }
-    mbar_init(smem_u32(pfull), 1);
-    mbar_init(smem_u32(mma_done), 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  {  // M image rows D..127 of each atom (never copied in) must be finite
-    const int tail = (128 - D) * 8;
-    for (int idx = threadIdx.x; idx < kHScanStages * 2 * tail; idx += blockDim.x) {
-      const int region = idx / tail, c = idx % tail;
-      reinterpret_cast<uint4*>(mring + region * (128 * 128) + D * 128)[c] = make_uint4(0, 0, 0, 0);
-    }
-  }
-  fence_proxy_async_smem();
-  if (warp == 0) {
-    tmem_alloc(smem_u32(tmem_slot), 256);  // P: hi and lo of every column block, 2D columns
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  griddep_wait();  // no global memory is touched before the preceding kernel completes
-  griddep_launch_dependents();
-
-  if (warp == 16) {
-    // ---------------- copies in: the M_t image and the whole b_t
-    if (lane == 0) {
-      Ring<kHScanStages> r;
-      for (int j = 0; j < nsteps; ++j) {
-        if (!wait_or_abort(smem_u32(&empty[r.stage]), r.phase ^ 1, abort_flag, a.status)) break;
-        const long long f = bh * T + t0 + j;
-        const uint32_t fb = smem_u32(&full[r.stage]);
-        mbar_arrive_expect_tx(fb, NA * D * 128 + bstage);
-        const uint8_t* src = a.m_img + (size_t)f * NA * D * 128;
-        if (in_region(((size_t)f + 1) * NA * D * 128, a.m_span, a.status))
-          for (int at = 0; at < NA; ++at)
-            bulk_g2s(smem_u32(mring + r.stage * kScanMStage + at * 128 * 128), src + at * D * 128, D * 128, fb);
-        if (in_region(((size_t)f + 1) * bstage, a.b_span, a.status))
-          bulk_g2s(smem_u32(bring + r.stage * bstage), a.b_blk + (size_t)f * D * D, bstage, fb);
-        r.mark_issued();
-        r.advance();
-      }
-      r.drain(full);
-    }
-  } else if (warp < 16) {
-    const int q = warp & 3, cg = warp >> 2;
-    const int i = q * 32 + lane;
-    const bool row = i < D;
-    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    const int nb = (cg < ncb ? 1 : 0) + (cg + 4 < ncb ? 1 : 0);  // column blocks cg and cg + 4
-    bool fail = false;
-    int mstage = 0;
-    uint32_t mphase = 0;
-    const uint32_t id = idesc_bf16(128, 2 * D, 0, 0);
-    // the image of S_u (u = frame index in the chunk) to the read-out's blocks
-    auto store_img = [&](int u) {
-      const long long f = bh * T + t0 + u;
-      if (in_region(((size_t)f + 1) * ncb * NA * (32 * 128), a.s_span, a.status))
-        for (int cb = 0; cb < ncb; ++cb)
-          for (int at = 0; at < NA; ++at)
-            bulk_s2g(a.s_img + (((size_t)f * ncb + cb) * NA + at) * (32 * 128),
-                     smem_u32(img + at * img_atom + cb * 32 * 128), 32 * 128);
-      bulk_commit();
-    };
-    // thread 0: step j's MMA chain, P = M_t S_{j-1}, then the store of S_{j-1}'s image
-    auto issue = [&](int j) -> bool {
-      if (!wait_or_abort(smem_u32(&full[mstage]), mphase, abort_flag, a.status)) return false;
-      tc_fence_after();
-      const uint32_t mb = smem_u32(mring + mstage * kScanMStage), ib = smem_u32(img);
-      for (int kk = 0; kk < KS; ++kk)
-        mma_bf16(tmem, smem_desc(mb + (kk >> 2) * (128 * 128) + (kk & 3) * 32, 16, 1024),
-                 smem_desc(ib + (kk >> 2) * img_atom + (kk & 3) * 32, 16, 1024), id, kk > 0 ? 1u : 0u);
-      if (j >= 1) store_img(j - 1);
-      // the stores have read the image, which S_j may then overwrite
-      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-      mma_commit(smem_u32(pfull));
-      mma_commit(smem_u32(&empty[mstage]));
-      if (++mstage == kHScanStages) { mstage = 0; mphase ^= 1; }
-      return true;
-    };
-    float x[2][16];
-    const float* src = a.state_src ? a.state_src + (size_t)bh * D * D : nullptr;
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int cb = cg + 4 * u;
-#pragma unroll
-      for (int jj = 0; jj < 16; ++jj) x[u][jj] = 0.f;
-      if (u < nb && row && src) {
-        const float4* si = reinterpret_cast<const float4*>(src + (size_t)i * D + 16 * cb);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float4 w = si[e];
-          x[u][4 * e] = w.x;
-          x[u][4 * e + 1] = w.y;
-          x[u][4 * e + 2] = w.z;
-          x[u][4 * e + 3] = w.w;
-        }
-      }
-    }
-    auto write_img = [&]() {
-      if (!row) return;
-      uint8_t* at = img + (i >> 6) * img_atom;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (u >= nb) break;
-        const int r0 = 32 * (cg + 4 * u);
-#pragma unroll
-        for (int n = 0; n < 16; n += 2) {
-          uint32_t hv, lv;
-          split2(x[u][n], x[u][n + 1], hv, lv);
-          *reinterpret_cast<uint16_t*>(at + sw128_off(r0 + n, i & 63)) = (uint16_t)(hv & 0xFFFF);
-          *reinterpret_cast<uint16_t*>(at + sw128_off(r0 + n + 1, i & 63)) = (uint16_t)(hv >> 16);
-          *reinterpret_cast<uint16_t*>(at + sw128_off(r0 + 16 + n, i & 63)) = (uint16_t)(lv & 0xFFFF);
-          *reinterpret_cast<uint16_t*>(at + sw128_off(r0 + 17 + n, i & 63)) = (uint16_t)(lv >> 16);
-        }
-      }
-    };
-    write_img();
-    fence_proxy_async_smem();
-    named_barrier(1, 512);
-    if (threadIdx.x == 0 && nsteps > 0) fail = !issue(0);
-    const bool relu_lin = a.variant == kReluLinear;
-    float gnext = (nsteps > 0 && !relu_lin) ? __ldg(a.g + bh * T + t0) : 0.f;
-    int stage = 0;
-    uint32_t phase = 0;
-    for (int j = 0; j < nsteps; ++j) {
-      const long long f = bh * T + t0 + j;
-      const float gt = relu_lin ? 1.f : decay_of(gnext, a.gate_logits);
-      if (j + 1 < nsteps && !relu_lin) gnext = __ldg(a.g + f + 1);
-      const bool ok = !fail && wait_or_abort(smem_u32(pfull), j & 1, abort_flag, a.status) &&
-                      wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
-      if (!__all_sync(0xffffffffu, ok)) goto done;
-      tc_fence_after();
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (u >= nb) break;
-        const int cb = cg + 4 * u;
-        float p[16], pl[16];
-        tmem_ld16(tmem + lane_base + 32 * cb, p);
-        tmem_ld16(tmem + lane_base + 32 * cb + 16, pl);
-        float bv[16];
-        if (row) {
-          const float4* bp = reinterpret_cast<const float4*>(bring + stage * bstage + ((size_t)cb * D + i) * 64);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float4 w = bp[e];
-            bv[4 * e] = w.x;
-            bv[4 * e + 1] = w.y;
-            bv[4 * e + 2] = w.z;
-            bv[4 * e + 3] = w.w;
-          }
-        }
-        tmem_ld_wait();
-        if (row) {
-#pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
-            x[u][jj] = relu_lin ? x[u][jj] + bv[jj] : fmaf(gt, x[u][jj] - (p[jj] + pl[jj]), bv[jj]);
-        }
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
-      write_img();  // S_j over S_{j-1}: MMA j and the store of S_{j-1} have read it (pfull(j))
-      fence_proxy_async_smem();
-      if (++stage == kHScanStages) { stage = 0; phase ^= 1; }
-      named_barrier(1, 512);  // S_j's image is complete; every TMEM read of step j is done
-      if (threadIdx.x == 0) {
-        if (j + 1 < nsteps)
-          fail = !issue(j + 1);
-        else
-          store_img(j);
-      }
-    }
-    if (a.state_dst && row) {
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (u >= nb) break;
-        float4* so = reinterpret_cast<float4*>(a.state_dst + ((size_t)bh * D + i) * D + 16 * (cg + 4 * u));
-#pragma unroll
-        for (int e = 0; e < 4; ++e) so[e] = make_float4(x[u][4 * e], x[u][4 * e + 1], x[u][4 * e + 2], x[u][4 * e + 3]);
-      }
-    }
-  }
-done:
-  if (threadIdx.x == 0) {  // the thread that issued the MMAs and the image stores
-    bulk_wait0();
-    mma_commit(smem_u32(mma_done));
-    wait_bounded(smem_u32(mma_done), 0, 500000000ull);
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 256);
-  }
-}
-
-// =============================================================================
 // readout: O_t = Q_t S_t / sqrt(D) per frame-head and 128-token tile.
 //
-// Persistent CTAs.  Per frame-head the S_t image (bf16 hi + lo, the B operand:
-// K-major, row n = value column, D rows) is gathered from the scan's column
-// blocks (2 KB bulk copies) into one of two buffers; Q tiles of 128 tokens stream through a 2-deep TMA ring; per tile
+// Persistent CTAs.  Whole frame-heads are dealt round-robin while every CTA gets
+// one; the tiles of the frame-heads left over are then split into contiguous
+// ranges as equal as whole tiles allow, one per CTA (so a call of few
+// frame-heads still fills every SM).  Per frame-head of its work a CTA gathers
+// the S_t image (bf16 hi + lo, the B operand: K-major, row n = value column, D
+// rows) from the scan's column blocks (2 KB bulk copies) into one of two
+// buffers; Q tiles of 128 tokens stream through a 2-deep TMA ring; per tile
 // two MMA chains (hi, lo) accumulate O_tile (128 tokens x D) in one of four
 // TMEM accumulators.  Each epilogue warp owns 32 token rows: it scales and
 // rounds them to bf16 into its own slice of a staging tile and TMA-stores the
 // slice, waiting only for its own previous store.
 // =============================================================================
+// A read-out CTA's work: units u = f * ntiles + tile, the k-th of count.
+struct TileSched {
+  long long per1;   // units in the round-robin phase (whole frame-heads)
+  long long base;   // first unit of this CTA's tail range
+  long long count;  // units in all
+  int ntiles;
+  __device__ TileSched(long long F, int nt) : ntiles(nt) {
+    const long long G = gridDim.x, rounds = F / G, tail = (F - rounds * G) * nt;
+    const long long r0 = tail * blockIdx.x / G, r1 = tail * (blockIdx.x + 1) / G;
+    per1 = rounds * nt;
+    base = rounds * G * nt + r0;
+    count = per1 + (r1 - r0);
+  }
+  __device__ long long unit(long long k) const {
+    return k < per1 ? (blockIdx.x + (k / ntiles) * gridDim.x) * ntiles + k % ntiles : base + (k - per1);
+  }
+  // the unit starts / ends this CTA's share of its frame-head
+  __device__ bool first(long long k, int tile) const { return k == 0 || k == per1 || tile == 0; }
+  __device__ bool last(long long k, int tile) const { return k + 1 == count || tile == ntiles - 1; }
+};
+
 struct OutArgs {
   const uint8_t* s_img;
   int variant;  // kReluLinear: relu(Q) is applied to each Q tile in shared memory
@@ -1091,7 +854,6 @@ struct OutArgs {
   // same image read as an MN-major B operand.
   int transpose_s;
   size_t s_span;  // extent (bytes) of the state image region (debug checks)
-  ItemMap map;    // items -> frame-heads (zero: item i is frame-head i)
 };
 
 __global__ void __launch_bounds__(kOutThreads, 1)
@@ -1146,6 +908,7 @@ __global__ void __launch_bounds__(kOutThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const int ntiles = (S + kOutTok - 1) / kOutTok;
+  const TileSched sc(a.nitems, ntiles);
   griddep_wait();  // no global memory is touched before the preceding kernel completes
   griddep_launch_dependents();
 
@@ -1155,35 +918,32 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       prefetch_tmap(&mapQ);
       Ring<2> ra;
       Ring<kOutQStages> rq;
-      bool ok = true;
-      for (long long it = blockIdx.x; ok && it < a.nitems; it += gridDim.x) {
-        const long long f = a.map.f(it);
-        if (!wait_or_abort(smem_u32(&aempty[ra.stage]), ra.phase ^ 1, abort_flag, a.status)) break;
-        const uint32_t afb = smem_u32(&afull[ra.stage]);
-        mbar_arrive_expect_tx(afb, img_bytes);
-        // block cb of the scan = [atom][hi 16 rows | lo 16 rows][128 B]
-        const uint8_t* src = a.s_img + (size_t)f * img_bytes;
-        if (in_region(((size_t)f + 1) * img_bytes, a.s_span, a.status))
-          for (int cb = 0; cb < D / 16; ++cb)
-            for (int at = 0; at < NA; ++at)
-              for (int hl = 0; hl < 2; ++hl)
-                bulk_g2s(smem_u32(imgs + ra.stage * img_stride + (hl * NA + at) * D * 128 + cb * 16 * 128),
-                         src + ((size_t)cb * NA + at) * (32 * 128) + hl * 16 * 128, 16 * 128, afb);
-        ra.mark_issued();
-        ra.advance();
-        for (int tile = 0; tile < ntiles; ++tile) {
-          if (!wait_or_abort(smem_u32(&qempty[rq.stage]), rq.phase ^ 1, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          const uint32_t qfb = smem_u32(&qfull[rq.stage]);
-          mbar_arrive_expect_tx(qfb, q_bytes);
-          for (int at = 0; at < NA; ++at)
-            tma_load_3d(smem_u32(qst + rq.stage * q_bytes + at * kOutTok * 128), &mapQ, qfb, 64 * at,
-                        tile * kOutTok, (int)f);
-          rq.mark_issued();
-          rq.advance();
+      for (long long k = 0; k < sc.count; ++k) {
+        const long long u = sc.unit(k), f = u / ntiles;
+        const int tile = (int)(u % ntiles);
+        if (sc.first(k, tile)) {
+          if (!wait_or_abort(smem_u32(&aempty[ra.stage]), ra.phase ^ 1, abort_flag, a.status)) break;
+          const uint32_t afb = smem_u32(&afull[ra.stage]);
+          mbar_arrive_expect_tx(afb, img_bytes);
+          // block cb of the scan = [atom][hi 16 rows | lo 16 rows][128 B]
+          const uint8_t* src = a.s_img + (size_t)f * img_bytes;
+          if (in_region(((size_t)f + 1) * img_bytes, a.s_span, a.status))
+            for (int cb = 0; cb < D / 16; ++cb)
+              for (int at = 0; at < NA; ++at)
+                for (int hl = 0; hl < 2; ++hl)
+                  bulk_g2s(smem_u32(imgs + ra.stage * img_stride + (hl * NA + at) * D * 128 + cb * 16 * 128),
+                           src + ((size_t)cb * NA + at) * (32 * 128) + hl * 16 * 128, 16 * 128, afb);
+          ra.mark_issued();
+          ra.advance();
         }
+        if (!wait_or_abort(smem_u32(&qempty[rq.stage]), rq.phase ^ 1, abort_flag, a.status)) break;
+        const uint32_t qfb = smem_u32(&qfull[rq.stage]);
+        mbar_arrive_expect_tx(qfb, q_bytes);
+        for (int at = 0; at < NA; ++at)
+          tma_load_3d(smem_u32(qst + rq.stage * q_bytes + at * kOutTok * 128), &mapQ, qfb, 64 * at, tile * kOutTok,
+                      (int)f);
+        rq.mark_issued();
+        rq.advance();
       }
       ra.drain(afull);
       rq.drain(qfull);
@@ -1201,10 +961,12 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       const uint64_t lo_off = (uint64_t)((NA * D * 128) >> 4);
       int ab = 0, qs = 0, cb = 0;
       uint32_t aph = 0, qph = 0, cph = 0;
-      for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
-        if (!wait_or_abort(smem_u32(&afull[ab]), aph, abort_flag, a.status)) goto done;
+      for (long long k = 0; k < sc.count; ++k) {
+        const int tile = (int)(sc.unit(k) % ntiles);
+        if (sc.first(k, tile))
+          if (!wait_or_abort(smem_u32(&afull[ab]), aph, abort_flag, a.status)) goto done;
         const uint64_t io = (uint64_t)((ab * img_stride) >> 4);
-        for (int tile = 0; tile < ntiles; ++tile) {
+        {
           if (!wait_or_abort(smem_u32(&accempty[cb]), cph ^ 1, abort_flag, a.status)) goto done;
           if (!wait_or_abort(smem_u32(relu_q ? &qready[qs] : &qfull[qs]), qph, abort_flag, a.status)) goto done;
           tc_fence_after();
@@ -1222,8 +984,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
           if (++qs == kOutQStages) { qs = 0; qph ^= 1; }
           if (++cb == kOutAcc) { cb = 0; cph ^= 1; }
         }
-        mma_commit(smem_u32(&aempty[ab]));
-        if (++ab == 2) { ab = 0; aph ^= 1; }
+        if (sc.last(k, tile)) {  // the frame-head's last tile in this CTA's work
+          mma_commit(smem_u32(&aempty[ab]));
+          if (++ab == 2) { ab = 0; aph ^= 1; }
+        }
       }
     }
   } else if (warp >= 6) {
@@ -1233,8 +997,8 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       int qs = 0;
       uint32_t qph = 0;
       const __nv_bfloat162 zero = __floats2bfloat162_rn(0.f, 0.f);
-      for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
-        for (int tile = 0; tile < ntiles; ++tile) {
+      for (long long k = 0; k < sc.count; ++k) {
+        {
           if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&qfull[qs]), qph, abort_flag, a.status))) goto done;
           uint4* qt = reinterpret_cast<uint4*>(qst + qs * q_bytes);
           for (int idx = pt; idx < q_bytes / 16; idx += 128) {
@@ -1256,9 +1020,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     const int row = warp * 32 + lane;
     int cb = 0;
     uint32_t cph = 0;
-    for (long long it = blockIdx.x; it < a.nitems; it += gridDim.x) {
-      const long long f = a.map.f(it);
-      for (int tile = 0; tile < ntiles; ++tile) {
+    for (long long k = 0; k < sc.count; ++k) {
+      const long long u = sc.unit(k), f = u / ntiles;
+      const int tile = (int)(u % ntiles);
+      {
         if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[cb]), cph, abort_flag, a.status))) goto done;
         tc_fence_after();
         if (lane == 0) bulk_wait_read0();  // this warp's previous store has read its slice
@@ -1386,12 +1151,15 @@ struct KvArgs {
 // element-wise warps turn it into a bf16 hi + lo image in place of S_{t-1}'s
 // (row i of W is row i of its K-major image, W being symmetric) and sum its
 // trace.  Then per 128-token tile (K in a 2-deep ring, V single):
-//   warp 8 (MMA)    : X1 = K U_t, X3 = K W_t (K-major images), X2 = V U_t^T (U_t
-//                     read MN-major), all into TMEM;
+//   warp 8 (MMA)    : X1 = K U_t, then X3 = K W_t (K-major images) and
+//                     X2 = V U_t^T (U_t read MN-major), into TMEM as two groups
+//                     with their own full / empty barriers;
 //   warps 0-7       : two per TMEM lane quadrant, alternate 16-column chunks:
-//                     dV, dK~ straight from registers to global memory, the
-//                     partial dots of dbeta and dg (halves combined in shared
-//                     memory, fixed order);
+//                     dV from X1 (the X2 / X3 products run meanwhile), then dK~
+//                     from X2 and X3 (the next tile's X1 runs meanwhile), both
+//                     straight from registers to global memory, and the partial
+//                     dots of dbeta and dg (halves combined in shared memory,
+//                     fixed order);
 //   warp 9 (copies) : K and V tiles by TMA, the images by bulk copies.
 __global__ void __launch_bounds__(kKvThreads, 1)
     tc_kv_grad_kernel(const __grid_constant__ CUtensorMap mapK, const __grid_constant__ CUtensorMap mapV, KvArgs a) {
@@ -1411,12 +1179,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   uint64_t* wacc = bars + 2;     // W_t in TMEM
   uint64_t* wimg = bars + 3;     // W_t image written (8 warps)
   uint64_t* kfull = bars + 4;    // [2]
-  uint64_t* kempty = bars + 6;   // [2] (8 warps: K rows read after the tile's MMAs)
+  uint64_t* kempty = bars + 6;   // [2] (8 warps: K rows read; the MMA commit: the tile's MMAs done)
   uint64_t* vfull = bars + 8;
   uint64_t* vempty = bars + 9;   // the tile's MMAs done
-  uint64_t* xfull = bars + 10;   // X1..X3 in TMEM
-  uint64_t* xempty = bars + 11;  // X1..X3 read (8 warps)
+  uint64_t* x1full = bars + 10;   // X1 in TMEM
+  uint64_t* x1empty = bars + 11;  // X1 read (8 warps)
   uint64_t* mma_done = bars + 12;
+  uint64_t* x23full = bars + 13;   // X2, X3 in TMEM (and every MMA of the tile done)
+  uint64_t* x23empty = bars + 14;  // X2, X3 read (8 warps)
   float* red = reinterpret_cast<float*>(bars + 16);  // [2][8] per-warp dg partial sums, by tile parity
   float* dbh = red + 2 * 8;                          // [2][128] dbeta halves of warps 4-7, by tile parity
   float* trw = dbh + 2 * kKvTok;                     // [2][8] trace partials of W, by frame-head parity
@@ -1432,12 +1202,14 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     mbar_init(smem_u32(wimg), 8);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&kfull[b]), 1);
-      mbar_init(smem_u32(&kempty[b]), 8);
+      mbar_init(smem_u32(&kempty[b]), 9);
     }
     mbar_init(smem_u32(vfull), 1);
     mbar_init(smem_u32(vempty), 1);
-    mbar_init(smem_u32(xfull), 1);
-    mbar_init(smem_u32(xempty), 8);
+    mbar_init(smem_u32(x1full), 1);
+    mbar_init(smem_u32(x1empty), 8);
+    mbar_init(smem_u32(x23full), 1);
+    mbar_init(smem_u32(x23empty), 8);
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -1545,7 +1317,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
       const uint64_t tK0 = smem_desc(smem_u32(tK), 16, 1024), tV0 = smem_desc(smem_u32(tV), 16, 1024);
       const uint64_t lo16 = (uint64_t)(lo >> 4);
       int ks = 0;
-      uint32_t kph = 0, vph = 0, xph = 0, iph = 0, wph = 0;
+      uint32_t kph = 0, vph = 0, x1ph = 0, x23ph = 0, iph = 0, wph = 0;
       for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x) {
         if (!wait_or_abort(smem_u32(ifull), iph, abort_flag, a.status)) goto done;
         iph ^= 1;
@@ -1567,10 +1339,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         // the W image replaces S_{t-1}'s
         if (!wait_or_abort(smem_u32(wimg), wph, abort_flag, a.status)) goto done;
         wph ^= 1;
+        // Two accumulator groups per tile, so the element-wise warps' dV pass (X1)
+        // runs beside the X2 / X3 products and the next tile's X1 beside their
+        // dK pass (X2, X3).
         for (int tile = 0; tile < ntiles; ++tile) {
           if (!wait_or_abort(smem_u32(&kfull[ks]), kph, abort_flag, a.status)) goto done;
-          if (!wait_or_abort(smem_u32(vfull), vph, abort_flag, a.status)) goto done;
-          if (!wait_or_abort(smem_u32(xempty), xph ^ 1, abort_flag, a.status)) goto done;
+          if (!wait_or_abort(smem_u32(x1empty), x1ph ^ 1, abort_flag, a.status)) goto done;
           tc_fence_after();
           const uint64_t kso = (uint64_t)((ks * tile_bytes) >> 4);
           for (int kk = 0; kk < KS; ++kk) {  // K-dim = key dim i
@@ -1579,6 +1353,16 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             const uint64_t ad = tK0 + kso + ko;
             mma_bf16(tmem + kTX1, ad, uK + so, idK, kk > 0 ? 1u : 0u);
             mma_bf16(tmem + kTX1, ad, uK + lo16 + so, idK, 1u);
+          }
+          mma_commit(smem_u32(x1full));
+          x1ph ^= 1;
+          if (!wait_or_abort(smem_u32(vfull), vph, abort_flag, a.status)) goto done;
+          if (!wait_or_abort(smem_u32(x23empty), x23ph ^ 1, abort_flag, a.status)) goto done;
+          tc_fence_after();
+          for (int kk = 0; kk < KS; ++kk) {  // K-dim = key dim i
+            const uint64_t ko = (uint64_t)((((kk >> 2) * (kKvTok * 128) + (kk & 3) * 32)) >> 4);
+            const uint64_t so = (uint64_t)((((kk >> 2) * (D * 128) + (kk & 3) * 32)) >> 4);
+            const uint64_t ad = tK0 + kso + ko;
             mma_bf16(tmem + kTX3, ad, wK + so, idK, kk > 0 ? 1u : 0u);
             mma_bf16(tmem + kTX3, ad, wK + lo16 + so, idK, 1u);
           }
@@ -1589,10 +1373,11 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mma_bf16(tmem + kTX2, ad, uM + mo, idT, kk > 0 ? 1u : 0u);
             mma_bf16(tmem + kTX2, ad, uM + lo16 + mo, idT, 1u);
           }
-          mma_commit(smem_u32(xfull));
+          mma_commit(smem_u32(x23full));
+          mma_commit(smem_u32(&kempty[ks]));
           mma_commit(smem_u32(vempty));
           if (tile == ntiles - 1) mma_commit(smem_u32(iempty));
-          xph ^= 1;
+          x23ph ^= 1;
           vph ^= 1;
           if (++ks == 2) { ks = 0; kph ^= 1; }
         }
@@ -1608,7 +1393,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     const float ck = a.ck;
     long long n = 0;  // tiles of this CTA so far
     int ks = 0;
-    uint32_t kph = 0, xph = 0, wph = 0;
+    uint32_t kph = 0, x1ph = 0, x23ph = 0, wph = 0;
     int fpar = 0;  // frame-head parity (trace buffers)
     for (long long f = blockIdx.x; f < a.nitems; f += gridDim.x, fpar ^= 1) {
       const float gt = decay_of(__ldg(a.g + f), a.gate_logits);
@@ -1652,24 +1437,59 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const int s = tile * kKvTok + row;
         const bool valid = s < S;
         const float bt = valid ? beta_of(__ldg(a.beta + f * S + s), a.gate_logits) : 0.f;
-        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(xfull), xph, abort_flag, a.status))) goto done;
-        xph ^= 1;
-        tc_fence_after();
-        const uint8_t* kt = tK + ks * (NA * kKvTok * 128);
+        const float btck = bt * ck, gck = gt * ck;
         __nv_bfloat16* dvrow = a.dv + (f * S + s) * D;
         __nv_bfloat16* dkrow = a.dk + (f * S + s) * D;
+        // dV = beta ck X1 (the X1 group); this thread's K row chunks go to registers
+        // for the dK pass's dots, so the K slot is released (to the next load) as
+        // soon as the tile's MMAs are done
+        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(x1full), x1ph, abort_flag, a.status))) goto done;
+        x1ph ^= 1;
+        tc_fence_after();
+        const uint8_t* kt = tK + ks * (NA * kKvTok * 128);
+        uint4 krow[4][2];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int c0 = 16 * half + 32 * m;
+          if (c0 >= D) break;
+          float x1b[16];
+          tmem_ld16(tmem + lane_base + kTX1 + c0, x1b);
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            krow[m][h] = *reinterpret_cast<const uint4*>(kt + (c0 >> 6) * (kKvTok * 128) +
+                                                         sw128_off(row, (c0 & 63) + 8 * h));
+          tmem_ld_wait();
+          uint32_t ov[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) ov[e] = pack_bf16(btck * x1b[2 * e], btck * x1b[2 * e + 1]);
+          if (valid) {
+            reinterpret_cast<uint4*>(dvrow + c0)[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+            reinterpret_cast<uint4*>(dvrow + c0)[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(smem_u32(x1empty));
+          mbar_arrive(smem_u32(&kempty[ks]));
+        }
+        // dK~, the dbeta and dg dots (the X2, X3 group)
+        if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(x23full), x23ph, abort_flag, a.status))) goto done;
+        x23ph ^= 1;
+        tc_fence_after();
         float dot2 = 0.f, dot3 = 0.f;
-        for (int c0 = 16 * half; c0 < D; c0 += 32) {
-          float x1[16], x2[16], x3[16];
-          tmem_ld16(tmem + lane_base + kTX1 + c0, x1);
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          const int c0 = 16 * half + 32 * m;
+          if (c0 >= D) break;
+          float x2[16], x3[16];
           tmem_ld16(tmem + lane_base + kTX2 + c0, x2);
           tmem_ld16(tmem + lane_base + kTX3 + c0, x3);
           tmem_ld_wait();
-          uint32_t ov[8], ok[8];
+          uint32_t ok[8];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint4 kv = *reinterpret_cast<const uint4*>(kt + (c0 >> 6) * (kKvTok * 128) +
-                                                             sw128_off(row, (c0 & 63) + 8 * h));
+            const uint4 kv = krow[m][h];
             const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -1677,25 +1497,18 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               const int j = 8 * h + 2 * e;
               dot2 = fmaf(k2.x, x2[j], fmaf(k2.y, x2[j + 1], dot2));
               dot3 = fmaf(k2.x, x3[j], fmaf(k2.y, x3[j + 1], dot3));
-              ov[4 * h + e] = pack_bf16(bt * ck * x1[j], bt * ck * x1[j + 1]);
-              ok[4 * h + e] = pack_bf16(bt * ck * fmaf(-gt * ck, x3[j], x2[j]),
-                                        bt * ck * fmaf(-gt * ck, x3[j + 1], x2[j + 1]));
+              ok[4 * h + e] = pack_bf16(btck * fmaf(-gck, x3[j], x2[j]), btck * fmaf(-gck, x3[j + 1], x2[j + 1]));
             }
           }
           if (valid) {
-            reinterpret_cast<uint4*>(dvrow + c0)[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-            reinterpret_cast<uint4*>(dvrow + c0)[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
             reinterpret_cast<uint4*>(dkrow + c0)[0] = make_uint4(ok[0], ok[1], ok[2], ok[3]);
             reinterpret_cast<uint4*>(dkrow + c0)[1] = make_uint4(ok[4], ok[5], ok[6], ok[7]);
           }
         }
-        // this tile's TMEM and K rows are read
+        // this tile's X2 and X3 are read
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(smem_u32(xempty));
-          mbar_arrive(smem_u32(&kempty[ks]));
-        }
+        if (lane == 0) mbar_arrive(smem_u32(x23empty));
         if (++ks == 2) { ks = 0; kph ^= 1; }
         // dbeta_s = ck <k_s, X2_s> - (g / 2) ck^2 <k_s, X3_s>, this half's columns
         const float db = ck * dot2 - 0.5f * gt * ck * ck * dot3;
@@ -1778,7 +1591,7 @@ int gram_smem(int NA, int D) {
 int kv_smem(int NA, int D) { return 4 * NA * D * 128 + 3 * NA * kKvTok * 128 + kKvBarBytes + 1024; }
 static_assert(4 * 2 * 128 * 128 + 3 * 2 * kKvTok * 128 + 1792 + 1024 <= 232448, "kv_grad shared memory at D = 128");
 template <int STAGES>
-int scan_smem() { return STAGES * (kScanMStage + kScanBStage) + 2 * kScanImg + kBarBytes + 1024; }
+int scan_smem() { return STAGES * (kScanMStage + kScanBStage) + kScanImgBufs * kScanImg + kBarBytes + 1024; }
 
 constexpr int kTcChunk = kTcChunkFrames;
 
@@ -1817,134 +1630,40 @@ size_t tc_workspace_bytes(const Problem& p, int mode) { return tc_layout(p, mode
 
 namespace {
 
-// The gram over the call's frame-heads (`map`: all of them, or one frame chunk of
-// every head, `nitems` items on at most `max_ctas` persistent CTAs): the M_t
-// images and b_t blocks (regions of m_span and b_span bytes).
-int launch_gram(const Problem& p, const CUtensorMap& mapK, const CUtensorMap& mapV, uint8_t* m_img, float* b_mat,
-                size_t m_span, size_t b_span, cudaStream_t st, ItemMap map, long long nitems, int max_ctas) {
+// The gram over every frame-head of the call on persistent CTAs: the M_t images
+// and b_t blocks (regions of m_span and b_span bytes).
+int launch_gram(const Problem& p, uint8_t* m_img, float* b_mat, size_t m_span, size_t b_span, cudaStream_t st) {
   const int NA = num_atoms(p.D);
+  const long long F = p.BHT();
+  CUtensorMap mapK, mapV;
+  if (!make_map(&mapK, p.k, p.D, p.S, F, kGramTok) || !make_map(&mapV, p.v, p.D, p.S, F, kGramTok)) return kCuda;
   const int smem = gram_smem(NA, p.D);
   if (cudaFuncSetAttribute(tc_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return kCuda;
-  GramArgs ga{p.beta, p.gate_logits, p.variant, m_img, b_mat, nitems, p.S, p.D, NA, p.key_scale * p.key_scale,
-              p.key_scale, p.status, 0, m_span, b_span, map};
-  const unsigned grid = (unsigned)(nitems < max_ctas ? nitems : max_ctas);
+  GramArgs ga{p.beta, p.gate_logits, p.variant, m_img, b_mat, F, p.S, p.D, NA, p.key_scale * p.key_scale,
+              p.key_scale, p.status, 0, m_span, b_span};
+  const int nsm = num_sms();
+  const unsigned grid = (unsigned)(F < nsm ? F : nsm);
   ProfScope ps(st, "tc_gram");
   return launch_pdl(tc_gram_kernel, grid, kGramThreads, smem, st, mapK, mapV, ga) == cudaSuccess ? kOk : kCuda;
 }
 
-int launch_gram(const Problem& p, uint8_t* m_img, float* b_mat, size_t m_span, size_t b_span, cudaStream_t st) {
-  const long long F = p.BHT();
-  CUtensorMap mapK, mapV;
-  if (!make_map(&mapK, p.k, p.D, p.S, F, kGramTok) || !make_map(&mapV, p.v, p.D, p.S, F, kGramTok)) return kCuda;
-  return launch_gram(p, mapK, mapV, m_img, b_mat, m_span, b_span, st, ItemMap{0, 0, 0}, F, num_sms());
-}
-
-// The read-out over the call's frame-heads (`map`, `nitems`, `max_ctas` as launch_gram).
+// The read-out over every frame-head of the call on persistent CTAs.
 int launch_readout(const Problem& p, const CUtensorMap& mapQ, const CUtensorMap& mapO, const uint8_t* s_img,
-                   size_t s_span, cudaStream_t st, ItemMap map, long long nitems, int max_ctas) {
+                   size_t s_span, cudaStream_t st) {
+  const long long F = p.BHT();
+  const int nsm = num_sms();
   const int NA = num_atoms(p.D);
   const int smem = out_smem(NA, p.D);
   if (cudaFuncSetAttribute(tc_readout_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return kCuda;
   const size_t shrink = debug_shrink();
-  OutArgs oa{s_img, p.variant, static_cast<__nv_bfloat16*>(p.out), nitems, p.S, p.D, NA, p.out_scale, p.status, 0,
-             s_span > shrink ? s_span - shrink : 1, map};
-  const unsigned grid = (unsigned)(nitems < max_ctas ? nitems : max_ctas);
+  OutArgs oa{s_img, p.variant, static_cast<__nv_bfloat16*>(p.out), F, p.S, p.D, NA, p.out_scale, p.status, 0,
+             s_span > shrink ? s_span - shrink : 1};
+  const long long units = F * ((p.S + kOutTok - 1) / kOutTok);  // (frame-head, tile) pairs
+  const unsigned grid = (unsigned)(units < nsm ? units : nsm);
   ProfScope ps(st, "tc_readout");
   return launch_pdl(tc_readout_kernel, grid, kOutThreads, smem, st, mapQ, mapO, oa) == cudaSuccess ? kOk : kCuda;
-}
-
-// ---- pipelined form --------------------------------------------------------------
-// Frames in chunks of kPipeFrames.  The gram and read-out of each chunk (every
-// head) run on the caller's stream over num_sms - BH SMs, the head scan of chunk c
-// (one CTA per head) on a second stream, after the gram of c (an event) and before
-// the read-out of c (an event back): the scan of one chunk overlaps the gram of the
-// next and the read-out of the one before.  No kernel waits on another.
-constexpr int kPipeFrames = 32;
-
-bool pipeline_fits(const Problem& p) {
-  return p.dtype == GDN_BF16 && p.D <= kHScanMaxD && p.BH() * 4 <= num_sms() && p.T > kPipeFrames;
-}
-
-int hscan_smem(int NA, int D) {
-  return kHScanStages * kScanMStage + ((kHScanStages * D * D * 4 + 1023) & ~1023) + NA * 2 * D * 128 + kBarBytes +
-         1024;
-}
-
-// The second stream and the events of the pipelined form, per device (created on
-// first use, kept for the process).  Their users hold `mu` while they enqueue, so
-// each record is waited on before it is recorded again.
-struct PipeRes {
-  std::mutex mu;
-  cudaStream_t aux = nullptr;
-  cudaEvent_t start = nullptr, gram = nullptr, scan = nullptr;
-};
-
-PipeRes* pipe_res() {
-  static PipeRes res[64];
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  PipeRes& r = res[dev];
-  if (!r.aux) {
-    if (cudaStreamCreateWithFlags(&r.aux, cudaStreamNonBlocking) != cudaSuccess) return nullptr;
-    if (cudaEventCreateWithFlags(&r.start, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&r.gram, cudaEventDisableTiming) != cudaSuccess ||
-        cudaEventCreateWithFlags(&r.scan, cudaEventDisableTiming) != cudaSuccess)
-      return nullptr;
-  }
-  return &r;
-}
-
-int pipelined_forward(const Problem& p, const TcLayout& L, uint8_t* w, const CUtensorMap& mapQ,
-                      const CUtensorMap& mapO, cudaStream_t st) {
-  const long long F = p.BHT(), BH = p.BH();
-  CUtensorMap mapK, mapV;
-  if (!make_map(&mapK, p.k, p.D, p.S, F, kGramTok) || !make_map(&mapV, p.v, p.D, p.S, F, kGramTok)) return kCuda;
-  PipeRes* pr = pipe_res();
-  if (!pr) return kCuda;
-  std::lock_guard<std::mutex> lock(pr->mu);
-  const int NA = num_atoms(p.D);
-  uint8_t* m_img = w + L.m_off;
-  float* b_mat = reinterpret_cast<float*>(w + L.b_off);
-  uint8_t* s_img = w + L.s_off;
-  float* carry = reinterpret_cast<float*>(w + L.carry_off);
-  const size_t m_span = L.b_off - L.m_off, b_span = L.s_off - L.b_off, s_span = L.carry_off - L.s_off;
-  const int ctas = num_sms() - (int)BH;
-  const int smem = hscan_smem(NA, p.D);
-  if (cudaFuncSetAttribute(tc_hscan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-    return kCuda;
-  const int nch = (p.T + kPipeFrames - 1) / kPipeFrames;
-  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
-  // the second stream starts after the caller's work so far
-  if (!ok(cudaEventRecord(pr->start, st)) || !ok(cudaStreamWaitEvent(pr->aux, pr->start, 0))) return kCuda;
-  for (int c = 0; c <= nch; ++c) {
-    if (c < nch) {
-      const int t0 = c * kPipeFrames, n = p.T - t0 < kPipeFrames ? p.T - t0 : kPipeFrames;
-      int rc = launch_gram(p, mapK, mapV, m_img, b_mat, m_span, b_span, st, ItemMap{p.T, t0, n}, BH * n, ctas);
-      if (rc != kOk) return rc;
-      if (!ok(cudaEventRecord(pr->gram, st)) || !ok(cudaStreamWaitEvent(pr->aux, pr->gram, 0))) return kCuda;
-    }
-    if (c >= 1) {  // the read-out of the chunk before, once its scan is done
-      const int t0 = (c - 1) * kPipeFrames, n = p.T - t0 < kPipeFrames ? p.T - t0 : kPipeFrames;
-      if (!ok(cudaStreamWaitEvent(st, pr->scan, 0))) return kCuda;
-      const int rc = launch_readout(p, mapQ, mapO, s_img, s_span, st, ItemMap{p.T, t0, n}, BH * n, ctas);
-      if (rc != kOk) return rc;
-    }
-    if (c < nch) {
-      const int t0 = c * kPipeFrames, n = p.T - t0 < kPipeFrames ? p.T - t0 : kPipeFrames;
-      HScanArgs ha{m_img, b_mat, p.g, p.gate_logits, p.variant, c == 0 ? p.state_in : carry,
-                   c == nch - 1 ? p.state_out : carry, s_img, p.T, p.D, NA, t0, n, p.status, m_span, b_span, s_span};
-      {
-        ProfScope ps(pr->aux, "tc_hscan");
-        if (launch_pdl(tc_hscan_kernel, (unsigned)BH, kHScanThreads, smem, pr->aux, ha) != cudaSuccess) return kCuda;
-      }
-      if (!ok(cudaEventRecord(pr->scan, pr->aux))) return kCuda;
-    }
-  }
-  return kOk;
 }
 
 // The chunked scan's summary form: [A_c | b_c] of every (head, chunk) into `maps`.
@@ -1986,15 +1705,12 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
   float* b_mat = reinterpret_cast<float*>(w + L.b_off);
   uint8_t* s_img = w + L.s_off;
   const long long F = p.BHT();
-  const int nsm = num_sms();
 
   CUtensorMap mapQ, mapO;
   if (!make_map(&mapQ, p.q, p.D, p.S, F, kOutTok) || !make_map(&mapO, p.out, p.D, p.S, F, 32)) return kCuda;
-  if (p.mode == GDN_MODE_PIPELINED && pipeline_fits(p)) return pipelined_forward(p, L, w, mapQ, mapO, st);
 
   const size_t m_span = L.b_off - L.m_off, b_span = L.s_off - L.b_off;
-  const size_t s_span =
-      (p.mode == GDN_MODE_PREFIX ? L.maps_off : (p.mode == GDN_MODE_PIPELINED ? L.carry_off : L.total)) - L.s_off;
+  const size_t s_span = (p.mode == GDN_MODE_PREFIX ? L.maps_off : L.total) - L.s_off;
   int rc = launch_gram(p, m_img, b_mat, m_span, b_span, st);
   if (rc != kOk) return rc;
   if (p.mode == GDN_MODE_PREFIX) {
@@ -2029,7 +1745,7 @@ int tc_forward(const Problem& p, void* ws, cudaStream_t st) {
     rc = launch_scan<4>(sa, p.BH() * (p.D / 16), st, "tc_scan");
     if (rc != kOk) return rc;
   }
-  return launch_readout(p, mapQ, mapO, s_img, s_span, st, ItemMap{0, 0, 0}, F, nsm);
+  return launch_readout(p, mapQ, mapO, s_img, s_span, st);
 }
 
 

@@ -187,7 +187,7 @@ def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("what", choices=["launches", "counters", "traffic"])
     ap.add_argument("--workload", default="minute", choices=sorted(synth.WORKLOADS))
-    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2, 3])
+    ap.add_argument("--mode", type=int, default=0, choices=[0, 1, 2])
     ap.add_argument("--backward", action="store_true")
     ap.add_argument("--kernel", default="tc_gram", help="kernel function name prefix (counters, traffic)")
     ap.add_argument("--frames", type=int, default=None, help="first N frames only (counters, traffic)")

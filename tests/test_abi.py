@@ -69,7 +69,7 @@ def _call(B=1, H=2, T=3, S=17, D=32, dtype=1, ptr=A16, g=A16, beta=A16, out=A16,
 
 @pytest.mark.parametrize("kw,code", [
     (dict(B=0), 1), (dict(H=0), 1), (dict(T=-1), 1), (dict(S=0), 1), (dict(D=0), 1),
-    (dict(dtype=2), 1), (dict(mode=4), 1), (dict(mode=-1), 1), (dict(mode=5), 1),
+    (dict(dtype=2), 1), (dict(mode=4), 1), (dict(mode=-1), 1), (dict(mode=3), 1), (dict(mode=3, dtype=0), 1),
     (dict(D=24), 2), (dict(D=144), 2), (dict(D=8), 2),
     (dict(ptr=None), 1), (dict(g=None), 1), (dict(beta=None), 1), (dict(out=None), 1),
     (dict(ptr=MIS), 3), (dict(out=MIS), 3), (dict(g=A16 + 2), 3), (dict(state_in=MIS), 3),
@@ -97,15 +97,12 @@ def test_workspace_bytes_is_pure_and_scales(lib):
 
 
 @pytest.mark.parametrize("D", [16, 32, 48, 64, 80, 96, 112, 128])
-def test_every_form_needs_a_workspace_and_no_mode_4(lib, D):
-    """Modes 0-3 need scratch (the pipelined form the split form's plus one state
-    buffer per head); mode 4 (no such form) is rejected: 0 bytes, and
-    GDN_ERR_INVALID_ARG from the entry points (test_validation_rejects)."""
-    for mode in (0, 1, 2, 3):
+def test_every_form_needs_a_workspace_and_no_mode_3(lib, D):
+    """Modes 0-2 need scratch; mode 3 (no such form) is rejected: 0 bytes, and
+    GDN_ERR_INVALID_ARG from the entry points (test_host_validation)."""
+    for mode in (0, 1, 2):
         assert binding.gdn_workspace_bytes(4, 16, 241, 3600, D, 1, mode) > 0
-    assert binding.gdn_workspace_bytes(4, 16, 241, 3600, D, 1, 3) == (
-        binding.gdn_workspace_bytes(4, 16, 241, 3600, D, 1, 2) + 4 * 16 * D * D * 4)
-    assert binding.gdn_workspace_bytes(4, 16, 241, 3600, D, 1, 4) == 0
+    assert binding.gdn_workspace_bytes(4, 16, 241, 3600, D, 1, 3) == 0
 
 
 def test_no_gpu_call_fails_loudly_not_silently(lib):
