@@ -202,8 +202,8 @@ struct GramArgs {
   float m_scale, b_scale;
   unsigned int* status;
   // 1: only the b part, with beta = 1 (the backward's Q^T dO: K holds Q, V holds
-  // dO); no M image.  The A operand is then exact in bf16, so its lo part is zero
-  // and its MMA is skipped.
+  // dO); no M image.  The A operand is then the Q tile itself, exact in bf16: the
+  // MMA reads it straight from the TMA ring and the beta-scaling warps sit out.
   int b_only;
   size_t m_span, b_span;  // extents (bytes) of the M image and b block regions (debug checks)
 };
@@ -318,7 +318,9 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         tc_fence_after();
         const uint32_t acc = tmem + ab * 256;
         for (int c = 0; c < nchunks; ++c) {
-          if (!wait_or_abort(smem_u32(&conv_full[cs]), cph, abort_flag, a.status)) goto done;
+          if (!wait_or_abort(a.b_only ? smem_u32(&raw_full[rs]) : smem_u32(&conv_full[cs]), a.b_only ? rph : cph,
+                             abort_flag, a.status))
+            goto done;
           tc_fence_after();
           const uint64_t ro = (uint64_t)((rs * kRawStage) >> 4), co = (uint64_t)((cs * kConvStage) >> 4);
 #pragma unroll
@@ -326,16 +328,18 @@ __global__ void __launch_bounds__(kGramThreads, 1)
             const uint64_t ko = (uint64_t)((kk * 2048) >> 4);
             const uint32_t accum = (c > 0 || kk > 0) ? 1u : 0u;
             if (a.b_only) {
-              mma_bf16(acc + accb, dH0 + co + ko, dV0 + ro + ko, id2, accum);
+              mma_bf16(acc + accb, dK0 + ro + ko, dV0 + ro + ko, id2, accum);
               continue;
             }
             mma_bf16(acc, dH0 + co + ko, dK0 + ro + ko, id1, accum);
             mma_bf16(acc + accb, dL0 + co + ko, dV0 + ro + ko, id2, 1u);
           }
           mma_commit(smem_u32(&raw_empty[rs]));
-          mma_commit(smem_u32(&conv_empty[cs]));
           if (++rs == kGramRaw) { rs = 0; rph ^= 1; }
-          if (++cs == kGramConv) { cs = 0; cph ^= 1; }
+          if (!a.b_only) {
+            mma_commit(smem_u32(&conv_empty[cs]));
+            if (++cs == kGramConv) { cs = 0; cph ^= 1; }
+          }
         }
         mma_commit(smem_u32(&accfull[ab]));
         if (++ab == 2) { ab = 0; aph ^= 1; }
@@ -345,6 +349,7 @@ __global__ void __launch_bounds__(kGramThreads, 1)
     // ---------------- beta scaling: A = diag(beta) K, split into bf16 hi + lo.
     // Elementwise, so each 16-byte chunk is transformed where it lies in the
     // swizzled tile (the hi / lo tiles share the K tile's layout).
+    if (a.b_only) goto done;  // the MMA reads the raw tiles
     const int ct = threadIdx.x - 128;
     int rs = 0, cs = 0;
     uint32_t rph = 0, cph = 0;
@@ -446,11 +451,15 @@ __global__ void __launch_bounds__(kGramThreads, 1)
         tmem_ld16(acc + NA * 64 + 16 * cb, v);
         tmem_ld_wait();
         if (i < D && in_region(((((size_t)f * ncb + cb) * D + i) * 16 + 16) * 4, a.b_span, a.status)) {
-          float4* dst = reinterpret_cast<float4*>(a.b_blk + (((size_t)f * ncb + cb) * D + i) * 16);
+          // row i of the block: 64 contiguous bytes (the workspace is 256-byte aligned)
+          float* dst = a.b_blk + (((size_t)f * ncb + cb) * D + i) * 16;
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            dst[q] = make_float4(v[4 * q] * a.b_scale, v[4 * q + 1] * a.b_scale, v[4 * q + 2] * a.b_scale,
-                                 v[4 * q + 3] * a.b_scale);
+          for (int q = 0; q < 2; ++q) {
+            uint32_t w[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = __float_as_uint(v[8 * q + e] * a.b_scale);
+            st_global_v8(dst + 8 * q, w);
+          }
         }
       }
       tc_fence_before();
@@ -834,10 +843,22 @@ struct TileSched {
     base = rounds * G * nt + r0;
     count = per1 + (r1 - r0);
   }
-  __device__ long long unit(long long k) const {
-    return k < per1 ? (blockIdx.x + (k / ntiles) * gridDim.x) * ntiles + k % ntiles : base + (k - per1);
+  // frame-head and tile of unit 0
+  __device__ void start(long long& f, int& tile) const {
+    f = per1 > 0 ? (long long)blockIdx.x : base / ntiles;
+    tile = per1 > 0 ? 0 : (int)(base % ntiles);
   }
-  // the unit starts / ends this CTA's share of its frame-head
+  // from unit k to unit k + 1 (no division but at the phase change)
+  __device__ void advance(long long k, long long& f, int& tile) const {
+    if (k + 1 == per1) {
+      f = base / ntiles;
+      tile = (int)(base % ntiles);
+    } else if (++tile == ntiles) {
+      tile = 0;
+      f += k < per1 ? (long long)gridDim.x : 1;
+    }
+  }
+  // unit k starts / ends this CTA's share of its frame-head
   __device__ bool first(long long k, int tile) const { return k == 0 || k == per1 || tile == 0; }
   __device__ bool last(long long k, int tile) const { return k + 1 == count || tile == ntiles - 1; }
 };
@@ -918,9 +939,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       prefetch_tmap(&mapQ);
       Ring<2> ra;
       Ring<kOutQStages> rq;
-      for (long long k = 0; k < sc.count; ++k) {
-        const long long u = sc.unit(k), f = u / ntiles;
-        const int tile = (int)(u % ntiles);
+      long long f;
+      int tile;
+      sc.start(f, tile);
+      for (long long k = 0; k < sc.count; sc.advance(k++, f, tile)) {
         if (sc.first(k, tile)) {
           if (!wait_or_abort(smem_u32(&aempty[ra.stage]), ra.phase ^ 1, abort_flag, a.status)) break;
           const uint32_t afb = smem_u32(&afull[ra.stage]);
@@ -961,8 +983,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
       const uint64_t lo_off = (uint64_t)((NA * D * 128) >> 4);
       int ab = 0, qs = 0, cb = 0;
       uint32_t aph = 0, qph = 0, cph = 0;
-      for (long long k = 0; k < sc.count; ++k) {
-        const int tile = (int)(sc.unit(k) % ntiles);
+      long long f;
+      int tile;
+      sc.start(f, tile);
+      for (long long k = 0; k < sc.count; sc.advance(k++, f, tile)) {
         if (sc.first(k, tile))
           if (!wait_or_abort(smem_u32(&afull[ab]), aph, abort_flag, a.status)) goto done;
         const uint64_t io = (uint64_t)((ab * img_stride) >> 4);
@@ -1020,9 +1044,10 @@ __global__ void __launch_bounds__(kOutThreads, 1)
     const int row = warp * 32 + lane;
     int cb = 0;
     uint32_t cph = 0;
-    for (long long k = 0; k < sc.count; ++k) {
-      const long long u = sc.unit(k), f = u / ntiles;
-      const int tile = (int)(u % ntiles);
+    long long f;
+    int tile;
+    sc.start(f, tile);
+    for (long long k = 0; k < sc.count; sc.advance(k++, f, tile)) {
       {
         if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(&accfull[cb]), cph, abort_flag, a.status))) goto done;
         tc_fence_after();
@@ -1143,6 +1168,9 @@ struct KvArgs {
   float ck;  // 1/sqrt(D*S)
   unsigned int* status;
   size_t s_span, s0_span, u_span;  // extents (bytes) of the image regions (debug checks)
+  // dk and dv are 32-byte aligned: each thread writes its 16 columns of a row in
+  // one 32-byte store (a row is 2 D bytes, a multiple of 32)
+  int wide_stores;
 };
 
 // Persistent CTAs over frame-heads.  Per frame-head: the S_{t-1} and U_t images
@@ -1179,7 +1207,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
   uint64_t* wacc = bars + 2;     // W_t in TMEM
   uint64_t* wimg = bars + 3;     // W_t image written (8 warps)
   uint64_t* kfull = bars + 4;    // [2]
-  uint64_t* kempty = bars + 6;   // [2] (8 warps: K rows read; the MMA commit: the tile's MMAs done)
+  uint64_t* kempty = bars + 6;   // [2] (8 warps: K rows read after the tile's MMAs)
   uint64_t* vfull = bars + 8;
   uint64_t* vempty = bars + 9;   // the tile's MMAs done
   uint64_t* x1full = bars + 10;   // X1 in TMEM
@@ -1202,7 +1230,7 @@ __global__ void __launch_bounds__(kKvThreads, 1)
     mbar_init(smem_u32(wimg), 8);
     for (int b = 0; b < 2; ++b) {
       mbar_init(smem_u32(&kfull[b]), 1);
-      mbar_init(smem_u32(&kempty[b]), 9);
+      mbar_init(smem_u32(&kempty[b]), 8);
     }
     mbar_init(smem_u32(vfull), 1);
     mbar_init(smem_u32(vempty), 1);
@@ -1374,7 +1402,6 @@ __global__ void __launch_bounds__(kKvThreads, 1)
             mma_bf16(tmem + kTX2, ad, uM + lo16 + mo, idT, 1u);
           }
           mma_commit(smem_u32(x23full));
-          mma_commit(smem_u32(&kempty[ks]));
           mma_commit(smem_u32(vempty));
           if (tile == ntiles - 1) mma_commit(smem_u32(iempty));
           x23ph ^= 1;
@@ -1440,29 +1467,23 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         const float btck = bt * ck, gck = gt * ck;
         __nv_bfloat16* dvrow = a.dv + (f * S + s) * D;
         __nv_bfloat16* dkrow = a.dk + (f * S + s) * D;
-        // dV = beta ck X1 (the X1 group); this thread's K row chunks go to registers
-        // for the dK pass's dots, so the K slot is released (to the next load) as
-        // soon as the tile's MMAs are done
+        // dV = beta ck X1 (the X1 group)
         if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(x1full), x1ph, abort_flag, a.status))) goto done;
         x1ph ^= 1;
         tc_fence_after();
-        const uint8_t* kt = tK + ks * (NA * kKvTok * 128);
-        uint4 krow[4][2];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
           const int c0 = 16 * half + 32 * m;
           if (c0 >= D) break;
           float x1b[16];
           tmem_ld16(tmem + lane_base + kTX1 + c0, x1b);
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            krow[m][h] = *reinterpret_cast<const uint4*>(kt + (c0 >> 6) * (kKvTok * 128) +
-                                                         sw128_off(row, (c0 & 63) + 8 * h));
           tmem_ld_wait();
           uint32_t ov[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) ov[e] = pack_bf16(btck * x1b[2 * e], btck * x1b[2 * e + 1]);
-          if (valid) {
+          if (valid && a.wide_stores) {
+            st_global_v8(dvrow + c0, ov);
+          } else if (valid) {
             reinterpret_cast<uint4*>(dvrow + c0)[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
             reinterpret_cast<uint4*>(dvrow + c0)[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
           }
@@ -1471,12 +1492,12 @@ __global__ void __launch_bounds__(kKvThreads, 1)
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(smem_u32(x1empty));
-          mbar_arrive(smem_u32(&kempty[ks]));
         }
         // dK~, the dbeta and dg dots (the X2, X3 group)
         if (!__all_sync(0xffffffffu, wait_or_abort(smem_u32(x23full), x23ph, abort_flag, a.status))) goto done;
         x23ph ^= 1;
         tc_fence_after();
+        const uint8_t* kt = tK + ks * (NA * kKvTok * 128);
         float dot2 = 0.f, dot3 = 0.f;
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
@@ -1489,7 +1510,8 @@ __global__ void __launch_bounds__(kKvThreads, 1)
           uint32_t ok[8];
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            const uint4 kv = krow[m][h];
+            const uint4 kv = *reinterpret_cast<const uint4*>(kt + (c0 >> 6) * (kKvTok * 128) +
+                                                             sw128_off(row, (c0 & 63) + 8 * h));
             const uint32_t kw[4] = {kv.x, kv.y, kv.z, kv.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
@@ -1500,15 +1522,20 @@ __global__ void __launch_bounds__(kKvThreads, 1)
               ok[4 * h + e] = pack_bf16(btck * fmaf(-gck, x3[j], x2[j]), btck * fmaf(-gck, x3[j + 1], x2[j + 1]));
             }
           }
-          if (valid) {
+          if (valid && a.wide_stores) {
+            st_global_v8(dkrow + c0, ok);
+          } else if (valid) {
             reinterpret_cast<uint4*>(dkrow + c0)[0] = make_uint4(ok[0], ok[1], ok[2], ok[3]);
             reinterpret_cast<uint4*>(dkrow + c0)[1] = make_uint4(ok[4], ok[5], ok[6], ok[7]);
           }
         }
-        // this tile's X2 and X3 are read
+        // this tile's X2, X3 and K rows are read
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(x23empty));
+        if (lane == 0) {
+          mbar_arrive(smem_u32(x23empty));
+          mbar_arrive(smem_u32(&kempty[ks]));
+        }
         if (++ks == 2) { ks = 0; kph ^= 1; }
         // dbeta_s = ck <k_s, X2_s> - (g / 2) ck^2 <k_s, X3_s>, this half's columns
         const float db = ck * dot2 - 0.5f * gt * ck * ck * dot3;
@@ -1861,7 +1888,8 @@ int tc_backward(const Problem& p, const BwdGrads& gr, void* ws, cudaStream_t st,
               static_cast<const __nv_bfloat16*>(p.v), p.gate_logits,
               static_cast<__nv_bfloat16*>(gr.dk),
               static_cast<__nv_bfloat16*>(gr.dv), gr.dbeta, dg_part, F, p.T, p.S, D, NA, p.key_scale, p.status,
-              L.u_off - L.s_off, L.dg_off - L.s0_off, L.s0_off - L.u_off};
+              L.u_off - L.s_off, L.dg_off - L.s0_off, L.s0_off - L.u_off,
+              ((reinterpret_cast<uintptr_t>(gr.dk) | reinterpret_cast<uintptr_t>(gr.dv)) & 31) == 0 ? 1 : 0};
     ProfScope ps(st, "tc_bwd_kv_grad");
     tc_kv_grad_kernel<<<pgrid, kKvThreads, smem, st>>>(mapK128, mapV128, ka);
   }

@@ -226,3 +226,35 @@ def test_backward_reuses_the_forward_states(case):
     else:
         for key in parity.GRAD_KEYS:
             assert torch.equal(a[key], b[key]), key
+
+
+def test_backward_outputs_only_16_byte_aligned():
+    """dk and dv on 16- but not 32-byte boundaries (the kernel's 32-byte row stores
+    fall back to 16-byte ones): the same gradients, bit for bit."""
+    wl, x, gr, S0 = _case_inputs("bf16", 1, 2, 5, 130, 112, True, 6600)
+    ref = _run_bwd(wl, x, gr["dout"], S0, gr["dstate"])
+    q, k, v, g, beta = parity.upload(wl, x)
+    do = torch.from_numpy(np.ascontiguousarray(gr["dout"])).cuda().to(q.dtype).contiguous()
+    si = torch.from_numpy(S0).cuda()
+    ds = torch.from_numpy(gr["dstate"]).cuda()
+    n = q.numel()
+    raw = [torch.empty(n + 16, dtype=q.dtype, device="cuda") for _ in range(2)]
+    dk, dv = (r[8:8 + n] for r in raw)  # 16 bytes past a 256-byte boundary
+    assert dk.data_ptr() % 32 == 16 and dv.data_ptr() % 32 == 16
+    dq = torch.empty_like(q)
+    dg = torch.empty(g.shape, device="cuda")
+    db = torch.empty(beta.shape, device="cuda")
+    dsi = torch.empty_like(si)
+    B, H, T, S, D = q.shape
+    need = binding.gdn_bwd_workspace_bytes(B, H, T, S, D, binding.GDN_BF16)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    rc = binding.gdn_frame_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), g.data_ptr(), beta.data_ptr(), si.data_ptr(),
+                               do.data_ptr(), ds.data_ptr(), dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), dg.data_ptr(),
+                               db.data_ptr(), dsi.data_ptr(), B, H, T, S, D, binding.GDN_BF16, ws.data_ptr(), need, st)
+    assert rc == 0
+    torch.cuda.synchronize()
+    parity.check_status()
+    np.testing.assert_array_equal(np_(dk.view(q.shape)), ref["dk"])
+    np.testing.assert_array_equal(np_(dv.view(q.shape)), ref["dv"])
+    np.testing.assert_array_equal(np_(dq), ref["dq"])
