@@ -510,7 +510,10 @@ done:
 //   replay  : each chunk from its true initial state (`starts`), writing the
 //             S_t images as the single pass does.
 // =============================================================================
-constexpr int kScanThreads = 192;         // 4 epilogue, 1 copy, 1 MMA warps
+// Warps 0-7 epilogue (two per TMEM lane quadrant, 8 of the block's 16 columns
+// each), warp 8 copies, warp 9 issues the MMAs.
+constexpr int kScanEpiWarps = 8, kScanCopyWarp = 8, kScanMmaWarp = 9;
+constexpr int kScanThreads = 320;
 constexpr int kScanMStage = 2 * 128 * 128;  // M image: 2 atoms x 128 rows x 128 B
 constexpr int kScanBStage = 128 * 64;       // b block: up to 128 rows x 16 floats
 constexpr int kScanImg = 2 * 32 * 128;      // state block image: 2 atoms x 32 rows (hi 0-15, lo 16-31) x 128 B
@@ -580,10 +583,10 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(smem_u32(&full[s]), 1);
-      mbar_init(smem_u32(&empty[s]), 5);  // the MMA's commit + the 4 epilogue warps (b read)
+      mbar_init(smem_u32(&empty[s]), 1 + kScanEpiWarps);  // the MMA's commit + each epilogue warp (b read)
     }
     mbar_init(smem_u32(pfull), 1);
-    mbar_init(smem_u32(sready), 4);  // each epilogue warp, once its rows of the state image are written
+    mbar_init(smem_u32(sready), kScanEpiWarps);  // each epilogue warp, once its part of the state image is written
     mbar_init(smem_u32(mma_done), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -597,7 +600,7 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
     }
   }
   fence_proxy_async_smem();
-  if (warp == 5) {
+  if (warp == kScanMmaWarp) {
     tmem_alloc(smem_u32(tmem_slot), 32);  // P_hi (columns 0-15) and P_lo (16-31)
     tmem_relinquish();
   }
@@ -608,7 +611,7 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
   griddep_wait();  // no global memory is touched before the preceding kernel completes
   griddep_launch_dependents();
 
-  if (warp == 4) {
+  if (warp == kScanCopyWarp) {
     // ---------------- copies in: M_t image (NA atoms of D rows) and the b_t block
     if (lane == 0) {
       Ring<STAGES> r;
@@ -632,7 +635,7 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       }
       r.drain(full);
     }
-  } else if (warp == 5) {
+  } else if (warp == kScanMmaWarp) {
     // ---------------- MMA: P = M_t S_{t-1}[:, J]
     if (lane == 0) {
       const uint32_t id = idesc_bf16(128, 32, 0, 0);
@@ -684,22 +687,24 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       }
     }
   } else {
-    // ---------------- epilogue (4 warps): thread i owns row i of the column block
-    const int i = threadIdx.x;
+    // ---------------- epilogue (8 warps): thread (i, h) owns row i of the column
+    // block, columns 8h .. 8h + 7 (i = 32 (warp % 4) + lane, h = warp / 4; a warp
+    // reads TMEM lanes 32 (warp % 4) ..)
+    const int i = (warp & 3) * 32 + lane, h8 = 8 * (warp >> 2);
     const bool row = i < D;
-    float x[16];
+    float x[8];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) x[j] = (ident && i == 16 * cb + j) ? 1.f : 0.f;
+    for (int j = 0; j < 8; ++j) x[j] = (ident && i == 16 * cb + h8 + j) ? 1.f : 0.f;
     const float* s_init = a.starts ? a.starts + (size_t)(bh * a.nchunks + chunk_id) * D * D
                                    : (a.maps ? nullptr : (a.state_in ? a.state_in + (size_t)bh * D * D : nullptr));
     // (rows past D read nothing, so they check nothing)
     const bool init_ok = !a.starts || !row ||
-                         in_region(((size_t)(bh * a.nchunks + chunk_id) * D * D + (size_t)i * D + 16 * cb + 16) * 4,
+                         in_region(((size_t)(bh * a.nchunks + chunk_id) * D * D + (size_t)i * D + 16 * cb + h8 + 8) * 4,
                                    a.starts_span, a.status);
     if (row && s_init && init_ok) {
-      const float4* si = reinterpret_cast<const float4*>(s_init + (size_t)i * D + 16 * cb);
+      const float4* si = reinterpret_cast<const float4*>(s_init + (size_t)i * D + 16 * cb + h8);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         const float4 w = si[q];
         x[4 * q] = w.x;
         x[4 * q + 1] = w.y;
@@ -708,9 +713,10 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       }
     }
     if (row && a.reverse && T > 0) {  // U_{T-1} = dS_T + E_{T-1}
-      const float4* e = reinterpret_cast<const float4*>(a.b_blk + (((size_t)(bh * T + T - 1) * ncb + cb) * D + i) * 16);
+      const float4* e =
+          reinterpret_cast<const float4*>(a.b_blk + (((size_t)(bh * T + T - 1) * ncb + cb) * D + i) * 16 + h8);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
+      for (int q = 0; q < 2; ++q) {
         const float4 w = e[q];
         x[4 * q] += w.x;
         x[4 * q + 1] += w.y;
@@ -724,13 +730,13 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       if (!row) return;
       uint8_t* at = im + (i >> 6) * (32 * 128);
 #pragma unroll
-      for (int n = 0; n < 16; n += 2) {
+      for (int n = 0; n < 8; n += 2) {
         uint32_t hv, lv;
         split2(x[n], x[n + 1], hv, lv);
-        *reinterpret_cast<uint16_t*>(at + sw128_off(n, i & 63)) = (uint16_t)(hv & 0xFFFF);
-        *reinterpret_cast<uint16_t*>(at + sw128_off(n + 1, i & 63)) = (uint16_t)(hv >> 16);
-        *reinterpret_cast<uint16_t*>(at + sw128_off(16 + n, i & 63)) = (uint16_t)(lv & 0xFFFF);
-        *reinterpret_cast<uint16_t*>(at + sw128_off(17 + n, i & 63)) = (uint16_t)(lv >> 16);
+        *reinterpret_cast<uint16_t*>(at + sw128_off(h8 + n, i & 63)) = (uint16_t)(hv & 0xFFFF);
+        *reinterpret_cast<uint16_t*>(at + sw128_off(h8 + n + 1, i & 63)) = (uint16_t)(hv >> 16);
+        *reinterpret_cast<uint16_t*>(at + sw128_off(16 + h8 + n, i & 63)) = (uint16_t)(lv & 0xFFFF);
+        *reinterpret_cast<uint16_t*>(at + sw128_off(17 + h8 + n, i & 63)) = (uint16_t)(lv >> 16);
       }
     };
     write_img(img);  // the initial state into buffer 0
@@ -742,6 +748,7 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
     const bool relu_lin = a.variant == kReluLinear;  // g = 1, no delta-rule term
     // raw decay of the next step's frame; mapped when used
     float gnext = (nsteps > 0 && !relu_lin) ? __ldg(a.g + bh * T + (a.reverse ? T - 1 : t0)) : 0.f;
+    const uint32_t tl = tmem + ((uint32_t)((warp & 3) * 32) << 16) + h8;
     for (int j = 0; j < nsteps; ++j) {  // j counts steps; the step's frame is fr
       const int fr = a.reverse ? T - 1 - j : t0 + j;
       const long long f = bh * T + fr;
@@ -752,16 +759,16 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
                       wait_or_abort(smem_u32(&full[stage]), phase, abort_flag, a.status);
       if (__all_sync(0xffffffffu, ok)) {
         tc_fence_after();
-        float p[16], pl[16];
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16), p);
-        tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + 16, pl);
-        float bv[16];
+        float p[8], pl[8];
+        tmem_ld8(tl, p);
+        tmem_ld8(tl + 16, pl);
+        float bv[8];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) bv[q] = 0.f;
+        for (int q = 0; q < 8; ++q) bv[q] = 0.f;
         if (row && use_b) {
-          const float4* bp = reinterpret_cast<const float4*>(bring + stage * kScanBStage + i * 64);
+          const float4* bp = reinterpret_cast<const float4*>(bring + stage * kScanBStage + i * 64 + h8 * 4);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
+          for (int q = 0; q < 2; ++q) {
             const float4 w = bp[q];
             bv[4 * q] = w.x;
             bv[4 * q + 1] = w.y;
@@ -775,11 +782,11 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
         if (lane == 0) mbar_arrive(smem_u32(&empty[stage]));
         if (row) {
 #pragma unroll
-          for (int jj = 0; jj < 16; ++jj)
+          for (int jj = 0; jj < 8; ++jj)
             x[jj] = relu_lin ? x[jj] + bv[jj] : fmaf(gt, x[jj] - (p[jj] + pl[jj]), add_b ? bv[jj] : 0.f);
         }
         // S_j goes into the buffer of S_{j-3}, whose store has read it (the MMA
-        // thread waited for that before committing pfull(j)).
+        // thread waited for that before issuing step j's MMAs).
         write_img(img + ((j + 1) % kScanImgBufs) * kScanImg);
         fence_proxy_async_smem();
       }
@@ -789,27 +796,28 @@ __global__ void __launch_bounds__(kScanThreads, (STAGES <= 2 ? 2 : 1)) tc_scan_k
       if (lane == 0) mbar_arrive(smem_u32(sready));
     }
     if (row && a.maps) {
-      const size_t mo_end = ((size_t)(bh * a.nchunks + chunk_id) * D + i) * 2 * D + (ident ? 0 : D) + 16 * cb + 16;
-      float4* mo = reinterpret_cast<float4*>(a.maps + mo_end - 16);
+      const size_t mo_end =
+          ((size_t)(bh * a.nchunks + chunk_id) * D + i) * 2 * D + (ident ? 0 : D) + 16 * cb + h8 + 8;
+      float4* mo = reinterpret_cast<float4*>(a.maps + mo_end - 8);
       if (in_region(mo_end * 4, a.maps_span, a.status)) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) mo[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        for (int q = 0; q < 2; ++q) mo[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
       }
     } else if (row && a.state_out && chunk_id == a.nchunks - 1) {
-      float4* so = reinterpret_cast<float4*>(a.state_out + ((size_t)bh * D + i) * D + 16 * cb);
+      float4* so = reinterpret_cast<float4*>(a.state_out + ((size_t)bh * D + i) * D + 16 * cb + h8);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) so[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+      for (int q = 0; q < 2; ++q) so[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
     }
   }
 done:
-  if (warp == 5 && lane == 0) {
+  if (warp == kScanMmaWarp && lane == 0) {
     bulk_wait0();  // state block stores complete
     mma_commit(smem_u32(mma_done));
     wait_bounded(smem_u32(mma_done), 0, 500000000ull);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kScanMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 32);
   }
