@@ -67,9 +67,18 @@ def bench_cmd(args, steps=2, warmup=3) -> list:
     return cmd
 
 
+def shown(cmd) -> str:
+    """The command as run from the repository root (interpreter and paths relative)."""
+    out = []
+    for c in cmd:
+        c = "python" if c == sys.executable else c
+        out.append(os.path.relpath(c, ROOT) if os.path.isabs(c) and c.startswith(ROOT + os.sep) else c)
+    return shlex.join(out)
+
+
 def run(cmd, log) -> int:
     with open(log, "w") as f:
-        f.write("$ " + shlex.join(cmd) + "\n")
+        f.write("$ " + shown(cmd) + "\n")
         f.flush()
         return subprocess.run(cmd, stdout=f, stderr=subprocess.STDOUT, cwd=ROOT).returncode
 
@@ -112,14 +121,15 @@ def launches(args) -> str:
     for r in rows[1:]:
         if len(r) <= iv:
             continue
-        scale = {"nsecond": 1e-3, "usecond": 1.0, "msecond": 1e3, "second": 1e6}.get(r[iu], 1.0)
+        scale = {"nsecond": 1e-3, "ns": 1e-3, "usecond": 1.0, "us": 1.0, "msecond": 1e3, "ms": 1e3,
+                 "second": 1e6, "s": 1e6}[r[iu]]
         name = r[ik].split("(")[0].split("<")[0]
         name = name.split("::")[-1]
         n, tot = per.get(name, (0, 0.0))
         per[name] = (n + 1, tot + num(r[iv]) * scale)
     total = sum(t for _, t in per.values())
     lines = [f"# Launch list: {args.workload} workload, mode {args.mode}{' (backward)' if args.backward else ''}",
-             "", "Command (plain run first, exit 0, then):", "", "```", shlex.join(ncu_cmd), "```", "",
+             "", "Command (plain run first, exit 0, then):", "", "```", shown(ncu_cmd), "```", "",
              "Per-launch times are cold-cache and serialised under ncu: compare shares, not absolutes.", "",
              "| kernel | launches | total µs | share |", "|---|---|---|---|"]
     for name, (n, t) in sorted(per.items(), key=lambda kv: -kv[1][1]):
@@ -131,7 +141,7 @@ def capture(args):
     cmd = bench_cmd(args)
     rep = os.path.join(args.out, f"counters_{args.kernel}_{args.workload}{args.frames or ''}")
     ncu_cmd = [NCU, "--clock-control", "none", "-k", f"regex:^{args.kernel}", "-s", str(args.skip), "-c",
-               str(args.count)]
+               str(args.count), "--metrics", "dram__bytes_read.sum,dram__bytes_write.sum"]
     for sec in SECTIONS:
         ncu_cmd += ["--section", sec]
     ncu_cmd += ["-o", rep, "-f"] + cmd
@@ -146,7 +156,7 @@ def counters(args) -> str:
     ncu_cmd, hdr, unit, vals = capture(args)
     lines = [f"# ncu counters: {args.kernel}, {args.workload} workload"
              f"{f', first {args.frames} frames' if args.frames else ''}", "",
-             "Command (plain run first, exit 0, then):", "", "```", shlex.join(ncu_cmd), "```", "",
+             "Command (plain run first, exit 0, then):", "", "```", shown(ncu_cmd), "```", "",
              "| counter | " + " | ".join(f"launch {i}" for i in range(len(vals))) + " |",
              "|---|" + "---|" * len(vals)]
     for c in COUNTERS:
@@ -176,7 +186,7 @@ def traffic(args) -> str:
     full = small * scale
     line = f"{args.kernel} {full:.0f} {bench.csrc_hash()} {args.workload}"
     return (f"# DRAM traffic of {args.kernel}, {args.workload} workload\n\nCommand (plain run first, exit 0, then):"
-            f"\n\n```\n{shlex.join(ncu_cmd)}\n```\n\nDRAM bytes (read + write) per launch on the first "
+            f"\n\n```\n{shown(ncu_cmd)}\n```\n\nDRAM bytes (read + write) per launch on the first "
             f"{args.frames} frames: {small:.4g}; scaled x{scale:.3f} by frame-heads to the full workload: "
             f"{full:.4g}\n\nprofiles/ncu_traffic.txt line:\n\n    {line}\n")
 
