@@ -310,3 +310,21 @@ def test_large_sequential_and_prefix_agree():
     assert beyond / rms_o <= parity.BF16_MAX_ABS_OVER_RMS
     assert rms_d / rms_o <= parity.BF16_RMS_ERR_OVER_RMS
     assert d_s / rms_s <= parity.BF16_MAX_ABS_OVER_RMS
+
+
+# (H, T, S): frame-head counts just below, at and above one and two rounds of the
+# 148 persistent CTAs, token counts giving 1, 3 and 7 read-out tiles (the last one
+# ragged), so the read-out's round-robin phase, its balanced tail and the
+# boundary between them all run
+ROUNDS = [(7, 21, 300), (4, 37, 129), (1, 149, 880), (3, 99, 250), (9, 33, 64), (2, 74, 700)]
+
+
+@pytest.mark.parametrize("case", ROUNDS, ids=lambda c: "-".join(map(str, c)))
+def test_readout_work_split_over_frame_head_counts(case):
+    H, T, S = case
+    wl = synth.WORKLOADS["short"].with_(H=H, T=T, S=S, D=64, seed=7300 + H * T)
+    x = synth.full(wl)
+    out, st = run(*parity.upload(wl, x), mode=0)
+    ro, rs = oracle.frame_fwd(x["q"], x["k"], x["v"], x["g"], x["beta"])
+    eo, es = parity.assert_parity("bf16", np_(out), ro, np_(st), rs, f"read-out split {case}")
+    print(f"read-out split {case} (F = {H * T}): out {eo} state {es}")
