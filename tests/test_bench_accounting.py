@@ -48,3 +48,19 @@ def test_backward_work():
     fh = wl.B * wl.H * wl.T
     assert bench.kernel_alg_bytes("tc_bwd_kv_grad", wl) == fh * (4 * wl.S * wl.D * 2 + 8 * wl.S + 4)
     assert bench.kernel_alg_bytes("tc_bwd_q_grad", wl) == fh * 2 * wl.S * wl.D * 2
+
+
+def test_link_bound_reduces_to_the_textbook_cases():
+    # full duplex (each direction keeps its rate): the slower direction alone
+    full = {"h2d_gbs": 50.0, "d2h_gbs": 40.0, "duplex_h2d_gbs": 50.0, "duplex_d2h_gbs": 40.0}
+    assert abs(bench.link_bound_ms(10e9, 4e9, full) - 200.0) < 1e-9  # 10 GB at 50 GB/s
+    assert abs(bench.link_bound_ms(1e9, 8e9, full) - 200.0) < 1e-9   # 8 GB at 40 GB/s
+    # half duplex (the directions split one link): the bytes add up
+    half = {"h2d_gbs": 50.0, "d2h_gbs": 50.0, "duplex_h2d_gbs": 25.0, "duplex_d2h_gbs": 25.0}
+    assert abs(bench.link_bound_ms(3e9, 2e9, half) - 100.0) < 1e-9
+    # one direction only
+    assert abs(bench.link_bound_ms(5e9, 0.0, half) - 100.0) < 1e-9
+    # in between (as measured on one B300 host): between the two extremes
+    meas = {"h2d_gbs": 55.6, "d2h_gbs": 57.3, "duplex_h2d_gbs": 37.4, "duplex_d2h_gbs": 54.4}
+    b = bench.link_bound_ms(11.43e9, 3.79e9, meas)
+    assert 11.43e9 / 55.6e6 < b < 11.43e9 / 55.6e6 + 3.79e9 / 57.3e6
