@@ -16,7 +16,7 @@ bench times), each preceded by the same command without ncu, which must exit 0:
             bench.py reads from profiles/ncu_traffic.txt.
 
 Every ncu command carries ``--clock-control none`` (the GPU's clocks are left as
-they are).  Raw reports and CSVs go to ``--out`` (default gpurun_out/); the
+they are).  Raw reports and CSVs go to ``--out`` (default ncu_out/); the
 markdown summary, headed by the exact commands, is printed and written beside
 them.
 
@@ -203,7 +203,7 @@ def main():
     ap.add_argument("--frames", type=int, default=None, help="first N frames only (counters, traffic)")
     ap.add_argument("--skip", type=int, default=3, help="launches of the kernel skipped before capturing")
     ap.add_argument("--count", type=int, default=1, help="launches captured (counters, traffic; at most 2)")
-    ap.add_argument("--out", default=os.path.join(ROOT, "gpurun_out"))
+    ap.add_argument("--out", default=os.path.join(ROOT, "ncu_out"))
     args = ap.parse_args()
     if args.what != "launches" and args.frames is None:
         args.frames = 128  # a small case: a few GB on the device, larger than L2
