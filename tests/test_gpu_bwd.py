@@ -58,6 +58,8 @@ CASES = [
     ("bf16", 1, 1, 3, 200, 96, True, True),
     ("bf16", 1, 1, 2, 1, 16, False, True),
     ("bf16", 1, 1, 17, 31, 80, True, False),
+    ("bf16", 1, 2, 4, 150, 128, True, True),
+    ("bf16", 2, 1, 3, 257, 32, False, True),
 ]
 
 
